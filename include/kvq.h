@@ -1,0 +1,211 @@
+/*
+ * kvq.h -- C ABI of libkvq: an FP4 (E2M1 codes, one E4M3 scale per 16
+ * channels) key/value cache, an FP8 E4M3 sliding-window cache beside it, and
+ * the split-K decode attention that reads both back.
+ *
+ * Sources (page title, section):
+ *   "Quantising the KV cache", section "Code": the block quantiser
+ *       (s = RNE_e4m3(amax/6) saturating, s == 0 -> E4M3 min subnormal 2^-9,
+ *       codes = RNE_e2m1(v/s) saturating) and the place of the quantised K/V
+ *       between projection and an unchanged attention.
+ *   "Quantising the KV cache", section "FP4 with a fine-grained scale" and
+ *       section "Maths": E2M1 with an E4M3 scale per 16 costs 4.5 bits/number.
+ *   "Quantising the KV cache", section "Concept": decode reads the whole cache
+ *       for every new token, so decode time is mostly spent reading it.
+ *   "KV Cache Quantisation", section "Common questions": the win holds only if
+ *       the attention kernel handles the scales and dequantisation itself.
+ *   "Week 6 -- FP4 KV Caches and Bounded Replay", "Overview": global KV goes
+ *       ~4-bit, sliding-window (SWA) KV stays FP8.
+ *
+ * Conventions shared by every entry point
+ *   - All pointers named d_* or documented as "device" are CUDA device memory
+ *     owned by the caller.  The library allocates nothing and keeps no global
+ *     state; calls on different streams with disjoint buffers are independent.
+ *   - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).  The return value reports only host-side
+ *     argument checks and launch errors:
+ *       KVQ_ERR_INVALID_ARGUMENT  a size, pointer or layout is invalid; nothing
+ *                                 was enqueued.
+ *       KVQ_ERR_UNSUPPORTED       valid but outside what the kernels handle
+ *                                 (e.g. head_dim not 64/128 in decode); nothing
+ *                                 was enqueued.
+ *       KVQ_ERR_WORKSPACE         workspace too small; nothing was enqueued.
+ *       KVQ_ERR_CUDA              a CUDA call or launch failed.
+ *   - Data-dependent problems found on the device set bits (atomicOr) in the
+ *     caller's int32 device word `d_err_flag` (may be NULL: then they are not
+ *     reported).  Kernels never trap or assert; the offending element is
+ *     skipped (append, dequant) or contributes nothing (decode).  Read the flag
+ *     after synchronising the stream.
+ *   - Key/value inputs are bf16; query heads h use kv head h / (Hq / Hkv).
+ *
+ * FP4 paged cache layout (format KVQ_FORMAT_FP4_E2M1_E4M3_G16), per K and V:
+ *   codes : uint8 [num_pages][num_kv_heads][page_size][head_dim/2]
+ *           byte j of a 16-channel block holds channel 2j in its low nibble,
+ *           channel 2j+1 in its high nibble; nibble = sign<<3 | E2M1 magnitude
+ *           (0..7 -> 0, .5, 1, 1.5, 2, 3, 4, 6); the sign of zero is kept.
+ *   scales: uint8 [num_pages][num_kv_heads][page_size][head_dim/16], one E4M3FN
+ *           byte per block (never 0x00: an all-zero block stores 0x01).
+ *   Position p of sequence b lives in page page_table[b*max_pages_per_seq +
+ *   p/page_size], slot p % page_size.  With page_table == NULL the cache is
+ *   contiguous: page p/page_size of sequence b is b*max_pages_per_seq +
+ *   p/page_size.
+ *
+ * FP8 window cache layout (format KVQ_FORMAT_FP8_E4M3_HEAD), per K and V:
+ *   codes : uint8 [num_pages][num_kv_heads][page_size][head_dim], one E4M3FN
+ *           byte per value; here num_pages counts rings (one per sequence b)
+ *           and page_size is the window length W: position p of sequence b
+ *           lives in slot p % W of ring b.
+ *   scales: float [num_kv_heads], one fp32 scale per kv head (K and V apart):
+ *           value = fp32(E4M3(code) * scale).
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ_VERSION 1
+
+typedef enum kvq_status {
+    KVQ_OK = 0,
+    KVQ_ERR_INVALID_ARGUMENT = 1,
+    KVQ_ERR_UNSUPPORTED = 2,
+    KVQ_ERR_WORKSPACE = 3,
+    KVQ_ERR_CUDA = 4
+} kvq_status;
+
+/* Bits OR-ed into *d_err_flag by the kernels. */
+#define KVQ_FLAG_NONFINITE 0x1 /* a key/value/query input held Inf or NaN */
+#define KVQ_FLAG_PAGE_OOB 0x2  /* a page id outside [0, num_pages) or a page index
+                                  outside [0, max_pages_per_seq) */
+#define KVQ_FLAG_TIMEOUT 0x4   /* a bounded wait inside a kernel gave up (~2 s) */
+#define KVQ_FLAG_BAD_LENGTH 0x8 /* a negative sequence length or start position */
+
+typedef enum kvq_format {
+    KVQ_FORMAT_FP4_E2M1_E4M3_G16 = 1,
+    KVQ_FORMAT_FP8_E4M3_HEAD = 2
+} kvq_format;
+
+typedef struct kvq_stream_opaque *kvq_stream; /* a cudaStream_t */
+
+/* Description of one cache (K and V of one layer).  All buffers are device
+ * memory owned by the caller; see the layouts above. */
+typedef struct kvq_cache {
+    int32_t format;            /* kvq_format */
+    int32_t num_kv_heads;      /* Hkv >= 1 */
+    int32_t head_dim;          /* multiple of 16, <= 512 */
+    int32_t page_size;         /* FP4: tokens per page, one of 16, 32, 64, 128, 256;
+                                  FP8: window length W, 1..1024 */
+    int64_t num_pages;         /* FP4: pages in the pool; FP8: number of rings */
+    int32_t max_pages_per_seq; /* FP4: row length of page_table (or pages per
+                                  sequence when contiguous); FP8: ignored */
+    int32_t reserved;          /* must be 0 */
+    const int32_t *page_table; /* FP4: device int32 [batch][max_pages_per_seq] or NULL;
+                                  FP8: must be NULL */
+    void *k_codes;             /* device, see layouts */
+    void *v_codes;
+    void *k_scales;            /* FP4: uint8 E4M3 per block; FP8: float [Hkv] */
+    void *v_scales;
+} kvq_cache;
+
+/*
+ * kvq_append -- quantise n_new new tokens per sequence into `cache`.
+ * ("Quantising the KV cache", section "Code": per 16-channel block, scale
+ * RNE_e4m3(amax/6) saturating with 0 -> 2^-9, codes RNE_e2m1(v/s) saturating,
+ * IEEE fp32 divisions; FP8 caches: code RNE_e4m3(x / s_h) saturating.)
+ *   cache       FP4 or FP8 cache (an FP8 cache needs its scales set first,
+ *               e.g. by kvq_fp8_set_scales).
+ *   batch       number of sequences (rows of page_table / rings), >= 0.
+ *   n_new       new tokens per sequence, >= 0.
+ *   d_start_pos device int32 [batch]: position of each sequence's first new
+ *               token; token t goes to position d_start_pos[b] + t.
+ *   k, v        device bf16 [batch][n_new][num_kv_heads][head_dim], contiguous.
+ * Device flags: NONFINITE (the block's codes and scale are whatever the
+ * conversion produces), PAGE_OOB (token skipped), BAD_LENGTH (negative start;
+ * sequence skipped).
+ */
+kvq_status kvq_append(const kvq_cache *cache, int32_t batch, int32_t n_new,
+                      const int32_t *d_start_pos, const void *k, const void *v,
+                      int32_t *d_err_flag, kvq_stream stream);
+
+/*
+ * kvq_fp8_set_scales -- set an FP8 window cache's per-head scales from a
+ * calibration set of tokens: s_h = amax / 448 in fp32 over every value of kv
+ * head h in k (resp. v), 1 where amax == 0.  ("Week 6 -- FP4 KV Caches and
+ * Bounded Replay": SWA KV stays FP8; "Quantising the KV cache" table row
+ * "FP8 E4M3, one scale per tensor", here one scale per head.)
+ *   k, v   device bf16 [batch][n][num_kv_heads][head_dim].
+ * Writes cache->k_scales and cache->v_scales (float [Hkv]).  Device flags:
+ * NONFINITE.
+ */
+kvq_status kvq_fp8_set_scales(const kvq_cache *cache, int32_t batch, int32_t n,
+                              const void *k, const void *v, int32_t *d_err_flag,
+                              kvq_stream stream);
+
+/*
+ * kvq_decode_workspace_bytes -- bytes of device workspace kvq_decode_attn
+ * needs for these sizes on the current device (it depends on the device's SM
+ * count).  Returns 0 for invalid sizes.
+ */
+size_t kvq_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim);
+
+/*
+ * kvq_decode_attn -- one decode step of attention for every sequence and
+ * query head, reading keys and values from the FP4 cache (dequantised in the
+ * kernel) and, when `swa` is given, the last min(W, T) positions from the FP8
+ * window cache instead; one softmax over the union.  ("Quantising the KV
+ * cache", section "Code": quantised K/V feed an unchanged attention;
+ * "Concept": decode reads the whole cache.)
+ *   out[b][h][:] = sum_t softmax_t(softmax_scale * q[b][h] . K^[b][t]) V^[b][t]
+ *   global       FP4 cache, head_dim 64 or 128, page_size 16..256.
+ *   swa          FP8 window cache with the same num_kv_heads/head_dim, or NULL.
+ *   batch        sequences, >= 1.
+ *   num_q_heads  Hq, a multiple of num_kv_heads with Hq/Hkv <= 8.
+ *   d_seq_lens   device int32 [batch]: T_b, positions 0..T_b-1 are attended
+ *                (T_b == 0 gives a zero output row).
+ *   q            device bf16 [batch][num_q_heads][head_dim].
+ *   softmax_scale scale applied to q.k (usually 1/sqrt(head_dim)), > 0.
+ *   out          device float [batch][num_q_heads][head_dim].
+ *   workspace    device scratch of at least kvq_decode_workspace_bytes(...)
+ *                bytes, 16-byte aligned; needs no initialisation; must not be
+ *                shared by calls that may run concurrently.
+ * Device flags: PAGE_OOB (the page's tokens are left out), BAD_LENGTH,
+ * TIMEOUT.
+ */
+kvq_status kvq_decode_attn(const kvq_cache *global, const kvq_cache *swa, int32_t batch,
+                           int32_t num_q_heads, const int32_t *d_seq_lens, const void *q,
+                           float softmax_scale, float *out, void *workspace,
+                           size_t workspace_bytes, int32_t *d_err_flag, kvq_stream stream);
+
+/*
+ * kvq_dequant -- expand a cache to dense values (value = E2M1(code) * E4M3(s)
+ * for FP4, exact in fp32 and bf16; fp32(E4M3(code) * s_h) for FP8).
+ * ("Quantising the KV cache", section "Code": the dequantised value is the
+ * code times its scale.)
+ *   FP4: k_out, v_out [batch][max_len][num_kv_heads][head_dim]; positions
+ *        >= d_seq_lens[b] are written as 0.
+ *   FP8: max_len must equal the window W; the rings are written in slot order
+ *        [batch][W][num_kv_heads][head_dim] and d_seq_lens is ignored (NULL ok).
+ *   out_dtype 0 = float32, 1 = bfloat16.
+ * Device flags: PAGE_OOB, BAD_LENGTH.
+ */
+kvq_status kvq_dequant(const kvq_cache *cache, int32_t batch, const int32_t *d_seq_lens,
+                       int32_t max_len, int32_t out_dtype, void *k_out, void *v_out,
+                       int32_t *d_err_flag, kvq_stream stream);
+
+/* A static, human-readable name for a status code. */
+const char *kvq_status_string(kvq_status status);
+
+/* KVQ_VERSION of the built library. */
+int32_t kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */
