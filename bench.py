@@ -1,0 +1,439 @@
+#!/usr/bin/env python3
+"""Decode-attention throughput on the FP4 KV cache (one JSON line on rank 0).
+
+A step is one pass of the hot path over the long_context workload (B32,
+Hkv8, Hq64, d128, context 32768, one layer): append one new bf16 token per
+sequence into the FP4 cache (quantise-on-append), then split-K decode
+attention of 64 query heads per sequence over the cache (dequantised in the
+kernel) and the cross-split merge.  The appended position cycles through the
+64 slots after the prefilled context, so every step attends 32769..32832
+positions.  `value` is KV-tokens/s (one KV-token = one cached position of one
+sequence across all kv heads, K and V) over the timed steps; inputs are
+resident in HBM and the 1.2 GB cache is far larger than L2.
+
+--impl reference times the CPU oracle (plain C, fp64 attention over the
+dequantised cache) on the host cores on a bounded sample of the same step.
+Under torchrun every rank runs an independent replica (weak scaling, no
+data-path collective); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import math
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from fp4_kv_cache_kvq_gb300 import workloads  # noqa: E402
+
+METRIC = "decode-attn KV-tokens/s and achieved HBM GB/s (% of ~8 TB/s) on FP4 cache, 1xGB300"
+UNIT = "KV-tokens/s"
+CYCLE = 64          # appended positions cycle through this many slots after the context
+NQ = 8              # distinct query sets cycled through the steps
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SRC = os.path.join(ROOT, "fp4_kv_cache_kvq_gb300", "csrc", "kvq_decode.cu")
+PROFILE = os.path.join(ROOT, "profiles", "decode_fp4_long_context.md")
+
+
+# ----------------------------------------------------------------- distributed plumbing
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def _dev(self):
+        return torch.device("cuda", self.local) if (self.pg and self.pg.get_backend() == "nccl") else "cpu"
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def reduce(self, x: float, op: str) -> float:
+        if not self.pg:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=self._dev())
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX if op == "max" else self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def combine_ranks(dist: Dist, units: float, seconds: float):
+    """Whole-job throughput: units summed over ranks / max time over ranks."""
+    total_units = dist.reduce(units, "sum")
+    max_s = dist.reduce(seconds, "max")
+    return total_units / max_s, max_s
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        exe = shutil.which("nvidia-smi")
+        if exe is None:
+            return
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        self.proc = subprocess.Popen([exe, f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                      "-i", str(device_index), "-lms", "200"],
+                                     stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.strip()]
+        os.unlink(self.path)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = max(mx, float(r[2]))
+                for i, n in enumerate(names):
+                    if r[5 + i].strip().lower().startswith("active"):
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- helpers
+def measured_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode source (else None)."""
+    try:
+        text = open(PROFILE).read()
+        sha = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()
+        fields = dict(line.split(":", 1) for line in text.splitlines() if line.startswith(("traffic_", "source_")))
+        if fields.get("source_sha256", "").strip() != sha:
+            return None
+        return int(float(fields["traffic_bytes_per_launch"].strip()))
+    except Exception:
+        return None
+
+
+def fp4_bytes_per_token(w) -> int:
+    """FP4 cache bytes of one KV-token: K and V, all kv heads, codes + scales."""
+    return 2 * w.num_kv_heads * (w.head_dim // 2 + w.head_dim // 16)
+
+
+class Setup:
+    """The resident FP4 cache of a workload plus the per-step inputs."""
+
+    def __init__(self, w, seed: int, device):
+        from fp4_kv_cache_kvq_gb300 import kvq
+        self.w = w
+        self.kvq = kvq
+        self.lens0 = workloads.lengths(w, seed)
+        table, num_pages, max_pages = workloads.page_layout(w, self.lens0, reserve=CYCLE, seed=seed)
+        self.table = table.to(device) if table is not None else None
+        self.cache = kvq.Fp4Cache(w.num_kv_heads, w.head_dim, w.page_size, num_pages, max_pages,
+                                  page_table=self.table, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        zero = torch.zeros(1, dtype=torch.int32, device=device)
+        for b, n in enumerate(self.lens0):
+            k, v = workloads.sequence_kv(w, b, n, seed=seed, device=device)
+            row = self.table[b:b + 1] if self.table is not None else torch.arange(
+                b * max_pages, (b + 1) * max_pages, dtype=torch.int32, device=device)[None]
+            kvq.append(self.cache, zero, k[None], v[None], err=self.err, page_table=row)
+            del k, v
+        toks = [workloads.step_tokens(w, i, seed=seed, device=device) for i in range(CYCLE)]
+        self.k_new = [t[0] for t in toks]
+        self.v_new = [t[1] for t in toks]
+        self.q = [workloads.queries(w, seed=seed, step=i, device=device) for i in range(NQ)]
+        base = torch.tensor(self.lens0, dtype=torch.int32, device=device)
+        self.pos = [base + i for i in range(CYCLE)]
+        self.lens = [base + i + 1 for i in range(CYCLE)]
+        self.kv_tokens = [sum(self.lens0) + (i + 1) * w.batch for i in range(CYCLE)]
+        self.scale = 1.0 / math.sqrt(w.head_dim)
+        B, Hq, D = w.batch, w.num_q_heads, w.head_dim
+        self.out = torch.empty((B, Hq, D), dtype=torch.float32, device=device)
+        nbytes = kvq.decode_workspace_bytes(B, Hq, w.num_kv_heads, D)
+        self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+        torch.cuda.synchronize()
+
+    def step(self, i: int, q=None, k=None, v=None, ev=None):
+        s = i % CYCLE
+        kvq = self.kvq
+        kvq.append(self.cache, self.pos[s], self.k_new[s] if k is None else k, self.v_new[s] if v is None else v,
+                   err=self.err)
+        if ev is not None:
+            ev[0].record()
+        kvq.decode_attn(self.cache, self.lens[s], self.q[i % NQ] if q is None else q, self.scale, out=self.out,
+                        workspace=self.ws, err=self.err)
+        if ev is not None:
+            ev[1].record()
+        return self.kv_tokens[s]
+
+    def decode_algorithmic_bytes(self, i: int) -> int:
+        w = self.w
+        s = i % CYCLE
+        b = self.kv_tokens[s] * fp4_bytes_per_token(w)
+        b += w.batch * w.num_q_heads * w.head_dim * (2 + 4)  # q in, out
+        b += w.batch * 4                                      # lengths
+        if self.table is not None:
+            b += sum(-(-(n + s + 1) // w.page_size) for n in self.lens0) * 4
+        return b
+
+
+# ----------------------------------------------------------------- GPU arm
+def run_gpu(args, dist: Dist):
+    device = torch.device("cuda", dist.local)
+    torch.cuda.set_device(device)
+    from fp4_kv_cache_kvq_gb300 import build
+    build.build()
+    w = workloads.WORKLOADS[args.workload]
+    st = Setup(w, args.seed, device)
+    K, Wm = args.steps, args.warmup
+    for i in range(Wm):
+        st.step(i)
+    torch.cuda.synchronize()
+    if st.err.item() != 0:
+        raise RuntimeError(f"device error flag {st.err.item()} during warm-up")
+
+    # ---- device-resident timing
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(device.index)
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0.record()
+    tokens = 0
+    for i in range(K):
+        tokens += st.step(Wm + i, ev=evs[i])
+    t1.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    elapsed_s = t0.elapsed_time(t1) / 1e3
+    decode_ms = [a.elapsed_time(b) for a, b in evs]
+    if st.err.item() != 0:
+        raise RuntimeError(f"device error flag {st.err.item()} during the timed steps")
+    value, max_s = combine_ranks(dist, tokens, elapsed_s)
+    dec_bytes = statistics.mean(st.decode_algorithmic_bytes(Wm + i) for i in range(K))
+    dec_s = statistics.mean(decode_ms) / 1e3
+    achieved = dec_bytes / dec_s / 1e9
+    peak, peak_src = measured_hbm_peak()
+    # append: read the new bf16 K and V, write their codes and scales
+    append_bytes = w.batch * (2 * w.num_kv_heads * w.head_dim * 2 + fp4_bytes_per_token(w))
+    step_bytes = dec_bytes + append_bytes
+
+    # ---- end to end through the public API with pinned host buffers
+    Ke = min(K, max(50, K // 4))
+    q_host = [q.cpu().pin_memory() for q in st.q]
+    k_host = [k.cpu().pin_memory() for k in st.k_new]
+    v_host = [v.cpu().pin_memory() for v in st.v_new]
+    out_host = torch.empty(st.out.shape, dtype=torch.float32).pin_memory()
+    q_dev, k_dev, v_dev = torch.empty_like(st.q[0]), torch.empty_like(st.k_new[0]), torch.empty_like(st.v_new[0])
+    torch.cuda.synchronize()
+    dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    e2e_tokens = 0
+    for i in range(Ke):
+        s = (Wm + i) % CYCLE
+        q_dev.copy_(q_host[(Wm + i) % NQ], non_blocking=True)
+        k_dev.copy_(k_host[s], non_blocking=True)
+        v_dev.copy_(v_host[s], non_blocking=True)
+        e2e_tokens += st.step(Wm + i, q=q_dev, k=k_dev, v=v_dev)
+        out_host.copy_(st.out, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    e2e_value, _ = combine_ranks(dist, e2e_tokens, e0.elapsed_time(e1) / 1e3)
+    h2d = q_dev.numel() * 2 + k_dev.numel() * 2 + v_dev.numel() * 2
+    d2h = out_host.numel() * 4
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": K, "warmup": Wm,
+        "ms_per_step": max_s * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.description}; step = append 1 token/seq + decode attention",
+                   "batch": w.batch, "kv_heads": w.num_kv_heads, "q_heads": w.num_q_heads,
+                   "head_dim": w.head_dim, "context": w.context, "page_size": w.page_size,
+                   "cache_bytes": st.cache.nbytes, "l2": "inputs larger than L2 (FP4 cache >> 129 MB), no flush",
+                   "parallelism": f"replicas x{dist.world}"},
+        "hbm_gbs_step": step_bytes * K / elapsed_s / 1e9,
+        "hbm_gbs_decode": achieved,
+        "hbm_pct_of_8tbs_decode": 100.0 * achieved / 8000.0,
+        "roofline": {"bound": "hbm", "kernel": "kvq_decode_attn (split-K decode + merge launches)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": peak_src, "traffic": profiled_traffic(),
+                     "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_s * 1e3},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": Ke},
+        "gpu_launches": 3 * K,
+    }
+    if clk is not None:
+        result["clocks"] = clk
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, args.seed, st, budget_s=args.cpu_budget)
+    return result
+
+
+# ----------------------------------------------------------------- CPU oracle (baseline / reference arm)
+class OracleSample:
+    """Host copies of some (sequence, kv head) units of the workload, already
+    quantised by the oracle (the cache is resident state, not step work)."""
+
+    def __init__(self, w, seed: int, n_units: int, max_tokens=None, device="cpu"):
+        import numpy as np
+
+        import oracle
+        self.o = oracle
+        self.w = w
+        rng = np.random.default_rng(seed + 99)
+        lens = workloads.lengths(w, seed)
+        self.units = []
+        for _ in range(n_units):
+            b = int(rng.integers(0, w.batch))
+            h = int(rng.integers(0, w.num_kv_heads))
+            T = lens[b] if max_tokens is None else min(lens[b], max_tokens)
+            k, v = workloads.sequence_kv(w, b, lens[b], seed=seed, device=device)
+            kh = k[:T, h].float().cpu().numpy()
+            vh = v[:T, h].float().cpu().numpy()
+            q = workloads.queries(w, seed=seed, device=device)[b, h * w.group:(h + 1) * w.group].float().cpu()
+            kc, ks, _ = oracle.quantize_rows(kh)
+            vc, vs, _ = oracle.quantize_rows(vh)
+            self.units.append((q.numpy(), kc, ks, vc, vs, kh[-1:].copy(), vh[-1:].copy(), T))
+
+    def run_unit(self, u):
+        q, kc, ks, vc, vs, knew, vnew, T = u
+        o = self.o
+        o.quantize_rows(knew)   # the step's append of this unit's new token
+        o.quantize_rows(vnew)
+        kd = o.dequantize_rows(kc, ks)
+        vd = o.dequantize_rows(vc, vs)
+        o.attend(q, kd, vd, 1.0 / math.sqrt(self.w.head_dim))
+        return T
+
+    def run(self, pool):
+        t = time.perf_counter()
+        toks = sum(pool.map(self.run_unit, self.units))
+        return toks / self.w.num_kv_heads, time.perf_counter() - t
+
+
+def cpu_baseline(w, seed, st=None, budget_s=20.0):
+    cores = os.cpu_count() or 1
+    n_units = max(cores, 8)
+    sample = OracleSample(w, seed, n_units, device="cuda" if torch.cuda.is_available() else "cpu")
+    with cf.ThreadPoolExecutor(max_workers=cores) as pool:
+        kv, secs = sample.run(pool)
+        reps = 1
+        while secs < budget_s / 2 and reps < 8:
+            k2, s2 = sample.run(pool)
+            kv += k2
+            secs += s2
+            reps += 1
+    return {"value": kv / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n_units} (sequence, kv head) units of one {w.name} step x{reps}: append quantise + "
+                      f"dequantise + fp64 attention, {cores} threads, {secs:.1f} s"}
+
+
+def run_reference(args, dist: Dist):
+    w = workloads.WORKLOADS[args.workload]
+    if dist.rank != 0:
+        return None
+    cores = os.cpu_count() or 1
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    # size each step so the whole warm-up + timed run stays around a minute
+    probe = OracleSample(w, args.seed, 1, max_tokens=4096, device=dev)
+    with cf.ThreadPoolExecutor(max_workers=cores) as pool:
+        _, t_probe = probe.run(pool)
+        per_token_s = t_probe / 4096
+        budget_per_step = 60.0 / max(1, args.steps + args.warmup)
+        max_tokens = int(min(w.context or 131072, max(64, budget_per_step * cores / per_token_s)))
+        sample = OracleSample(w, args.seed, cores, max_tokens=max_tokens, device=dev)
+        for _ in range(args.warmup):
+            sample.run(pool)
+        kv, secs = 0.0, 0.0
+        for _ in range(args.steps):
+            k2, s2 = sample.run(pool)
+            kv += k2
+            secs += s2
+    value = kv / secs
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.description}; step = append 1 token/seq + decode attention",
+                   "batch": w.batch, "kv_heads": w.num_kv_heads, "q_heads": w.num_q_heads,
+                   "head_dim": w.head_dim, "context": w.context, "page_size": w.page_size,
+                   "parallelism": "host threads"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{cores} units x {max_tokens} positions per step (CPU oracle)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
+    ap.add_argument("--workload", default="long_context",
+                    choices=["long_context", "gqa_outliers", "paged_ragged", "tiny"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    dist = Dist()
+    try:
+        res = run_reference(args, dist) if args.impl == "reference" else run_gpu(args, dist)
+        if dist.rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,60 @@
+// kvq_host.cuh -- host-side argument checks and launch helpers shared by the
+// libkvq entry points.  Checks run before anything is enqueued.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+inline bool is_pow2_page(int32_t p) { return p == 16 || p == 32 || p == 64 || p == 128 || p == 256; }
+
+inline bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Validates a cache description for `batch` sequences.
+inline kvq_status check_cache(const kvq_cache* c, int32_t batch) {
+  if (c == nullptr || c->reserved != 0) return KVQ_ERR_INVALID_ARGUMENT;
+  if (c->num_kv_heads < 1 || c->head_dim < 16 || c->head_dim > 512 || (c->head_dim % 16) != 0)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (c->k_codes == nullptr || c->v_codes == nullptr || c->k_scales == nullptr || c->v_scales == nullptr)
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned_to(c->k_codes, 16) || !aligned_to(c->v_codes, 16)) return KVQ_ERR_INVALID_ARGUMENT;
+  if (c->format == KVQ_FORMAT_FP4_E2M1_E4M3_G16) {
+    if (!is_pow2_page(c->page_size) || c->num_pages < 1 || c->max_pages_per_seq < 1)
+      return KVQ_ERR_INVALID_ARGUMENT;
+    if (!aligned_to(c->k_scales, 16) || !aligned_to(c->v_scales, 16)) return KVQ_ERR_INVALID_ARGUMENT;
+    if (c->page_table == nullptr && (int64_t)batch * c->max_pages_per_seq > c->num_pages)
+      return KVQ_ERR_INVALID_ARGUMENT;
+    if (c->num_pages * (int64_t)c->num_kv_heads > (int64_t)INT32_MAX) return KVQ_ERR_UNSUPPORTED;
+    return KVQ_OK;
+  }
+  if (c->format == KVQ_FORMAT_FP8_E4M3_HEAD) {
+    if (c->page_size < 1 || c->page_size > 1024 || c->page_table != nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+    if (c->num_pages < batch) return KVQ_ERR_INVALID_ARGUMENT;
+    if (!aligned_to(c->k_scales, 4) || !aligned_to(c->v_scales, 4)) return KVQ_ERR_INVALID_ARGUMENT;
+    return KVQ_OK;
+  }
+  return KVQ_ERR_INVALID_ARGUMENT;
+}
+
+inline int device_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+inline unsigned grid_for(int64_t work_items, int threads) {
+  int64_t g = (work_items + threads - 1) / threads;
+  if (g < 1) g = 1;
+  if (g > 0x7FFFFFFF) g = 0x7FFFFFFF;
+  return (unsigned)g;
+}
+
+inline kvq_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // namespace kvq

@@ -1,0 +1,244 @@
+"""Thin Python binding of libkvq (the C ABI declared in include/kvq.h).
+
+Argument marshalling only: every step of the path runs in the CUDA kernels of
+libkvq.so.  PyTorch is used for device memory and streams.  There is no CPU
+fallback -- if libkvq.so is missing, ``load()`` raises.
+
+Names follow the header: ``append`` (kvq_append), ``fp8_set_scales``
+(kvq_fp8_set_scales), ``decode_attn`` (kvq_decode_attn), ``dequant``
+(kvq_dequant), ``decode_workspace_bytes`` (kvq_decode_workspace_bytes).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvq.so")
+
+FORMAT_FP4 = 1
+FORMAT_FP8 = 2
+FLAG_NONFINITE = 0x1
+FLAG_PAGE_OOB = 0x2
+FLAG_TIMEOUT = 0x4
+FLAG_BAD_LENGTH = 0x8
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {_status_string(status)} (status {status})")
+        self.status = status
+
+
+class KvqCacheStruct(ctypes.Structure):
+    _fields_ = [
+        ("format", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("num_pages", ctypes.c_int64),
+        ("max_pages_per_seq", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("page_table", ctypes.c_void_p),
+        ("k_codes", ctypes.c_void_p),
+        ("v_codes", ctypes.c_void_p),
+        ("k_scales", ctypes.c_void_p),
+        ("v_scales", ctypes.c_void_p),
+    ]
+
+
+_P = ctypes.c_void_p
+_CP = ctypes.POINTER(KvqCacheStruct)
+
+
+def load() -> ctypes.CDLL:
+    """Load libkvq.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m fp4_kv_cache_kvq_gb300.build` (nvcc, sm_103a)")
+            L = ctypes.CDLL(LIB_PATH)
+            L.kvq_append.restype = ctypes.c_int
+            L.kvq_append.argtypes = [_CP, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P]
+            L.kvq_fp8_set_scales.restype = ctypes.c_int
+            L.kvq_fp8_set_scales.argtypes = [_CP, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]
+            L.kvq_decode_workspace_bytes.restype = ctypes.c_size_t
+            L.kvq_decode_workspace_bytes.argtypes = [ctypes.c_int32] * 4
+            L.kvq_decode_attn.restype = ctypes.c_int
+            L.kvq_decode_attn.argtypes = [_CP, _CP, ctypes.c_int32, ctypes.c_int32, _P, _P, ctypes.c_float,
+                                          _P, _P, ctypes.c_size_t, _P, _P]
+            L.kvq_dequant.restype = ctypes.c_int
+            L.kvq_dequant.argtypes = [_CP, ctypes.c_int32, _P, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]
+            L.kvq_status_string.restype = ctypes.c_char_p
+            L.kvq_status_string.argtypes = [ctypes.c_int]
+            L.kvq_version.restype = ctypes.c_int32
+            L.kvq_version.argtypes = []
+            _lib = L
+    return _lib
+
+
+def _status_string(status: int) -> str:
+    try:
+        return load().kvq_status_string(status).decode()
+    except Exception:  # pragma: no cover
+        return "unknown"
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise KvqError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _need(t: torch.Tensor, dtype: torch.dtype, name: str) -> None:
+    if t.dtype != dtype or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor of dtype {dtype}")
+
+
+class Fp4Cache:
+    """FP4 (E2M1 codes, E4M3 scale per 16 channels) paged cache for K and V.
+
+    codes  uint8 [num_pages][num_kv_heads][page_size][head_dim/2]
+    scales uint8 [num_pages][num_kv_heads][page_size][head_dim/16]
+    page_table int32 [batch][max_pages_per_seq] or None (contiguous).
+    """
+
+    def __init__(self, num_kv_heads: int, head_dim: int, page_size: int, num_pages: int,
+                 max_pages_per_seq: int, page_table: Optional[torch.Tensor] = None, device="cuda"):
+        self.num_kv_heads, self.head_dim, self.page_size = num_kv_heads, head_dim, page_size
+        self.num_pages, self.max_pages_per_seq = num_pages, max_pages_per_seq
+        shape = (num_pages, num_kv_heads, page_size)
+        self.k_codes = torch.zeros(shape + (head_dim // 2,), dtype=torch.uint8, device=device)
+        self.v_codes = torch.zeros_like(self.k_codes)
+        self.k_scales = torch.zeros(shape + (head_dim // 16,), dtype=torch.uint8, device=device)
+        self.v_scales = torch.zeros_like(self.k_scales)
+        if page_table is not None:
+            _need(page_table, torch.int32, "page_table")
+        self.page_table = page_table
+
+    def struct(self, page_table: Optional[torch.Tensor] = None) -> KvqCacheStruct:
+        pt = self.page_table if page_table is None else page_table
+        return KvqCacheStruct(FORMAT_FP4, self.num_kv_heads, self.head_dim, self.page_size, self.num_pages,
+                              self.max_pages_per_seq, 0, _ptr(pt), _ptr(self.k_codes), _ptr(self.v_codes),
+                              _ptr(self.k_scales), _ptr(self.v_scales))
+
+    @property
+    def nbytes(self) -> int:
+        return 2 * (self.k_codes.numel() + self.k_scales.numel())
+
+
+class Fp8WindowCache:
+    """FP8 E4M3 sliding-window cache: one ring of `window` slots per sequence,
+    one fp32 scale per kv head (K and V apart).
+
+    codes  uint8 [num_seqs][num_kv_heads][window][head_dim]
+    scales float32 [num_kv_heads]
+    """
+
+    def __init__(self, num_seqs: int, num_kv_heads: int, head_dim: int, window: int, device="cuda"):
+        self.num_seqs, self.num_kv_heads, self.head_dim, self.window = num_seqs, num_kv_heads, head_dim, window
+        shape = (num_seqs, num_kv_heads, window, head_dim)
+        self.k_codes = torch.zeros(shape, dtype=torch.uint8, device=device)
+        self.v_codes = torch.zeros_like(self.k_codes)
+        self.k_scales = torch.ones(num_kv_heads, dtype=torch.float32, device=device)
+        self.v_scales = torch.ones_like(self.k_scales)
+
+    def struct(self) -> KvqCacheStruct:
+        return KvqCacheStruct(FORMAT_FP8, self.num_kv_heads, self.head_dim, self.window, self.num_seqs, 0, 0,
+                              None, _ptr(self.k_codes), _ptr(self.v_codes), _ptr(self.k_scales),
+                              _ptr(self.v_scales))
+
+
+def append(cache, start_pos: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+           err: Optional[torch.Tensor] = None, stream=None, page_table: Optional[torch.Tensor] = None) -> None:
+    """kvq_append: k, v bf16 [batch][n_new][Hkv][head_dim]; start_pos int32 [batch]."""
+    _need(k, torch.bfloat16, "k")
+    _need(v, torch.bfloat16, "v")
+    _need(start_pos, torch.int32, "start_pos")
+    if k.dim() != 4 or k.shape != v.shape:
+        raise ValueError("k and v must have shape [batch, n_new, num_kv_heads, head_dim]")
+    s = cache.struct(page_table) if isinstance(cache, Fp4Cache) else cache.struct()
+    st = load().kvq_append(ctypes.byref(s), k.shape[0], k.shape[1], _ptr(start_pos), _ptr(k), _ptr(v),
+                           _ptr(err), _stream(stream))
+    _check(st, "kvq_append")
+
+
+def fp8_set_scales(cache: Fp8WindowCache, k: torch.Tensor, v: torch.Tensor,
+                   err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """kvq_fp8_set_scales: per-head s_h = amax/448 over k, v bf16 [batch][n][Hkv][D]."""
+    _need(k, torch.bfloat16, "k")
+    _need(v, torch.bfloat16, "v")
+    s = cache.struct()
+    st = load().kvq_fp8_set_scales(ctypes.byref(s), k.shape[0], k.shape[1], _ptr(k), _ptr(v), _ptr(err),
+                                   _stream(stream))
+    _check(st, "kvq_fp8_set_scales")
+
+
+def decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(load().kvq_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim))
+
+
+def decode_attn(cache: Fp4Cache, seq_lens: torch.Tensor, q: torch.Tensor, softmax_scale: Optional[float] = None,
+                swa: Optional[Fp8WindowCache] = None, out: Optional[torch.Tensor] = None,
+                workspace: Optional[torch.Tensor] = None, err: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    """kvq_decode_attn: q bf16 [batch][Hq][head_dim] -> out float32 [batch][Hq][head_dim]."""
+    _need(q, torch.bfloat16, "q")
+    _need(seq_lens, torch.int32, "seq_lens")
+    batch, hq, d = q.shape
+    if out is None:
+        out = torch.empty((batch, hq, d), dtype=torch.float32, device=q.device)
+    _need(out, torch.float32, "out")
+    need = decode_workspace_bytes(batch, hq, cache.num_kv_heads, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    g = cache.struct()
+    w = swa.struct() if swa is not None else None
+    st = load().kvq_decode_attn(ctypes.byref(g), ctypes.byref(w) if w is not None else None, batch, hq,
+                                _ptr(seq_lens), _ptr(q), float(softmax_scale), _ptr(out), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream))
+    _check(st, "kvq_decode_attn")
+    return out
+
+
+def dequant(cache, seq_lens: Optional[torch.Tensor], max_len: int, dtype: torch.dtype = torch.float32,
+            err: Optional[torch.Tensor] = None, stream=None):
+    """kvq_dequant: dense K, V [batch][max_len][Hkv][head_dim] (FP8: max_len == window, slot order)."""
+    if isinstance(cache, Fp4Cache):
+        batch = seq_lens.shape[0]
+        s = cache.struct()
+        device = cache.k_codes.device
+    else:
+        batch = cache.num_seqs
+        s = cache.struct()
+        device = cache.k_codes.device
+    code = {torch.float32: 0, torch.bfloat16: 1}[dtype]
+    shape = (batch, max_len, cache.num_kv_heads, cache.head_dim)
+    k = torch.empty(shape, dtype=dtype, device=device)
+    v = torch.empty(shape, dtype=dtype, device=device)
+    st = load().kvq_dequant(ctypes.byref(s), batch, _ptr(seq_lens), max_len, code, _ptr(k), _ptr(v), _ptr(err),
+                            _stream(stream))
+    _check(st, "kvq_dequant")
+    return k, v

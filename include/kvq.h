@@ -124,6 +124,8 @@ typedef struct kvq_cache {
  *   d_start_pos device int32 [batch]: position of each sequence's first new
  *               token; token t goes to position d_start_pos[b] + t.
  *   k, v        device bf16 [batch][n_new][num_kv_heads][head_dim], contiguous.
+ * FP8 caches keep a ring of W slots: when n_new > W only the last W new
+ * tokens are written (the earlier ones would be overwritten in the same call).
  * Device flags: NONFINITE (the block's codes and scale are whatever the
  * conversion produces), PAGE_OOB (token skipped), BAD_LENGTH (negative start;
  * sequence skipped).

@@ -1,0 +1,106 @@
+"""The C ABI without a GPU: libkvq.so builds (nvcc cross-compiles for
+sm_103a), loads, exports every function include/kvq.h declares, matches the
+binding's struct layout, and rejects invalid arguments on the host before
+touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+from fp4_kv_cache_kvq_gb300 import build, kvq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return kvq.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    assert declared_functions() == sorted([
+        "kvq_append", "kvq_decode_attn", "kvq_decode_workspace_bytes", "kvq_dequant", "kvq_fp8_set_scales",
+        "kvq_status_string", "kvq_version"])
+
+
+def test_library_exports_every_declared_function(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", kvq.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (kvq_[a-z0-9_]+)\b", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_struct_layout_matches_header():
+    src = r'''
+#include <stddef.h>
+#include <stdio.h>
+#include "kvq.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(kvq_cache), offsetof(kvq_cache, num_pages),
+         offsetof(kvq_cache, max_pages_per_seq), offsetof(kvq_cache, page_table),
+         offsetof(kvq_cache, k_codes), offsetof(kvq_cache, k_scales), offsetof(kvq_cache, v_scales));
+  return 0;
+}
+'''
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "layout.c")
+        exe = os.path.join(d, "layout")
+        open(c, "w").write(src)
+        subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
+        got = [int(x) for x in subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()]
+    S = kvq.KvqCacheStruct
+    want = [ctypes.sizeof(S), S.num_pages.offset, S.max_pages_per_seq.offset, S.page_table.offset,
+            S.k_codes.offset, S.k_scales.offset, S.v_scales.offset]
+    assert got == want
+
+
+def test_status_strings_and_version(lib):
+    assert lib.kvq_version() == 1
+    assert lib.kvq_status_string(0) == b"ok"
+    assert lib.kvq_status_string(1) == b"invalid argument"
+    assert lib.kvq_status_string(3) == b"workspace too small"
+
+
+def _fp4_struct(**kw):
+    fields = dict(format=kvq.FORMAT_FP4, num_kv_heads=2, head_dim=128, page_size=64, num_pages=4,
+                  max_pages_per_seq=2, reserved=0, page_table=None, k_codes=4096, v_codes=8192,
+                  k_scales=12288, v_scales=16384)
+    fields.update(kw)
+    return kvq.KvqCacheStruct(**fields)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(head_dim=24), dict(head_dim=0), dict(page_size=48), dict(num_kv_heads=0), dict(reserved=1),
+    dict(k_codes=None), dict(k_codes=4097), dict(format=7), dict(num_pages=1)])
+def test_invalid_cache_is_rejected_on_the_host(lib, bad):
+    s = _fp4_struct(**bad)
+    st = lib.kvq_append(ctypes.byref(s), 2, 1, 16, 32, 64, None, None)
+    assert st == 1  # KVQ_ERR_INVALID_ARGUMENT, nothing enqueued
+
+
+def test_invalid_sizes_are_rejected_on_the_host(lib):
+    s = _fp4_struct()
+    assert lib.kvq_append(ctypes.byref(s), -1, 1, 16, 32, 64, None, None) == 1
+    assert lib.kvq_append(ctypes.byref(s), 2, -3, 16, 32, 64, None, None) == 1
+    assert lib.kvq_append(ctypes.byref(s), 2, 1, None, 32, 64, None, None) == 1
+    # empty work is a no-op that succeeds without a launch
+    assert lib.kvq_append(ctypes.byref(s), 0, 5, None, None, None, None, None) == 0
+    assert lib.kvq_append(ctypes.byref(s), 2, 0, None, None, None, None, None) == 0
+    # decode: bad group size, scale and null pointers are rejected before any launch
+    assert lib.kvq_decode_attn(ctypes.byref(s), None, 2, 3, 16, 32, 0.1, 64, 128, 1 << 20, None, None) == 1
+    assert lib.kvq_decode_attn(ctypes.byref(s), None, 2, 4, 16, 32, -1.0, 64, 128, 1 << 20, None, None) == 1
+    assert lib.kvq_decode_attn(ctypes.byref(s), None, 2, 4, None, 32, 0.1, 64, 128, 1 << 20, None, None) == 1
+    assert lib.kvq_dequant(ctypes.byref(s), 2, 16, 8, 5, 32, 64, None, None) == 1

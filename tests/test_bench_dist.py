@@ -1,0 +1,58 @@
+"""bench.py's multi-process host logic on CPU: two gloo ranks, each timing its
+own replica; the job value is the units summed over ranks divided by the
+slowest rank's time, and the reference arm runs on rank 0 only."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, q):
+    os.environ.update({"RANK": str(rank), "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    import bench
+    d = bench.Dist()
+    try:
+        units = 1000.0 * (rank + 1)
+        seconds = 2.0 if rank == 0 else 5.0
+        value, max_s = bench.combine_ranks(d, units, seconds)
+        d.barrier()
+        q.put((rank, value, max_s))
+    finally:
+        d.close()
+
+
+def test_two_rank_weak_scaling_combine():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=5) for _ in range(2))
+    for rank, value, max_s in got:
+        assert max_s == 5.0
+        assert value == pytest.approx(3000.0 / 5.0)
+
+
+def test_reference_arm_on_tiny_workload(capsys):
+    import json
+
+    import bench
+    bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3"])
+    line = capsys.readouterr().out.strip().splitlines()[-1]
+    res = json.loads(line)
+    assert res["impl"] == "reference" and res["value"] > 0 and res["unit"] == bench.UNIT
+    assert res["e2e"]["h2d_bytes_per_step"] == 0 and res["cpu_baseline"]["kind"] == "oracle"
