@@ -366,7 +366,7 @@ def cpu_baseline(w, seed, st=None, budget_s=20.0):
     with cf.ThreadPoolExecutor(max_workers=cores) as pool:
         kv, secs = sample.run(pool)
         reps = 1
-        while secs < budget_s / 2 and reps < 8:
+        while secs < budget_s / 2 and reps < 200:
             k2, s2 = sample.run(pool)
             kv += k2
             secs += s2
