@@ -57,6 +57,31 @@ __device__ __forceinline__ uint32_t f16x2_from_e2m1x2(uint32_t byte) {
   return r;
 }
 
+// The four bytes of a word (8 E2M1 codes) -> four f16x2, byte k -> r[k].  The
+// word is split into byte registers for the conversions, which lets the
+// conversion read each byte in place instead of shifting it down first.
+__device__ __forceinline__ void f16x2x4_from_e2m1x8(uint32_t w, uint32_t (&r)[4]) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(w));
+}
+
+// Transpose of an 8x8 b16 tile held in mma fragment layout (thread (g, t)
+// holds row g, columns 2t and 2t+1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(r) : "r"(x));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;\n" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
 // Two E4M3 bytes (low byte -> low half) -> f16x2.
 __device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t two_bytes) {
   uint32_t r;

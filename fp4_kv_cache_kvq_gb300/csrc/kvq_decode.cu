@@ -11,24 +11,28 @@
 // registers right before the tensor-core products.
 //
 // Work decomposition (stream-K over the whole batch).  Every (sequence b,
-// kv head h) pair is a unit; its FP4 positions are cut into chunks of 64
+// kv head h) pair is a unit; its FP4 positions are cut into chunks of 128
 // tokens.  All units' chunks are laid end to end and the persistent grid (two
 // CTAs per SM) splits that line into equal contiguous ranges, so ragged
 // lengths balance to within one chunk.  A CTA writes one partial (m, l, o) per
 // unit it touches; the merge kernel combines them.
 //
 // CTA = 4 consumer warps + 1 producer warp.  The producer's lane 0 streams the
-// chunk's K codes and V codes (3-D tiled TMA loads, 64-byte swizzle for
-// head_dim 128) and K/V scale bytes (1-D bulk copies) into an 8-stage ring
-// guarded by mbarriers.  Consumer warp w takes tokens [16w, 16w+16) of each
-// chunk and runs, per 16 tokens:
+// chunk's K codes and V codes (3-D tiled TMA loads, one per page, 64-byte
+// swizzle for head_dim 128) and K/V scale bytes (1-D bulk copies) into a
+// 4-stage ring guarded by mbarriers.  Consumer warp w takes tokens
+// [32w, 32w+32) of each chunk as two independent 16-token slices and runs,
+// per slice:
 //   S^T(16 tok x 8 q-rows) = K^(16 x d) Q^T    mma.m16n8k16, K^ dequantised in
 //                                              registers (cvt e2m1x2->f16x2,
 //                                              times the block scale)
 //   online softmax in the log2 domain with lazy rescaling (the running max is
 //   only raised when a score exceeds it by more than 8)
-//   O^T(d x 8) += V^T(d x 16 tok) P^T           mma.m16n8k16, P in f16
-// Tokens sit on the MMA's M side so a GQA group of up to 8 query heads fills
+//   O^T(d x 8) += V^T(d x 16 tok) P^T           mma.m16n8k16, P in f16 moved
+//                                              from the S^T fragment to the B
+//                                              fragment with movmatrix.trans
+// Codes are expanded a 32-bit word (8 codes) at a time.  Tokens sit on the
+// MMA's M side so a GQA group of up to 8 query heads fills
 // N = 8 without padding rows.  The query is pre-scaled per head by a power of
 // two so that its bf16 values are exact in f16; the factor is undone in fp32.
 #include "kvq_common.cuh"
@@ -37,10 +41,11 @@
 namespace kvq {
 namespace {
 
-constexpr int kChunk = 64;
+constexpr int kChunk = 128;          // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;
+constexpr int kSlices = kChunk / (16 * kConsumerWarps);  // 16-token slices per warp per stage
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kStages = 8;
+constexpr int kStages = 4;
 constexpr int kNG = 8;  // query rows per kv head held by one tile (G <= 8)
 constexpr float kLazySlack = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -325,106 +330,120 @@ __device__ __forceinline__ void begin_unit(const DecodeParams& p, ConsumerState<
   st.l[0] = st.l[1] = 0.0f;
 }
 
-// Broadcast a K scale byte into both halves of an f16x2.
-__device__ __forceinline__ uint32_t scale_pair_same(uint32_t byte) { return f16x2_from_e4m3x2(byte * 0x0101u); }
-
+// One stage for one consumer warp: two 16-token slices, rows [32w, 32w+32).
 template <int D>
-__device__ __forceinline__ void process_slice(const DecodeParams& p, ConsumerState<D>& st, const uint8_t* stage,
-                                              int ntok, uint32_t empty_bar) {
+__device__ __forceinline__ void consume_stage(ConsumerState<D>& st, const uint8_t* stage, int ntok,
+                                              uint32_t empty_bar) {
   using G = Geo<D>;
+  constexpr int KW = D / 32;  // words of K codes per thread per row (channels [tig*D/4, +D/4))
+  constexpr int VW = D / 64;  // words of V codes per thread per row (channels [g*D/8, +D/8))
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int g = lane >> 2, tig = lane & 3;
-  const int r0 = 16 * warp;
   const uint8_t* sK = stage + G::kOffK;
   const uint8_t* sV = stage + G::kOffV;
   const uint8_t* sKS = stage + G::kOffKS;
   const uint8_t* sVS = stage + G::kOffVS;
-  // V k-slot order: pair A = tokens (tA, tA+8), pair B = (tB, tB+8); the
-  // parity flip keeps the 8-byte V loads of a half-warp on distinct banks.
-  const int tA = 2 * tig + (tig & 1);
-  const int tB = 2 * tig + 1 - (tig & 1);
-  const int rowK0 = r0 + g, rowK1 = r0 + g + 8;
-  const int rVA0 = r0 + tA, rVA1 = r0 + tA + 8, rVB0 = r0 + tB, rVB1 = r0 + tB + 8;
 
-  // ---- loads from the stage (then release it)
-  uint32_t kw0[D / 32], kw1[D / 32];  // the thread's D/16 code bytes of rows g, g+8
-  uint32_t ksA, ksB;                  // K scale bytes (D=128: 2 per row, D=64: 1 per row)
-  uint32_t vA0[D / 64], vA1[D / 64], vB0[D / 64], vB1[D / 64];
-  uint32_t vsA, vsB;
-  if constexpr (D == 128) {
-    const int gr = tig ^ ((rowK0 >> 1) & 3);
-    const uint4 a = *reinterpret_cast<const uint4*>(sK + rowK0 * 64 + gr * 16);
-    const uint4 b = *reinterpret_cast<const uint4*>(sK + rowK1 * 64 + gr * 16);
-    kw0[0] = a.x; kw0[1] = a.y; kw0[2] = a.z; kw0[3] = a.w;
-    kw1[0] = b.x; kw1[1] = b.y; kw1[2] = b.z; kw1[3] = b.w;
-    ksA = *reinterpret_cast<const uint16_t*>(sKS + rowK0 * 8 + 2 * tig);
-    ksB = *reinterpret_cast<const uint16_t*>(sKS + rowK1 * 8 + 2 * tig);
-    const int vo = 8 * (g & 1);
-    const uint2 a0 = *reinterpret_cast<const uint2*>(sV + rVA0 * 64 + (((g >> 1) ^ ((rVA0 >> 1) & 3)) * 16) + vo);
-    const uint2 a1 = *reinterpret_cast<const uint2*>(sV + rVA1 * 64 + (((g >> 1) ^ ((rVA1 >> 1) & 3)) * 16) + vo);
-    const uint2 b0 = *reinterpret_cast<const uint2*>(sV + rVB0 * 64 + (((g >> 1) ^ ((rVB0 >> 1) & 3)) * 16) + vo);
-    const uint2 b1 = *reinterpret_cast<const uint2*>(sV + rVB1 * 64 + (((g >> 1) ^ ((rVB1 >> 1) & 3)) * 16) + vo);
-    vA0[0] = a0.x; vA0[1] = a0.y; vA1[0] = a1.x; vA1[1] = a1.y;
-    vB0[0] = b0.x; vB0[1] = b0.y; vB1[0] = b1.x; vB1[1] = b1.y;
-    vsA = sVS[rVA0 * 8 + g] | (sVS[rVA1 * 8 + g] << 8);
-    vsB = sVS[rVB0 * 8 + g] | (sVS[rVB1 * 8 + g] << 8);
-  } else {
-    const uint2 a = *reinterpret_cast<const uint2*>(sK + rowK0 * 32 + 8 * tig);
-    const uint2 b = *reinterpret_cast<const uint2*>(sK + rowK1 * 32 + 8 * tig);
-    kw0[0] = a.x; kw0[1] = a.y;
-    kw1[0] = b.x; kw1[1] = b.y;
-    ksA = sKS[rowK0 * 4 + tig];
-    ksB = sKS[rowK1 * 4 + tig];
-    vA0[0] = *reinterpret_cast<const uint32_t*>(sV + rVA0 * 32 + 4 * g);
-    vA1[0] = *reinterpret_cast<const uint32_t*>(sV + rVA1 * 32 + 4 * g);
-    vB0[0] = *reinterpret_cast<const uint32_t*>(sV + rVB0 * 32 + 4 * g);
-    vB1[0] = *reinterpret_cast<const uint32_t*>(sV + rVB1 * 32 + 4 * g);
-    vsA = sVS[rVA0 * 4 + (g >> 1)] | (sVS[rVA1 * 4 + (g >> 1)] << 8);
-    vsB = sVS[rVB0 * 4 + (g >> 1)] | (sVS[rVB1 * 4 + (g >> 1)] << 8);
+  // ---- loads from the stage, then release it
+  uint32_t kw[kSlices][2][KW];  // rows g, g+8 of each slice
+  uint32_t ksb[kSlices][2];     // their scale bytes (blocks of this thread's channels)
+  uint32_t vw[kSlices][4][VW];  // rows 2t, 2t+1, 2t+8, 2t+9 of each slice
+  uint32_t vsb[kSlices][2];     // scale-byte pairs (2t, 2t+1) and (2t+8, 2t+9), block of g
+#pragma unroll
+  for (int sl = 0; sl < kSlices; ++sl) {
+    const int r0 = 16 * (kSlices * warp + sl);
+    const int ra = r0 + g, rb = r0 + g + 8;
+    const int vr[4] = {r0 + 2 * tig, r0 + 2 * tig + 1, r0 + 2 * tig + 8, r0 + 2 * tig + 9};
+    if constexpr (D == 128) {
+      const int gr = tig ^ ((ra >> 1) & 3);  // 64-byte swizzle: granule ^= (row >> 1) & 3
+      const uint4 a = *reinterpret_cast<const uint4*>(sK + ra * 64 + gr * 16);
+      const uint4 b = *reinterpret_cast<const uint4*>(sK + rb * 64 + gr * 16);
+      kw[sl][0][0] = a.x; kw[sl][0][1] = a.y; kw[sl][0][2] = a.z; kw[sl][0][3] = a.w;
+      kw[sl][1][0] = b.x; kw[sl][1][1] = b.y; kw[sl][1][2] = b.z; kw[sl][1][3] = b.w;
+      ksb[sl][0] = *reinterpret_cast<const uint16_t*>(sKS + ra * 8 + 2 * tig);
+      ksb[sl][1] = *reinterpret_cast<const uint16_t*>(sKS + rb * 8 + 2 * tig);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int gv = (g >> 1) ^ ((vr[i] >> 1) & 3);
+        const uint2 x = *reinterpret_cast<const uint2*>(sV + vr[i] * 64 + gv * 16 + 8 * (g & 1));
+        vw[sl][i][0] = x.x;
+        vw[sl][i][1] = x.y;
+      }
+      vsb[sl][0] = sVS[vr[0] * 8 + g] | (sVS[vr[1] * 8 + g] << 8);
+      vsb[sl][1] = sVS[vr[2] * 8 + g] | (sVS[vr[3] * 8 + g] << 8);
+    } else {
+      const uint2 a = *reinterpret_cast<const uint2*>(sK + ra * 32 + 8 * tig);
+      const uint2 b = *reinterpret_cast<const uint2*>(sK + rb * 32 + 8 * tig);
+      kw[sl][0][0] = a.x; kw[sl][0][1] = a.y;
+      kw[sl][1][0] = b.x; kw[sl][1][1] = b.y;
+      ksb[sl][0] = sKS[ra * 4 + tig];
+      ksb[sl][1] = sKS[rb * 4 + tig];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) vw[sl][i][0] = *reinterpret_cast<const uint32_t*>(sV + vr[i] * 32 + 4 * g);
+      vsb[sl][0] = sVS[vr[0] * 4 + (g >> 1)] | (sVS[vr[1] * 4 + (g >> 1)] << 8);
+      vsb[sl][1] = sVS[vr[2] * 4 + (g >> 1)] | (sVS[vr[3] * 4 + (g >> 1)] << 8);
+    }
   }
   mbar_arrive(empty_bar);
 
-  // ---- S^T = K^ Q^T  (rows: tokens g, g+8; cols: q rows)
-  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  uint32_t sA0, sA1, sB0, sB1;
-  if constexpr (D == 128) {
-    sA0 = scale_pair_same(ksA & 0xFFu);
-    sA1 = scale_pair_same(ksA >> 8);
-    sB0 = scale_pair_same(ksB & 0xFFu);
-    sB1 = scale_pair_same(ksB >> 8);
-  } else {
-    sA0 = sA1 = scale_pair_same(ksA);
-    sB0 = sB1 = scale_pair_same(ksB);
-  }
+  // ---- S^T = K^ Q^T per slice (rows: tokens g, g+8; columns: q rows 2t, 2t+1)
+  float S[kSlices][4];
 #pragma unroll
-  for (int j = 0; j < D / 16; ++j) {
-    const int sh = 16 * (j & 1);
-    const uint32_t wA = kw0[j >> 1], wB = kw1[j >> 1];
-    const uint32_t scA = (D == 128 && j >= 4) ? sA1 : sA0;
-    const uint32_t scB = (D == 128 && j >= 4) ? sB1 : sB0;
-    const uint32_t a0 = hmul2_u32(f16x2_from_e2m1x2(wA >> sh), scA);
-    const uint32_t a1 = hmul2_u32(f16x2_from_e2m1x2(wB >> sh), scB);
-    const uint32_t a2 = hmul2_u32(f16x2_from_e2m1x2(wA >> (sh + 8)), scA);
-    const uint32_t a3 = hmul2_u32(f16x2_from_e2m1x2(wB >> (sh + 8)), scB);
-    mma_f16_16816(acc[j & 1], a0, a1, a2, a3, st.qf[2 * j], st.qf[2 * j + 1]);
-  }
-  float x[4];
+  for (int sl = 0; sl < kSlices; ++sl) {
+    uint32_t sc[2][2];  // [row g / g+8][first / second block of the thread's channels]
 #pragma unroll
-  for (int i = 0; i < 4; ++i) x[i] = (acc[0][i] + acc[1][i]) * st.cs[i & 1];
-  if (r0 + g >= ntok) x[0] = x[1] = -INFINITY;
-  if (r0 + g + 8 >= ntok) x[2] = x[3] = -INFINITY;
+    for (int r = 0; r < 2; ++r) {
+      if constexpr (D == 128) {
+        const uint32_t u = f16x2_from_e4m3x2(ksb[sl][r]);
+        sc[r][0] = prmt(u, 0u, 0x1010u);
+        sc[r][1] = prmt(u, 0u, 0x3232u);
+      } else {
+        sc[r][0] = sc[r][1] = f16x2_from_e4m3x2(ksb[sl][r] * 0x0101u);
+      }
+    }
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int q = 0; q < KW; ++q) {  // word q holds k-steps 2q (bytes 0,1) and 2q+1 (bytes 2,3)
+      uint32_t ca[4], cb[4];
+      f16x2x4_from_e2m1x8(kw[sl][0][q], ca);
+      f16x2x4_from_e2m1x8(kw[sl][1][q], cb);
+      const int half = (D == 128 && q >= KW / 2) ? 1 : 0;
+      const uint32_t sA = sc[0][half], sB = sc[1][half];
+      mma_f16_16816(acc[0], hmul2_u32(ca[0], sA), hmul2_u32(cb[0], sB), hmul2_u32(ca[1], sA),
+                    hmul2_u32(cb[1], sB), st.qf[4 * q], st.qf[4 * q + 1]);
+      mma_f16_16816(acc[1], hmul2_u32(ca[2], sA), hmul2_u32(cb[2], sB), hmul2_u32(ca[3], sA),
+                    hmul2_u32(cb[3], sB), st.qf[4 * q + 2], st.qf[4 * q + 3]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) S[sl][i] = acc[0][i] + acc[1][i];
+  }
+  const bool partial = ntok < kChunk;  // only a unit's last chunk
+  if (partial) {
+#pragma unroll
+    for (int sl = 0; sl < kSlices; ++sl) {
+      const int t0 = 16 * (kSlices * warp + sl) + g;
+      if (t0 >= ntok) S[sl][0] = S[sl][1] = -INFINITY;
+      if (t0 + 8 >= ntok) S[sl][2] = S[sl][3] = -INFINITY;
+    }
+  }
 
-  // ---- online softmax (log2 domain, lazy rescale)
-  const bool need = fmaxf(x[0], x[2]) > st.m[0] + kLazySlack || fmaxf(x[1], x[3]) > st.m[1] + kLazySlack;
-  if (__any_sync(0xFFFFFFFFu, need)) {
-    float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+  // ---- online softmax in the log2 domain (cs > 0, so the max commutes with the scale)
+  float m0 = fmaxf(S[0][0], S[0][2]), m1 = fmaxf(S[0][1], S[0][3]);
+#pragma unroll
+  for (int sl = 1; sl < kSlices; ++sl) {
+    m0 = fmaxf(m0, fmaxf(S[sl][0], S[sl][2]));
+    m1 = fmaxf(m1, fmaxf(S[sl][1], S[sl][3]));
+  }
+  m0 *= st.cs[0];
+  m1 *= st.cs[1];
+  if (__any_sync(0xFFFFFFFFu, m0 > st.m[0] + kLazySlack || m1 > st.m[1] + kLazySlack)) {
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, o));
+      m0 = fmaxf(m0, __shfl_xor_sync(0xFFFFFFFFu, m0, o));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xFFFFFFFFu, m1, o));
     }
-    const float n0 = fmaxf(st.m[0], mx0), n1 = fmaxf(st.m[1], mx1);
+    const float n0 = fmaxf(st.m[0], m0), n1 = fmaxf(st.m[1], m1);
     const float al0 = (st.m[0] == -INFINITY) ? 0.0f : fast_exp2(st.m[0] - n0);
     const float al1 = (st.m[1] == -INFINITY) ? 0.0f : fast_exp2(st.m[1] - n1);
 #pragma unroll
@@ -439,59 +458,59 @@ __device__ __forceinline__ void process_slice(const DecodeParams& p, ConsumerSta
     st.m[0] = n0;
     st.m[1] = n1;
   }
-  const float ref0 = st.m[0] == -INFINITY ? 0.0f : st.m[0];
-  const float ref1 = st.m[1] == -INFINITY ? 0.0f : st.m[1];
-  const float p0 = fast_exp2(x[0] - ref0), p2 = fast_exp2(x[2] - ref0);
-  const float p1 = fast_exp2(x[1] - ref1), p3 = fast_exp2(x[3] - ref1);
-  st.l[0] += p0 + p2;
-  st.l[1] += p1 + p3;
-  const uint32_t xp = pack_f16x2(p0, p2);  // q row 2tig: tokens (g, g+8)
-  const uint32_t yp = pack_f16x2(p1, p3);  // q row 2tig+1
-  const int srcA = 4 * tA + (g >> 1), srcB = 4 * tB + (g >> 1);
-  const uint32_t XA = __shfl_sync(0xFFFFFFFFu, xp, srcA), YA = __shfl_sync(0xFFFFFFFFu, yp, srcA);
-  const uint32_t XB = __shfl_sync(0xFFFFFFFFu, xp, srcB), YB = __shfl_sync(0xFFFFFFFFu, yp, srcB);
-  const uint32_t pbA = (g & 1) ? YA : XA;
-  const uint32_t pbB = (g & 1) ? YB : XB;
+  const float nref0 = st.m[0] == -INFINITY ? 0.0f : -st.m[0];
+  const float nref1 = st.m[1] == -INFINITY ? 0.0f : -st.m[1];
 
-  // ---- O^T += V^T P^T
-  // masked tokens get a zero V scale so stale bytes cannot inject NaN
-  if (r0 + tA >= ntok) vsA &= 0xFF00u;
-  if (r0 + tA + 8 >= ntok) vsA &= 0x00FFu;
-  if (r0 + tB >= ntok) vsB &= 0xFF00u;
-  if (r0 + tB + 8 >= ntok) vsB &= 0x00FFu;
-  const uint32_t svA = f16x2_from_e4m3x2(vsA);
-  const uint32_t svB = f16x2_from_e4m3x2(vsB);
-  if constexpr (D == 128) {
-    uint32_t lo[2][2], hi[2][2];  // [pair A/B][x (ch 0-7) / y (ch 8-15)]
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      lo[0][q] = (vA0[q] & 0x0F0F0F0Fu) | ((vA1[q] & 0x0F0F0F0Fu) << 4);
-      hi[0][q] = ((vA0[q] >> 4) & 0x0F0F0F0Fu) | (vA1[q] & 0xF0F0F0F0u);
-      lo[1][q] = (vB0[q] & 0x0F0F0F0Fu) | ((vB1[q] & 0x0F0F0F0Fu) << 4);
-      hi[1][q] = ((vB0[q] >> 4) & 0x0F0F0F0Fu) | (vB1[q] & 0xF0F0F0F0u);
+  for (int sl = 0; sl < kSlices; ++sl) {
+    const float p0 = fast_exp2(fmaf(S[sl][0], st.cs[0], nref0));
+    const float p1 = fast_exp2(fmaf(S[sl][1], st.cs[1], nref1));
+    const float p2 = fast_exp2(fmaf(S[sl][2], st.cs[0], nref0));
+    const float p3 = fast_exp2(fmaf(S[sl][3], st.cs[1], nref1));
+    st.l[0] += p0 + p2;
+    st.l[1] += p1 + p3;
+    // P^T B fragment: k-slots (2t, 2t+1) <- tokens 2t, 2t+1; (2t+8, 2t+9) <- 2t+8, 2t+9
+    const uint32_t pbA = movmatrix_trans(pack_f16x2(p0, p1));
+    const uint32_t pbB = movmatrix_trans(pack_f16x2(p2, p3));
+
+    // ---- O^T += V^T P^T
+    uint32_t vsA = vsb[sl][0], vsB = vsb[sl][1];
+    if (partial) {  // masked tokens get a zero V scale so stale bytes cannot inject NaN
+      const int t0 = 16 * (kSlices * warp + sl) + 2 * tig;
+      if (t0 >= ntok) vsA &= 0xFF00u;
+      if (t0 + 1 >= ntok) vsA &= 0x00FFu;
+      if (t0 + 8 >= ntok) vsB &= 0xFF00u;
+      if (t0 + 9 >= ntok) vsB &= 0x00FFu;
+    }
+    const uint32_t svA = f16x2_from_e4m3x2(vsA);
+    const uint32_t svB = f16x2_from_e4m3x2(vsB);
+    // nibble interleave: byte i of lo = (token a, token b) codes of channel 2i, hi: channel 2i+1
+    uint32_t LA[VW][4], HA[VW][4], LB[VW][4], HB[VW][4];
+#pragma unroll
+    for (int w = 0; w < VW; ++w) {
+      const uint32_t a0 = vw[sl][0][w], a1 = vw[sl][1][w], b0 = vw[sl][2][w], b1 = vw[sl][3][w];
+      f16x2x4_from_e2m1x8((a0 & 0x0F0F0F0Fu) | ((a1 & 0x0F0F0F0Fu) << 4), LA[w]);
+      f16x2x4_from_e2m1x8(((a0 >> 4) & 0x0F0F0F0Fu) | (a1 & 0xF0F0F0F0u), HA[w]);
+      f16x2x4_from_e2m1x8((b0 & 0x0F0F0F0Fu) | ((b1 & 0x0F0F0F0Fu) << 4), LB[w]);
+      f16x2x4_from_e2m1x8(((b0 >> 4) & 0x0F0F0F0Fu) | (b1 & 0xF0F0F0F0u), HB[w]);
     }
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      const int sh = 8 * (mt >> 1);
-      const uint32_t a0 = hmul2_u32(f16x2_from_e2m1x2(((mt & 1) ? hi[0][0] : lo[0][0]) >> sh), svA);
-      const uint32_t a1 = hmul2_u32(f16x2_from_e2m1x2(((mt & 1) ? hi[0][1] : lo[0][1]) >> sh), svA);
-      const uint32_t a2 = hmul2_u32(f16x2_from_e2m1x2(((mt & 1) ? hi[1][0] : lo[1][0]) >> sh), svB);
-      const uint32_t a3 = hmul2_u32(f16x2_from_e2m1x2(((mt & 1) ? hi[1][1] : lo[1][1]) >> sh), svB);
-      mma_f16_16816(st.o[mt], a0, a1, a2, a3, pbA, pbB);
-    }
-  } else {
-    const uint32_t loA = (vA0[0] & 0x0F0F0F0Fu) | ((vA1[0] & 0x0F0F0F0Fu) << 4);
-    const uint32_t hiA = ((vA0[0] >> 4) & 0x0F0F0F0Fu) | (vA1[0] & 0xF0F0F0F0u);
-    const uint32_t loB = (vB0[0] & 0x0F0F0F0Fu) | ((vB1[0] & 0x0F0F0F0Fu) << 4);
-    const uint32_t hiB = ((vB0[0] >> 4) & 0x0F0F0F0Fu) | (vB1[0] & 0xF0F0F0F0u);
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      const int sh0 = 8 * (mt >> 1), sh1 = 8 * (2 + (mt >> 1));
-      const uint32_t a0 = hmul2_u32(f16x2_from_e2m1x2(((mt & 1) ? hiA : loA) >> sh0), svA);
-      const uint32_t a1 = hmul2_u32(f16x2_from_e2m1x2(((mt & 1) ? hiA : loA) >> sh1), svA);
-      const uint32_t a2 = hmul2_u32(f16x2_from_e2m1x2(((mt & 1) ? hiB : loB) >> sh0), svB);
-      const uint32_t a3 = hmul2_u32(f16x2_from_e2m1x2(((mt & 1) ? hiB : loB) >> sh1), svB);
-      mma_f16_16816(st.o[mt], a0, a1, a2, a3, pbA, pbB);
+    for (int mt = 0; mt < D / 16; ++mt) {
+      // row g <-> channel (D/8) g + mt, row g+8 <-> (D/8) g + D/16 + mt
+      uint32_t a0, a1, a2, a3;
+      if constexpr (D == 128) {
+        a0 = (mt & 1) ? HA[0][mt >> 1] : LA[0][mt >> 1];
+        a1 = (mt & 1) ? HA[1][mt >> 1] : LA[1][mt >> 1];
+        a2 = (mt & 1) ? HB[0][mt >> 1] : LB[0][mt >> 1];
+        a3 = (mt & 1) ? HB[1][mt >> 1] : LB[1][mt >> 1];
+      } else {
+        a0 = (mt & 1) ? HA[0][mt >> 1] : LA[0][mt >> 1];
+        a1 = (mt & 1) ? HA[0][2 + (mt >> 1)] : LA[0][2 + (mt >> 1)];
+        a2 = (mt & 1) ? HB[0][mt >> 1] : LB[0][mt >> 1];
+        a3 = (mt & 1) ? HB[0][2 + (mt >> 1)] : LB[0][2 + (mt >> 1)];
+      }
+      mma_f16_16816(st.o[mt], hmul2_u32(a0, svA), hmul2_u32(a1, svA), hmul2_u32(a2, svB), hmul2_u32(a3, svB),
+                    pbA, pbB);
     }
   }
 }
@@ -609,8 +628,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       continue;
     }
     const int ntok = sm.ntok[s];
-    if (ntok > 16 * warp) {
-      process_slice<D>(p, st, sm.stages + s * G::kStageBytes, ntok, smem_addr(&sm.empty[s]));
+    if (ntok > 16 * kSlices * warp) {
+      consume_stage<D>(st, sm.stages + s * G::kStageBytes, ntok, smem_addr(&sm.empty[s]));
     } else {
       mbar_arrive(smem_addr(&sm.empty[s]));
     }
@@ -637,117 +656,106 @@ struct MergeParams {
   float qk_log2;
 };
 
-// One CTA per unit (b, kv head): FP8 window attention for the unit's query
-// rows (fp32 products x^ = E4M3(c) * s_h, fp32 dot products), then the
-// log-sum-exp merge of that window with every FP4 partial of the unit.
+// Block-wide reductions over 128 threads (4 warps).
+__device__ __forceinline__ float block_max128(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  return fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+}
+
+__device__ __forceinline__ float block_sum128(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  return (red[0] + red[1]) + (red[2] + red[3]);
+}
+
+// One CTA per (unit, query row of the group), one thread per channel: the FP8
+// window's softmax terms for that query row (fp32 values x^ = E4M3(c) * s_h,
+// fp32 dot products), then the log-sum-exp merge of that window with every
+// FP4 partial of the unit.
 __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
   extern __shared__ float msm[];
   const int D = p.head_dim;
-  const int u = blockIdx.x;
+  const int u = blockIdx.x / p.g, r = blockIdx.x % p.g;
   const int b = u / p.hkv, h = u % p.hkv;
   const int tid = threadIdx.x;
   int32_t T = __ldg(p.lens + b);
   if (T < 0) {
-    if (tid == 0 && h == 0) set_flag(p.flag, KVQ_FLAG_BAD_LENGTH);
+    if (tid == 0 && h == 0 && r == 0) set_flag(p.flag, KVQ_FLAG_BAD_LENGTH);
     T = 0;
   }
   const int w = (p.k8 != nullptr) ? min(p.window, T) : 0;
   const int nch = (T - w + kChunk - 1) / kChunk;
-  float* qs = msm;                       // [G][D]
-  float* sc = qs + kNG * D;              // [G][window]
-  float* mw = sc + kNG * max(p.window, 1);  // [G] window max
-  float* lw = mw + kNG;                  // [G] window sum
-  float* ow = lw + kNG;                  // [G][D] window numerator
+  const int64_t qrow = (int64_t)b * p.hq + (int64_t)h * p.g + r;
+  float mw = -INFINITY, lw = 0.0f, ow = 0.0f;
   if (w > 0) {
-    for (int i = tid; i < p.g * D; i += blockDim.x) {
-      const int r = i / D, ch = i % D;
-      const uint16_t bits = p.q[((int64_t)b * p.hq + (int64_t)h * p.g + r) * D + ch];
-      qs[i] = __uint_as_float((uint32_t)bits << 16);
-    }
+    float* qs = msm;             // [D]
+    float* sc = qs + D;          // [window]
+    float* red = sc + p.window;  // [4]
+    if (tid < D) qs[tid] = __uint_as_float((uint32_t)p.q[qrow * D + tid] << 16);
     __syncthreads();
     const float sk = __ldg(p.k8_scale + h), sv = __ldg(p.v8_scale + h);
+    const uint8_t* kbase = p.k8 + ((int64_t)b * p.hkv + h) * p.window * D;
+    const uint8_t* vbase = p.v8 + ((int64_t)b * p.hkv + h) * p.window * D;
+    float lmax = -INFINITY;
     for (int t = tid; t < w; t += blockDim.x) {
-      const int pos = T - w + t;
-      const uint8_t* krow = p.k8 + (((int64_t)b * p.hkv + h) * p.window + (pos % p.window)) * D;
-      float acc[kNG];
-#pragma unroll
-      for (int r = 0; r < kNG; ++r) acc[r] = 0.0f;
+      const uint8_t* krow = kbase + (int64_t)((T - w + t) % p.window) * D;
+      float acc = 0.0f;
       for (int ch = 0; ch < D; ch += 16) {
         const uint4 cw = *reinterpret_cast<const uint4*>(krow + ch);
         const uint32_t ws[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const float2 f = f16x2_to_float2(f16x2_from_e4m3x2((ws[q >> 1] >> (16 * (q & 1))) & 0xFFFFu));
-          const float x0 = f.x * sk, x1 = f.y * sk;
-#pragma unroll
-          for (int r = 0; r < kNG; ++r) {
-            if (r < p.g) {
-              acc[r] = fmaf(qs[r * D + ch + 2 * q], x0, acc[r]);
-              acc[r] = fmaf(qs[r * D + ch + 2 * q + 1], x1, acc[r]);
-            }
-          }
+          acc = fmaf(qs[ch + 2 * q], f.x * sk, acc);
+          acc = fmaf(qs[ch + 2 * q + 1], f.y * sk, acc);
         }
       }
-      for (int r = 0; r < p.g; ++r) sc[r * p.window + t] = acc[r] * p.qk_log2;
+      sc[t] = acc * p.qk_log2;
+      lmax = fmaxf(lmax, sc[t]);
     }
-    __syncthreads();
-    // per q row: max, then weights in place, then the sum
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int r = warp; r < p.g; r += 4) {
-      float mx = -INFINITY;
-      for (int t = lane; t < w; t += 32) mx = fmaxf(mx, sc[r * p.window + t]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-      float l = 0.0f;
-      for (int t = lane; t < w; t += 32) {
-        const float e = fast_exp2(sc[r * p.window + t] - mx);
-        sc[r * p.window + t] = e;
-        l += e;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
-      if (lane == 0) {
-        mw[r] = mx;
-        lw[r] = l;
-      }
+    mw = block_max128(lmax, red);
+    float lsum = 0.0f;
+    for (int t = tid; t < w; t += blockDim.x) {
+      const float e = fast_exp2(sc[t] - mw);
+      sc[t] = e;
+      lsum += e;
     }
-    __syncthreads();
-    for (int i = tid; i < p.g * D; i += blockDim.x) {
-      const int r = i / D, ch = i % D;
-      float o = 0.0f;
+    lw = block_sum128(lsum, red);  // its barriers also publish sc[]
+    if (tid < D) {
       for (int t = 0; t < w; ++t) {
-        const int pos = T - w + t;
-        const uint8_t c = p.v8[(((int64_t)b * p.hkv + h) * p.window + (pos % p.window)) * D + ch];
-        const float x = e4m3_to_f32(c) * sv;
-        o = fmaf(sc[r * p.window + t], x, o);
-      }
-      ow[i] = o;
-    }
-    __syncthreads();
-  }
-  int2 rec = make_int2(0, 0);
-  if (nch > 0) rec = p.unit_rec[u];
-  for (int i = tid; i < p.g * D; i += blockDim.x) {
-    const int r = i / D, ch = i % D;
-    float mx = w > 0 ? mw[r] : -INFINITY;
-    for (int k = 0; k < rec.y; ++k) mx = fmaxf(mx, p.part_ml[((int64_t)(rec.x + k) * p.g + r) * 2]);
-    float o = 0.0f, l = 0.0f;
-    if (mx != -INFINITY) {
-      if (w > 0) {
-        const float f = mw[r] == -INFINITY ? 0.0f : fast_exp2(mw[r] - mx);
-        o += f * ow[i];
-        l += f * lw[r];
-      }
-      for (int k = 0; k < rec.y; ++k) {
-        const int64_t sl = rec.x + k;
-        const float m = p.part_ml[(sl * p.g + r) * 2];
-        const float f = m == -INFINITY ? 0.0f : fast_exp2(m - mx);
-        o += f * p.part_o[(sl * p.g + r) * D + ch];
-        l += f * p.part_ml[(sl * p.g + r) * 2 + 1];
+        const float x = e4m3_to_f32(vbase[(int64_t)((T - w + t) % p.window) * D + tid]) * sv;
+        ow = fmaf(sc[t], x, ow);
       }
     }
-    p.out[((int64_t)b * p.hq + (int64_t)h * p.g + r) * D + ch] = l > 0.0f ? o / l : 0.0f;
   }
+  if (tid >= D) return;
+  const int2 rec = nch > 0 ? p.unit_rec[u] : make_int2(0, 0);
+  float mx = mw;
+  for (int k = 0; k < rec.y; ++k) mx = fmaxf(mx, p.part_ml[((int64_t)(rec.x + k) * p.g + r) * 2]);
+  float o = 0.0f, l = 0.0f;
+  if (mx != -INFINITY) {
+    if (w > 0 && mw != -INFINITY) {
+      const float f = fast_exp2(mw - mx);
+      o = f * ow;
+      l = f * lw;
+    }
+    for (int k = 0; k < rec.y; ++k) {
+      const int64_t sl = (int64_t)(rec.x + k) * p.g + r;
+      const float m = p.part_ml[sl * 2];
+      if (m == -INFINITY) continue;
+      const float f = fast_exp2(m - mx);
+      o = fmaf(f, p.part_o[sl * D + tid], o);
+      l = fmaf(f, p.part_ml[sl * 2 + 1], l);
+    }
+  }
+  p.out[qrow * D + tid] = l > 0.0f ? o / l : 0.0f;
 }
 
 // ------------------------------------------------------------------ host side
@@ -846,6 +854,7 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* global, const kvq_cache* 
   }
   if (D != 64 && D != 128) return KVQ_ERR_UNSUPPORTED;
   if (g > kNG) return KVQ_ERR_UNSUPPORTED;
+  if (swa != nullptr && swa->page_size > kMaxWindow) return KVQ_ERR_UNSUPPORTED;
   const int ctas = decode_ctas();
   if (ctas <= 0) return KVQ_ERR_CUDA;
   const WsLayout L = ws_layout(batch, hkv, g, D, ctas);
@@ -893,11 +902,7 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* global, const kvq_cache* 
   mp.hq = num_q_heads;
   mp.head_dim = D;
   mp.qk_log2 = dp.qk_log2;
-  if (swa && swa->page_size > kMaxWindow) return KVQ_ERR_UNSUPPORTED;
-  const int msmem = (kNG * D + kNG * (swa ? swa->page_size : 1) + 2 * kNG + kNG * D) * (int)sizeof(float);
-  if (msmem > 48 * 1024 &&
-      cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, msmem) != cudaSuccess)
-    return KVQ_ERR_CUDA;
-  merge_kernel<<<(unsigned)(batch * hkv), 128, msmem, s>>>(mp);
+  const int msmem = (D + (swa ? swa->page_size : 0) + 4) * (int)sizeof(float);
+  merge_kernel<<<(unsigned)(batch * hkv * g), 128, msmem, s>>>(mp);
   return launch_status();
 }
