@@ -74,34 +74,53 @@ __device__ __forceinline__ uint2 quantize_block(const Block16& b, uint32_t& scal
   return make_uint2(w0, w1);
 }
 
+// Spread 8 nibbles (nibble c at bits 4c) to 8 bytes (nibble c in the low half
+// of byte c).
+__device__ __forceinline__ uint64_t spread_nibbles(uint32_t w) {
+  uint64_t x = w;
+  x = (x | (x << 16)) & 0x0000FFFF0000FFFFull;
+  x = (x | (x << 8)) & 0x00FF00FF00FF00FFull;
+  x = (x | (x << 4)) & 0x0F0F0F0F0F0F0F0Full;
+  return x;
+}
+
+// Work items: first one per (sequence, new token, kv head, 16-channel block)
+// for K, then one per (sequence, token pair, kv head, block) for V.  A V item
+// owns the 16 interleaved bytes of its pair, so when only one token of the pair
+// is new it keeps the other token's nibbles (read-modify-write, one writer).
 __global__ void __launch_bounds__(256) append_fp4_kernel(const kvq_cache c, int32_t batch, int32_t n_new,
                                                          const int32_t* __restrict__ start_pos,
                                                          const uint16_t* __restrict__ k,
                                                          const uint16_t* __restrict__ v, int32_t* flag) {
-  const int nblk = c.head_dim >> 4;
+  const Fp4Layout L(c.head_dim, c.page_size);
+  const int nb = L.nb;
   const int Hkv = c.num_kv_heads;
-  const int P = c.page_size;
-  const int64_t total = (int64_t)batch * n_new * Hkv * nblk;
-  uint8_t* kc = static_cast<uint8_t*>(c.k_codes);
-  uint8_t* vc = static_cast<uint8_t*>(c.v_codes);
-  uint8_t* ks = static_cast<uint8_t*>(c.k_scales);
-  uint8_t* vs = static_cast<uint8_t*>(c.v_scales);
+  const int D = c.head_dim;
+  const int npair = n_new / 2 + 1;  // token pairs a call of n_new tokens can touch
+  const int64_t nk = (int64_t)batch * n_new * Hkv * nb;
+  const int64_t total = nk + (int64_t)batch * npair * Hkv * nb;
+  uint8_t* pool = static_cast<uint8_t*>(c.data);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int j = (int)(i % nblk);
-    int64_t r = i / nblk;
+    const bool is_k = i < nk;
+    const int64_t e = is_k ? i : i - nk;
+    const int j = (int)(e % nb);
+    int64_t r = e / nb;
     const int h = (int)(r % Hkv);
     r /= Hkv;
-    const int t = (int)(r % n_new);
-    const int b = (int)(r / n_new);
+    const int per = is_k ? n_new : npair;
+    const int t = (int)(r % per);
+    const int b = (int)(r / per);
     const int32_t sp = __ldg(start_pos + b);
     if (sp < 0) {
-      set_flag(flag, KVQ_FLAG_BAD_LENGTH);
+      if (is_k) set_flag(flag, KVQ_FLAG_BAD_LENGTH);
       continue;
     }
-    const int64_t pos = (int64_t)sp + t;
-    const int64_t pg = pos / P;
-    const int slot = (int)(pos % P);
+    // first position handled by this item (K: the token, V: the pair's even token)
+    const int64_t pos = is_k ? (int64_t)sp + t : 2 * (((int64_t)sp >> 1) + t);
+    if (!is_k && pos >= (int64_t)sp + n_new) continue;
+    const int64_t pg = pos / L.P;
+    const int slot = (int)(pos % L.P);
     if (pg >= c.max_pages_per_seq) {
       set_flag(flag, KVQ_FLAG_PAGE_OOB);
       continue;
@@ -112,17 +131,44 @@ __global__ void __launch_bounds__(256) append_fp4_kernel(const kvq_cache c, int3
       set_flag(flag, KVQ_FLAG_PAGE_OOB);
       continue;
     }
-    const int64_t row = (phys * Hkv + h) * P + slot;
-    const Block16 kb = load_bf16x16(k + i * 16);
-    const Block16 vb = load_bf16x16(v + i * 16);
-    if (!kb.finite || !vb.finite) set_flag(flag, KVQ_FLAG_NONFINITE);
-    uint32_t ksb, vsb;
-    const uint2 kq = quantize_block(kb, ksb);
-    const uint2 vq = quantize_block(vb, vsb);
-    *reinterpret_cast<uint2*>(kc + row * (c.head_dim >> 1) + 8 * j) = kq;
-    *reinterpret_cast<uint2*>(vc + row * (c.head_dim >> 1) + 8 * j) = vq;
-    ks[row * nblk + j] = (uint8_t)ksb;
-    vs[row * nblk + j] = (uint8_t)vsb;
+    uint8_t* grp = pool + L.group(phys, Hkv, h, slot);
+    const int ls = slot % L.G;
+    if (is_k) {
+      const Block16 kb = load_bf16x16(k + (((int64_t)b * n_new + t) * Hkv + h) * D + 16 * j);
+      if (!kb.finite) set_flag(flag, KVQ_FLAG_NONFINITE);
+      uint32_t sb;
+      const uint2 q = quantize_block(kb, sb);
+      *reinterpret_cast<uint2*>(grp + (int64_t)ls * (D / 2) + 8 * j) = q;
+      grp[L.k_scales() + (int64_t)ls * nb + j] = (uint8_t)sb;
+    } else {
+      uint4* dst = reinterpret_cast<uint4*>(grp + L.v_block(ls >> 1, j));
+      uint4 old = make_uint4(0u, 0u, 0u, 0u);
+      uint64_t lo = 0, hi = 0;  // interleaved bytes of channels 0-7 and 8-15
+      uint64_t keep_lo = 0, keep_hi = 0;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int64_t p = pos + half;
+        const bool mine = p >= sp && p < (int64_t)sp + n_new;
+        if (mine) {
+          const int tt = (int)(p - sp);
+          const Block16 vb = load_bf16x16(v + (((int64_t)b * n_new + tt) * Hkv + h) * D + 16 * j);
+          if (!vb.finite) set_flag(flag, KVQ_FLAG_NONFINITE);
+          uint32_t sb;
+          const uint2 q = quantize_block(vb, sb);
+          lo |= spread_nibbles(q.x) << (4 * half);
+          hi |= spread_nibbles(q.y) << (4 * half);
+          grp[L.v_scales() + (int64_t)j * L.G + ls + half] = (uint8_t)sb;
+        } else {
+          const uint64_t m = half ? 0xF0F0F0F0F0F0F0F0ull : 0x0F0F0F0F0F0F0F0Full;
+          keep_lo |= m;
+          keep_hi |= m;
+        }
+      }
+      if (keep_lo) old = *dst;
+      lo |= (((uint64_t)old.y << 32) | old.x) & keep_lo;
+      hi |= (((uint64_t)old.w << 32) | old.z) & keep_hi;
+      *dst = make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32));
+    }
   }
 }
 
@@ -146,8 +192,8 @@ __global__ void __launch_bounds__(256) append_fp8_kernel(const kvq_cache c, int3
   const int Hkv = c.num_kv_heads;
   const int W = c.page_size;
   const int64_t total = (int64_t)batch * n_new * Hkv * nblk;
-  const float* ksc = static_cast<const float*>(c.k_scales);
-  const float* vsc = static_cast<const float*>(c.v_scales);
+  const float* ksc = static_cast<const float*>(c.k_scale);
+  const float* vsc = static_cast<const float*>(c.v_scale);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int j = (int)(i % nblk);
@@ -174,7 +220,7 @@ __global__ void __launch_bounds__(256) append_fp8_kernel(const kvq_cache c, int3
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         w[q] = e4m3_pair(blk.x[4 * q], blk.x[4 * q + 1], s) | (e4m3_pair(blk.x[4 * q + 2], blk.x[4 * q + 3], s) << 16);
-      uint8_t* base = static_cast<uint8_t*>(side ? c.v_codes : c.k_codes);
+      uint8_t* base = static_cast<uint8_t*>(side ? c.v_data : c.data);
       *reinterpret_cast<uint4*>(base + dst) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
@@ -215,7 +261,7 @@ __global__ void __launch_bounds__(256) fp8_scales_kernel(const kvq_cache c, int6
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) a = fmaxf(a, red[w]);
     if (bad) set_flag(flag, KVQ_FLAG_NONFINITE);
     const float s = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 448.0f);
-    static_cast<float*>(side ? c.v_scales : c.k_scales)[h] = s;
+    static_cast<float*>(side ? c.v_scale : c.k_scale)[h] = s;
   }
 }
 
@@ -232,7 +278,7 @@ extern "C" kvq_status kvq_append(const kvq_cache* cache, int32_t batch, int32_t 
   if (batch == 0 || n_new == 0) return KVQ_OK;
   if (d_start_pos == nullptr || k == nullptr || v == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
   if (!aligned_to(k, 16) || !aligned_to(v, 16)) return KVQ_ERR_INVALID_ARGUMENT;
-  const int64_t work = (int64_t)batch * n_new * cache->num_kv_heads * (cache->head_dim / 16);
+  const int64_t work = (int64_t)batch * (n_new + n_new / 2 + 1) * cache->num_kv_heads * (cache->head_dim / 16);
   const unsigned grid = grid_for(work, 256);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cache->format == KVQ_FORMAT_FP4_E2M1_E4M3_G16) {
@@ -271,3 +317,10 @@ extern "C" const char* kvq_status_string(kvq_status status) {
 }
 
 extern "C" int32_t kvq_version(void) { return KVQ_VERSION; }
+
+extern "C" size_t kvq_fp4_pool_bytes(int64_t num_pages, int32_t num_kv_heads, int32_t page_size, int32_t head_dim) {
+  if (num_pages < 0 || num_kv_heads < 1 || !is_pow2_page(page_size) ||
+      (head_dim != 64 && head_dim != 128 && head_dim != 256))
+    return 0;
+  return (size_t)num_pages * (size_t)num_kv_heads * (size_t)page_size * 9u * (size_t)head_dim / 8u;
+}

@@ -204,6 +204,32 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// ---------------------------------------------------------------- FP4 page-pool layout
+// One group = min(page_size, 128) tokens of one kv head, stored as a
+// contiguous block: K codes [G][D/2], K scales [G][D/16], V codes [G/2][D]
+// (token pairs interleaved by nibble, 16-byte or 8-byte chunks permuted per
+// row), V scales [D/16][G].  9*D/8 bytes per token.
+struct Fp4Layout {
+  int D, P, G, nb;
+  int64_t group_bytes;
+  __host__ __device__ Fp4Layout(int head_dim, int page_size)
+      : D(head_dim), P(page_size), G(page_size < 128 ? page_size : 128), nb(head_dim / 16),
+        group_bytes((int64_t)(page_size < 128 ? page_size : 128) * 9 * head_dim / 8) {}
+  __host__ __device__ int64_t k_scales() const { return (int64_t)G * D / 2; }
+  __host__ __device__ int64_t v_codes() const { return (int64_t)G * (D / 2 + nb); }
+  __host__ __device__ int64_t v_scales() const { return (int64_t)G * (D + nb); }
+  // byte offset of the group holding (physical page, kv head, slot)
+  __host__ __device__ int64_t group(int64_t phys, int hkv, int h, int slot) const {
+    return ((phys * hkv + h) * (P / G) + slot / G) * group_bytes;
+  }
+  // byte offset, inside a group, of the 16 V-code bytes of channels [16j, 16j+16)
+  // of token pair row i (the permutation keeps these 16 bytes contiguous)
+  __host__ __device__ int64_t v_block(int i, int j) const {
+    if (D == 64) return v_codes() + (int64_t)i * D + 8 * ((2 * j) ^ (((i >> 1) & 1) << 2));
+    return v_codes() + (int64_t)i * D + 16 * (j ^ ((i & 3) << 1));
+  }
+};
+
 // ---------------------------------------------------------------- host helpers
 struct HostCheck {
   static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

@@ -46,6 +46,7 @@ constexpr int kConsumerWarps = 4;
 constexpr int kSlices = kChunk / (16 * kConsumerWarps);  // 16-token slices per warp per stage
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kStages = 4;
+constexpr int kMaxCopies = kChunk / 16;  // pool groups per stage at the smallest page size
 constexpr int kNG = 8;  // query rows per kv head held by one tile (G <= 8)
 constexpr float kLazySlack = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -53,15 +54,8 @@ constexpr int kMaxWindow = 1024;
 
 template <int D>
 struct Geo {
-  static constexpr int kCodeRow = D / 2;
-  static constexpr int kScaleRow = D / 16;
-  static constexpr int kCodeBytes = kChunk * kCodeRow;
-  static constexpr int kScaleBytes = kChunk * kScaleRow;
-  static constexpr int kOffK = 0;
-  static constexpr int kOffV = kCodeBytes;
-  static constexpr int kOffKS = 2 * kCodeBytes;
-  static constexpr int kOffVS = 2 * kCodeBytes + kScaleBytes;
-  static constexpr int kStageBytes = ((2 * kCodeBytes + 2 * kScaleBytes) + 1023) / 1024 * 1024;
+  // a stage holds kChunk tokens = kChunk / min(P, kChunk) consecutive pool groups
+  static constexpr int kStageBytes = (kChunk * 9 * D / 8 + 1023) / 1024 * 1024;
   // flush buffer: O[warp][row][D], M[warp][row], L[warp][row]
   static constexpr int kFlushBytes = kConsumerWarps * kNG * (D + 2) * 4;
   static constexpr int kSmemBytes = kStages * kStageBytes + kFlushBytes + 2 * kStages * 8 + kStages * 4 + 16 + 1024;
@@ -70,8 +64,7 @@ struct Geo {
 struct DecodeParams {
   const int32_t* lens;
   const int32_t* page_table;
-  const uint8_t* k_scales;
-  const uint8_t* v_scales;
+  const uint8_t* pool;
   const uint16_t* q;
   float* part_o;
   float* part_ml;
@@ -203,11 +196,10 @@ __device__ __forceinline__ Smem<D> carve(uint8_t* raw) {
 
 // ------------------------------------------------------------------ producer
 template <int D>
-__device__ void producer(const DecodeParams& p, const CUtensorMap* tmk, const CUtensorMap* tmv, Smem<D>& sm,
-                         Walker wk, int64_t v1) {
+__device__ void producer(const DecodeParams& p, Smem<D>& sm, Walker wk, int64_t v1) {
   using G = Geo<D>;
   const int P = p.page;
-  const int rows_per_copy = P < kChunk ? P : kChunk;
+  const Fp4Layout L(D, P);
   uint32_t it = 0;
   for (; wk.v < v1; advance(p, wk), ++it) {
     const uint32_t s = it % kStages;
@@ -222,10 +214,10 @@ __device__ void producer(const DecodeParams& p, const CUtensorMap* tmk, const CU
     const int n4 = fp4_tokens(__ldg(p.lens + wk.b), p.window);
     const int tok0 = wk.c * kChunk;
     const int ntok = min(kChunk, n4 - tok0);
+    // one copy per pool group: a 128-token group of a larger page, or whole small pages
     const int ncopies = P < kChunk ? (ntok + P - 1) / P : 1;
     const int pg0 = tok0 / P;
-    const int off0 = P < kChunk ? 0 : tok0 % P;
-    int64_t phys[kChunk / 16];
+    int64_t src[kMaxCopies];
     bool ok = true;
     for (int i = 0; i < ncopies; ++i) {
       const int pg = pg0 + i;
@@ -234,7 +226,7 @@ __device__ void producer(const DecodeParams& p, const CUtensorMap* tmk, const CU
         ph = p.page_table ? (int64_t)__ldg(p.page_table + (int64_t)wk.b * p.max_pages + pg)
                           : (int64_t)wk.b * p.max_pages + pg;
       if (ph < 0 || ph >= p.num_pages) ok = false;
-      phys[i] = ph;
+      src[i] = L.group(ph, p.hkv, wk.h, P < kChunk ? 0 : tok0 % P);
     }
     const uint32_t full = smem_addr(&sm.full[s]);
     uint8_t* st = sm.stages + s * G::kStageBytes;
@@ -245,21 +237,9 @@ __device__ void producer(const DecodeParams& p, const CUtensorMap* tmk, const CU
       continue;
     }
     sm.ntok[s] = ntok;
-    const uint32_t code_bytes = (uint32_t)(ncopies * rows_per_copy * G::kCodeRow);
-    const uint32_t scale_bytes = (uint32_t)(ncopies * rows_per_copy * G::kScaleRow);
-    mbar_arrive_expect_tx(full, 2 * code_bytes + 2 * scale_bytes);
-    for (int i = 0; i < ncopies; ++i) {
-      const int64_t row0 = (phys[i] * p.hkv + wk.h) * P + off0;  // token row in the pool
-      const int z = (int)(phys[i] * p.hkv + wk.h);
-      const uint32_t dk = smem_addr(st + G::kOffK + i * rows_per_copy * G::kCodeRow);
-      const uint32_t dv = smem_addr(st + G::kOffV + i * rows_per_copy * G::kCodeRow);
-      tma_load_3d(dk, tmk, 0, off0, z, full);
-      tma_load_3d(dv, tmv, 0, off0, z, full);
-      bulk_g2s(smem_addr(st + G::kOffKS + i * rows_per_copy * G::kScaleRow), p.k_scales + row0 * G::kScaleRow,
-               rows_per_copy * G::kScaleRow, full);
-      bulk_g2s(smem_addr(st + G::kOffVS + i * rows_per_copy * G::kScaleRow), p.v_scales + row0 * G::kScaleRow,
-               rows_per_copy * G::kScaleRow, full);
-    }
+    mbar_arrive_expect_tx(full, (uint32_t)(ncopies * L.group_bytes));
+    for (int i = 0; i < ncopies; ++i)
+      bulk_g2s(smem_addr(st + i * L.group_bytes), p.pool + src[i], (uint32_t)L.group_bytes, full);
   }
   // Wait for every copy still in flight before the CTA can retire.
   const uint32_t issued = it;
@@ -331,59 +311,56 @@ __device__ __forceinline__ void begin_unit(const DecodeParams& p, ConsumerState<
 }
 
 // One stage for one consumer warp: two 16-token slices, rows [32w, 32w+32).
+// The stage holds pool groups of `gt` = min(page_size, 128) tokens back to back
+// (see Fp4Layout); a 16-token slice never straddles two groups.
 template <int D>
-__device__ __forceinline__ void consume_stage(ConsumerState<D>& st, const uint8_t* stage, int ntok,
-                                              uint32_t empty_bar) {
-  using G = Geo<D>;
+__device__ __forceinline__ void consume_stage(ConsumerState<D>& st, const uint8_t* stage, const Fp4Layout& L,
+                                              int ntok, uint32_t empty_bar) {
   constexpr int KW = D / 32;  // words of K codes per thread per row (channels [tig*D/4, +D/4))
-  constexpr int VW = D / 64;  // words of V codes per thread per row (channels [g*D/8, +D/8))
+  constexpr int VW = D / 32;  // words of V codes per thread per token pair (channels [g*D/8, +D/8))
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int g = lane >> 2, tig = lane & 3;
-  const uint8_t* sK = stage + G::kOffK;
-  const uint8_t* sV = stage + G::kOffV;
-  const uint8_t* sKS = stage + G::kOffKS;
-  const uint8_t* sVS = stage + G::kOffVS;
 
   // ---- loads from the stage, then release it
   uint32_t kw[kSlices][2][KW];  // rows g, g+8 of each slice
   uint32_t ksb[kSlices][2];     // their scale bytes (blocks of this thread's channels)
-  uint32_t vw[kSlices][4][VW];  // rows 2t, 2t+1, 2t+8, 2t+9 of each slice
-  uint32_t vsb[kSlices][2];     // scale-byte pairs (2t, 2t+1) and (2t+8, 2t+9), block of g
+  uint32_t vw[kSlices][2][VW];  // token pairs (2t, 2t+1) and (2t+8, 2t+9): interleaved code bytes
+  uint32_t vsb[kSlices][2];     // their scale-byte pairs, block of this thread's channels
 #pragma unroll
   for (int sl = 0; sl < kSlices; ++sl) {
     const int r0 = 16 * (kSlices * warp + sl);
-    const int ra = r0 + g, rb = r0 + g + 8;
-    const int vr[4] = {r0 + 2 * tig, r0 + 2 * tig + 1, r0 + 2 * tig + 8, r0 + 2 * tig + 9};
+    const uint8_t* grp = stage + (r0 / L.G) * L.group_bytes;
+    const int lr = r0 % L.G;
+    const int ra = lr + g, rb = lr + g + 8;
+    const int iA = (lr >> 1) + tig, iB = iA + 4;  // token-pair rows
+    const int blk = D == 128 ? g : (g >> 1);       // V scale block of this thread's channels
     if constexpr (D == 128) {
-      const int gr = tig ^ ((ra >> 1) & 3);  // 64-byte swizzle: granule ^= (row >> 1) & 3
-      const uint4 a = *reinterpret_cast<const uint4*>(sK + ra * 64 + gr * 16);
-      const uint4 b = *reinterpret_cast<const uint4*>(sK + rb * 64 + gr * 16);
+      const uint4 a = *reinterpret_cast<const uint4*>(grp + ra * 64 + 16 * tig);
+      const uint4 b = *reinterpret_cast<const uint4*>(grp + rb * 64 + 16 * tig);
       kw[sl][0][0] = a.x; kw[sl][0][1] = a.y; kw[sl][0][2] = a.z; kw[sl][0][3] = a.w;
       kw[sl][1][0] = b.x; kw[sl][1][1] = b.y; kw[sl][1][2] = b.z; kw[sl][1][3] = b.w;
-      ksb[sl][0] = *reinterpret_cast<const uint16_t*>(sKS + ra * 8 + 2 * tig);
-      ksb[sl][1] = *reinterpret_cast<const uint16_t*>(sKS + rb * 8 + 2 * tig);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int gv = (g >> 1) ^ ((vr[i] >> 1) & 3);
-        const uint2 x = *reinterpret_cast<const uint2*>(sV + vr[i] * 64 + gv * 16 + 8 * (g & 1));
-        vw[sl][i][0] = x.x;
-        vw[sl][i][1] = x.y;
-      }
-      vsb[sl][0] = sVS[vr[0] * 8 + g] | (sVS[vr[1] * 8 + g] << 8);
-      vsb[sl][1] = sVS[vr[2] * 8 + g] | (sVS[vr[3] * 8 + g] << 8);
+      ksb[sl][0] = *reinterpret_cast<const uint16_t*>(grp + L.k_scales() + ra * 8 + 2 * tig);
+      ksb[sl][1] = *reinterpret_cast<const uint16_t*>(grp + L.k_scales() + rb * 8 + 2 * tig);
+      const uint4 x = *reinterpret_cast<const uint4*>(grp + L.v_block(iA, g));
+      const uint4 y = *reinterpret_cast<const uint4*>(grp + L.v_block(iB, g));
+      vw[sl][0][0] = x.x; vw[sl][0][1] = x.y; vw[sl][0][2] = x.z; vw[sl][0][3] = x.w;
+      vw[sl][1][0] = y.x; vw[sl][1][1] = y.y; vw[sl][1][2] = y.z; vw[sl][1][3] = y.w;
     } else {
-      const uint2 a = *reinterpret_cast<const uint2*>(sK + ra * 32 + 8 * tig);
-      const uint2 b = *reinterpret_cast<const uint2*>(sK + rb * 32 + 8 * tig);
+      const uint2 a = *reinterpret_cast<const uint2*>(grp + ra * 32 + 8 * tig);
+      const uint2 b = *reinterpret_cast<const uint2*>(grp + rb * 32 + 8 * tig);
       kw[sl][0][0] = a.x; kw[sl][0][1] = a.y;
       kw[sl][1][0] = b.x; kw[sl][1][1] = b.y;
-      ksb[sl][0] = sKS[ra * 4 + tig];
-      ksb[sl][1] = sKS[rb * 4 + tig];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) vw[sl][i][0] = *reinterpret_cast<const uint32_t*>(sV + vr[i] * 32 + 4 * g);
-      vsb[sl][0] = sVS[vr[0] * 4 + (g >> 1)] | (sVS[vr[1] * 4 + (g >> 1)] << 8);
-      vsb[sl][1] = sVS[vr[2] * 4 + (g >> 1)] | (sVS[vr[3] * 4 + (g >> 1)] << 8);
+      ksb[sl][0] = grp[L.k_scales() + ra * 4 + tig];
+      ksb[sl][1] = grp[L.k_scales() + rb * 4 + tig];
+      // 8-byte chunk g of each pair row, chunk index permuted by ((i >> 1) & 1) << 2
+      const uint2 x = *reinterpret_cast<const uint2*>(grp + L.v_codes() + iA * 64 + 8 * (g ^ (((iA >> 1) & 1) << 2)));
+      const uint2 y = *reinterpret_cast<const uint2*>(grp + L.v_codes() + iB * 64 + 8 * (g ^ (((iB >> 1) & 1) << 2)));
+      vw[sl][0][0] = x.x; vw[sl][0][1] = x.y;
+      vw[sl][1][0] = y.x; vw[sl][1][1] = y.y;
     }
+    vsb[sl][0] = *reinterpret_cast<const uint16_t*>(grp + L.v_scales() + blk * L.G + lr + 2 * tig);
+    vsb[sl][1] = *reinterpret_cast<const uint16_t*>(grp + L.v_scales() + blk * L.G + lr + 2 * tig + 8);
   }
   mbar_arrive(empty_bar);
 
@@ -484,33 +461,24 @@ __device__ __forceinline__ void consume_stage(ConsumerState<D>& st, const uint8_
     }
     const uint32_t svA = f16x2_from_e4m3x2(vsA);
     const uint32_t svB = f16x2_from_e4m3x2(vsB);
-    // nibble interleave: byte i of lo = (token a, token b) codes of channel 2i, hi: channel 2i+1
-    uint32_t LA[VW][4], HA[VW][4], LB[VW][4], HB[VW][4];
+    // byte c of a pair row = channel c of tokens (2t, 2t+1) -> f16x2 (low, high)
+    uint32_t VA[4 * VW], VB[4 * VW];
 #pragma unroll
     for (int w = 0; w < VW; ++w) {
-      const uint32_t a0 = vw[sl][0][w], a1 = vw[sl][1][w], b0 = vw[sl][2][w], b1 = vw[sl][3][w];
-      f16x2x4_from_e2m1x8((a0 & 0x0F0F0F0Fu) | ((a1 & 0x0F0F0F0Fu) << 4), LA[w]);
-      f16x2x4_from_e2m1x8(((a0 >> 4) & 0x0F0F0F0Fu) | (a1 & 0xF0F0F0F0u), HA[w]);
-      f16x2x4_from_e2m1x8((b0 & 0x0F0F0F0Fu) | ((b1 & 0x0F0F0F0Fu) << 4), LB[w]);
-      f16x2x4_from_e2m1x8(((b0 >> 4) & 0x0F0F0F0Fu) | (b1 & 0xF0F0F0F0u), HB[w]);
+      uint32_t ta[4], tb[4];
+      f16x2x4_from_e2m1x8(vw[sl][0][w], ta);
+      f16x2x4_from_e2m1x8(vw[sl][1][w], tb);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        VA[4 * w + k] = ta[k];
+        VB[4 * w + k] = tb[k];
+      }
     }
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
       // row g <-> channel (D/8) g + mt, row g+8 <-> (D/8) g + D/16 + mt
-      uint32_t a0, a1, a2, a3;
-      if constexpr (D == 128) {
-        a0 = (mt & 1) ? HA[0][mt >> 1] : LA[0][mt >> 1];
-        a1 = (mt & 1) ? HA[1][mt >> 1] : LA[1][mt >> 1];
-        a2 = (mt & 1) ? HB[0][mt >> 1] : LB[0][mt >> 1];
-        a3 = (mt & 1) ? HB[1][mt >> 1] : LB[1][mt >> 1];
-      } else {
-        a0 = (mt & 1) ? HA[0][mt >> 1] : LA[0][mt >> 1];
-        a1 = (mt & 1) ? HA[0][2 + (mt >> 1)] : LA[0][2 + (mt >> 1)];
-        a2 = (mt & 1) ? HB[0][mt >> 1] : LB[0][mt >> 1];
-        a3 = (mt & 1) ? HB[0][2 + (mt >> 1)] : LB[0][2 + (mt >> 1)];
-      }
-      mma_f16_16816(st.o[mt], hmul2_u32(a0, svA), hmul2_u32(a1, svA), hmul2_u32(a2, svB), hmul2_u32(a3, svB),
-                    pbA, pbB);
+      mma_f16_16816(st.o[mt], hmul2_u32(VA[mt], svA), hmul2_u32(VA[D / 16 + mt], svA), hmul2_u32(VB[mt], svB),
+                    hmul2_u32(VB[D / 16 + mt], svB), pbA, pbB);
     }
   }
 }
@@ -568,8 +536,7 @@ __device__ void flush_unit(const DecodeParams& p, ConsumerState<D>& st, Smem<D>&
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 2)
-    decode_fp4_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                      const DecodeParams p) {
+    decode_fp4_kernel(const DecodeParams p) {
   using G = Geo<D>;
   extern __shared__ uint8_t smem_raw[];
   Smem<D> sm = carve<D>(smem_raw);
@@ -591,14 +558,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (warp == kConsumerWarps) {
     if (lane == 0) {
-      prefetch_tensormap(&tmk);
-      prefetch_tensormap(&tmv);
-      producer<D>(p, &tmk, &tmv, sm, wk, v1);
+      producer<D>(p, sm, wk, v1);
     }
     return;
   }
 
   const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+  const Fp4Layout lay(D, p.page);
   ConsumerState<D> st;
   bool have = false, dead = false;
   int64_t slot = 0;
@@ -629,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const int ntok = sm.ntok[s];
     if (ntok > 16 * kSlices * warp) {
-      consume_stage<D>(st, sm.stages + s * G::kStageBytes, ntok, smem_addr(&sm.empty[s]));
+      consume_stage<D>(st, sm.stages + s * G::kStageBytes, lay, ntok, smem_addr(&sm.empty[s]));
     } else {
       mbar_arrive(smem_addr(&sm.empty[s]));
     }
@@ -759,31 +725,6 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
 }
 
 // ------------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-  void* fn = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-          cudaSuccess ||
-      q != cudaDriverEntryPointSuccess)
-    return nullptr;
-  return reinterpret_cast<EncodeTiledFn>(fn);
-}
-
-bool make_code_map(EncodeTiledFn enc, CUtensorMap* map, void* base, const kvq_cache& c) {
-  const cuuint64_t row = (cuuint64_t)c.head_dim / 2;
-  cuuint64_t dims[3] = {row, (cuuint64_t)c.page_size, (cuuint64_t)c.num_pages * (cuuint64_t)c.num_kv_heads};
-  cuuint64_t strides[2] = {row, row * (cuuint64_t)c.page_size};
-  cuuint32_t box[3] = {(cuuint32_t)row, (cuuint32_t)(c.page_size < kChunk ? c.page_size : kChunk), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapSwizzle sw = c.head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE;
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 struct WsLayout {
   size_t rec_off, ml_off, o_off, total;
 };
@@ -803,16 +744,11 @@ WsLayout ws_layout(int64_t batch, int64_t hkv, int64_t g, int64_t d, int64_t cta
 int decode_ctas() { return 2 * device_sm_count(); }
 
 template <int D>
-kvq_status launch_decode(const kvq_cache& gc, const DecodeParams& dp, cudaStream_t s, int ctas) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (enc == nullptr) return KVQ_ERR_CUDA;
-  CUtensorMap tmk, tmv;
-  if (!make_code_map(enc, &tmk, gc.k_codes, gc) || !make_code_map(enc, &tmv, gc.v_codes, gc))
-    return KVQ_ERR_INVALID_ARGUMENT;
+kvq_status launch_decode(const DecodeParams& dp, cudaStream_t s, int ctas) {
   const int smem = Geo<D>::kSmemBytes;
   if (cudaFuncSetAttribute(decode_fp4_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return KVQ_ERR_CUDA;
-  decode_fp4_kernel<D><<<ctas, kThreads, smem, s>>>(tmk, tmv, dp);
+  decode_fp4_kernel<D><<<ctas, kThreads, smem, s>>>(dp);
   return launch_status();
 }
 
@@ -865,8 +801,7 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* global, const kvq_cache* 
   DecodeParams dp;
   dp.lens = d_seq_lens;
   dp.page_table = global->page_table;
-  dp.k_scales = static_cast<const uint8_t*>(global->k_scales);
-  dp.v_scales = static_cast<const uint8_t*>(global->v_scales);
+  dp.pool = static_cast<const uint8_t*>(global->data);
   dp.q = static_cast<const uint16_t*>(q);
   dp.part_o = reinterpret_cast<float*>(ws + L.o_off);
   dp.part_ml = reinterpret_cast<float*>(ws + L.ml_off);
@@ -881,7 +816,7 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* global, const kvq_cache* 
   dp.max_pages = global->max_pages_per_seq;
   dp.window = swa ? swa->page_size : 0;
   dp.qk_log2 = softmax_scale * kLog2e;
-  st = D == 128 ? launch_decode<128>(*global, dp, s, ctas) : launch_decode<64>(*global, dp, s, ctas);
+  st = D == 128 ? launch_decode<128>(dp, s, ctas) : launch_decode<64>(dp, s, ctas);
   if (st != KVQ_OK) return st;
 
   MergeParams mp;
@@ -892,10 +827,10 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* global, const kvq_cache* 
   mp.unit_rec = dp.unit_rec;
   mp.out = out;
   mp.flag = d_err_flag;
-  mp.k8 = swa ? static_cast<const uint8_t*>(swa->k_codes) : nullptr;
-  mp.v8 = swa ? static_cast<const uint8_t*>(swa->v_codes) : nullptr;
-  mp.k8_scale = swa ? static_cast<const float*>(swa->k_scales) : nullptr;
-  mp.v8_scale = swa ? static_cast<const float*>(swa->v_scales) : nullptr;
+  mp.k8 = swa ? static_cast<const uint8_t*>(swa->data) : nullptr;
+  mp.v8 = swa ? static_cast<const uint8_t*>(swa->v_data) : nullptr;
+  mp.k8_scale = swa ? static_cast<const float*>(swa->k_scale) : nullptr;
+  mp.v8_scale = swa ? static_cast<const float*>(swa->v_scale) : nullptr;
   mp.window = swa ? swa->page_size : 0;
   mp.hkv = hkv;
   mp.g = g;

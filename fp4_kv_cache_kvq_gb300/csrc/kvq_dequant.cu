@@ -1,7 +1,8 @@
 // kvq_dequant.cu -- expand a cache to dense fp32 or bf16 values.
 //
 // FP4: value = E2M1(code) * E4M3(scale) ("Quantising the KV cache", section
-// "Code": the stored value is the rounded code times its block scale).  The
+// "Code": the stored value is the rounded code times its block scale), read
+// from the page pool's group layout (K by token, V by interleaved token pair).  The
 // product has at most 6 significant bits and lies in [2^-10, 2688], so it is
 // exact in fp32, f16 and bf16.  FP8 window: value = fp32(E4M3(code) * s_h).
 //
@@ -58,7 +59,9 @@ __global__ void __launch_bounds__(256) dequant_fp4_kernel(const kvq_cache c, int
       set_flag(flag, KVQ_FLAG_BAD_LENGTH);
       ok = false;
     }
-    int64_t row = 0;
+    const Fp4Layout L(c.head_dim, c.page_size);
+    const uint8_t* grp = nullptr;
+    int ls = 0;
     if (ok) {
       const int pg = pos / P;
       const int64_t phys = pg >= c.max_pages_per_seq ? -1
@@ -67,24 +70,33 @@ __global__ void __launch_bounds__(256) dequant_fp4_kernel(const kvq_cache c, int
       if (phys < 0 || phys >= c.num_pages) {
         set_flag(flag, KVQ_FLAG_PAGE_OOB);
         ok = false;
+      } else {
+        grp = static_cast<const uint8_t*>(c.data) + L.group(phys, Hkv, h, pos % P);
+        ls = (pos % P) % L.G;
       }
-      row = (phys * Hkv + h) * P + (pos % P);
     }
     if (ok) {
+      // K: 8 code bytes (channels 2k, 2k+1 per byte) and the block's scale
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(grp + (int64_t)ls * (c.head_dim / 2) + 8 * j));
+      const float sk = e4m3_to_f32(__ldg(grp + L.k_scales() + (int64_t)ls * nblk + j));
 #pragma unroll
-      for (int side = 0; side < 2; ++side) {
-        const uint8_t* codes = static_cast<const uint8_t*>(side ? c.v_codes : c.k_codes);
-        const uint8_t* scales = static_cast<const uint8_t*>(side ? c.v_scales : c.k_scales);
-        const uint2 w = __ldg(reinterpret_cast<const uint2*>(codes + row * (c.head_dim >> 1) + 8 * j));
-        const float s = e4m3_to_f32(__ldg(scales + row * nblk + j));
-        float* x = side ? vx : kx;
+      for (int q = 0; q < 8; ++q) {
+        const float2 f = f16x2_to_float2(f16x2_from_e2m1x2(((q < 4 ? w.x : w.y) >> (8 * (q & 3))) & 0xFFu));
+        kx[2 * q] = f.x * sk;
+        kx[2 * q + 1] = f.y * sk;
+      }
+      // V: 16 interleaved bytes of the token pair; this token's nibbles
+      const uint4 vw = __ldg(reinterpret_cast<const uint4*>(grp + L.v_block(ls >> 1, j)));
+      const float sv = e4m3_to_f32(__ldg(grp + L.v_scales() + (int64_t)j * L.G + ls));
+      const uint32_t ws[4] = {vw.x, vw.y, vw.z, vw.w};
+      const int sh = 4 * (ls & 1);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint32_t byte = ((q < 4 ? w.x : w.y) >> (8 * (q & 3))) & 0xFFu;
-          const float2 f = f16x2_to_float2(f16x2_from_e2m1x2(byte));
-          x[2 * q] = f.x * s;
-          x[2 * q + 1] = f.y * s;
-        }
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t b0 = (ws[q >> 1] >> (16 * (q & 1) + sh)) & 0xFu;
+        const uint32_t b1 = (ws[q >> 1] >> (16 * (q & 1) + 8 + sh)) & 0xFu;
+        const float2 f = f16x2_to_float2(f16x2_from_e2m1x2(b0 | (b1 << 4)));
+        vx[2 * q] = f.x * sv;
+        vx[2 * q + 1] = f.y * sv;
       }
     }
     store16(k_out, i * 16, kx, out_dtype);
@@ -109,8 +121,8 @@ __global__ void __launch_bounds__(256) dequant_fp8_kernel(const kvq_cache c, int
     const int64_t src = (((int64_t)b * Hkv + h) * W + slot) * c.head_dim + 16 * j;
 #pragma unroll
     for (int side = 0; side < 2; ++side) {
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(side ? c.v_codes : c.k_codes) + src));
-      const float s = __ldg(static_cast<const float*>(side ? c.v_scales : c.k_scales) + h);
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(side ? c.v_data : c.data) + src));
+      const float s = __ldg(static_cast<const float*>(side ? c.v_scale : c.k_scale) + h);
       const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
       float x[16];
 #pragma unroll

@@ -15,25 +15,25 @@ inline bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<ui
 
 // Validates a cache description for `batch` sequences.
 inline kvq_status check_cache(const kvq_cache* c, int32_t batch) {
-  if (c == nullptr || c->reserved != 0) return KVQ_ERR_INVALID_ARGUMENT;
-  if (c->num_kv_heads < 1 || c->head_dim < 16 || c->head_dim > 512 || (c->head_dim % 16) != 0)
-    return KVQ_ERR_INVALID_ARGUMENT;
-  if (c->k_codes == nullptr || c->v_codes == nullptr || c->k_scales == nullptr || c->v_scales == nullptr)
-    return KVQ_ERR_INVALID_ARGUMENT;
-  if (!aligned_to(c->k_codes, 16) || !aligned_to(c->v_codes, 16)) return KVQ_ERR_INVALID_ARGUMENT;
+  if (c == nullptr || c->reserved != 0 || c->num_kv_heads < 1 || c->data == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+  if (!aligned_to(c->data, 16)) return KVQ_ERR_INVALID_ARGUMENT;
   if (c->format == KVQ_FORMAT_FP4_E2M1_E4M3_G16) {
+    if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return KVQ_ERR_INVALID_ARGUMENT;
     if (!is_pow2_page(c->page_size) || c->num_pages < 1 || c->max_pages_per_seq < 1)
       return KVQ_ERR_INVALID_ARGUMENT;
-    if (!aligned_to(c->k_scales, 16) || !aligned_to(c->v_scales, 16)) return KVQ_ERR_INVALID_ARGUMENT;
+    if (c->v_data != nullptr || c->k_scale != nullptr || c->v_scale != nullptr) return KVQ_ERR_INVALID_ARGUMENT;
     if (c->page_table == nullptr && (int64_t)batch * c->max_pages_per_seq > c->num_pages)
       return KVQ_ERR_INVALID_ARGUMENT;
     if (c->num_pages * (int64_t)c->num_kv_heads > (int64_t)INT32_MAX) return KVQ_ERR_UNSUPPORTED;
     return KVQ_OK;
   }
   if (c->format == KVQ_FORMAT_FP8_E4M3_HEAD) {
+    if (c->head_dim < 16 || c->head_dim > 512 || (c->head_dim % 16) != 0) return KVQ_ERR_INVALID_ARGUMENT;
+    if (c->v_data == nullptr || c->k_scale == nullptr || c->v_scale == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+    if (!aligned_to(c->v_data, 16)) return KVQ_ERR_INVALID_ARGUMENT;
     if (c->page_size < 1 || c->page_size > 1024 || c->page_table != nullptr) return KVQ_ERR_INVALID_ARGUMENT;
     if (c->num_pages < batch) return KVQ_ERR_INVALID_ARGUMENT;
-    if (!aligned_to(c->k_scales, 4) || !aligned_to(c->v_scales, 4)) return KVQ_ERR_INVALID_ARGUMENT;
+    if (!aligned_to(c->k_scale, 4) || !aligned_to(c->v_scale, 4)) return KVQ_ERR_INVALID_ARGUMENT;
     return KVQ_OK;
   }
   return KVQ_ERR_INVALID_ARGUMENT;

@@ -48,10 +48,10 @@ class KvqCacheStruct(ctypes.Structure):
         ("max_pages_per_seq", ctypes.c_int32),
         ("reserved", ctypes.c_int32),
         ("page_table", ctypes.c_void_p),
-        ("k_codes", ctypes.c_void_p),
-        ("v_codes", ctypes.c_void_p),
-        ("k_scales", ctypes.c_void_p),
-        ("v_scales", ctypes.c_void_p),
+        ("data", ctypes.c_void_p),
+        ("v_data", ctypes.c_void_p),
+        ("k_scale", ctypes.c_void_p),
+        ("v_scale", ctypes.c_void_p),
     ]
 
 
@@ -84,6 +84,8 @@ def load() -> ctypes.CDLL:
             L.kvq_status_string.argtypes = [ctypes.c_int]
             L.kvq_version.restype = ctypes.c_int32
             L.kvq_version.argtypes = []
+            L.kvq_fp4_pool_bytes.restype = ctypes.c_size_t
+            L.kvq_fp4_pool_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
             _lib = L
     return _lib
 
@@ -118,8 +120,10 @@ def _need(t: torch.Tensor, dtype: torch.dtype, name: str) -> None:
 class Fp4Cache:
     """FP4 (E2M1 codes, E4M3 scale per 16 channels) paged cache for K and V.
 
-    codes  uint8 [num_pages][num_kv_heads][page_size][head_dim/2]
-    scales uint8 [num_pages][num_kv_heads][page_size][head_dim/16]
+    pool  uint8 [num_pages][num_kv_heads][page_size / G][G * 9 * head_dim / 8],
+          G = min(page_size, 128): one contiguous block per group of G tokens
+          of one kv head (K codes, K scales, V codes in token pairs, V scales;
+          the byte layout is documented in include/kvq.h).
     page_table int32 [batch][max_pages_per_seq] or None (contiguous).
     """
 
@@ -127,11 +131,13 @@ class Fp4Cache:
                  max_pages_per_seq: int, page_table: Optional[torch.Tensor] = None, device="cuda"):
         self.num_kv_heads, self.head_dim, self.page_size = num_kv_heads, head_dim, page_size
         self.num_pages, self.max_pages_per_seq = num_pages, max_pages_per_seq
-        shape = (num_pages, num_kv_heads, page_size)
-        self.k_codes = torch.zeros(shape + (head_dim // 2,), dtype=torch.uint8, device=device)
-        self.v_codes = torch.zeros_like(self.k_codes)
-        self.k_scales = torch.zeros(shape + (head_dim // 16,), dtype=torch.uint8, device=device)
-        self.v_scales = torch.zeros_like(self.k_scales)
+        self.group = min(page_size, 128)
+        nbytes = load().kvq_fp4_pool_bytes(num_pages, num_kv_heads, page_size, head_dim)
+        if nbytes == 0:
+            raise ValueError("invalid FP4 cache geometry (head_dim 64/128/256, page_size 16..256)")
+        shape = (num_pages, num_kv_heads, page_size // self.group, self.group * 9 * head_dim // 8)
+        self.pool = torch.zeros(shape, dtype=torch.uint8, device=device)
+        assert self.pool.numel() == nbytes
         if page_table is not None:
             _need(page_table, torch.int32, "page_table")
         self.page_table = page_table
@@ -139,12 +145,11 @@ class Fp4Cache:
     def struct(self, page_table: Optional[torch.Tensor] = None) -> KvqCacheStruct:
         pt = self.page_table if page_table is None else page_table
         return KvqCacheStruct(FORMAT_FP4, self.num_kv_heads, self.head_dim, self.page_size, self.num_pages,
-                              self.max_pages_per_seq, 0, _ptr(pt), _ptr(self.k_codes), _ptr(self.v_codes),
-                              _ptr(self.k_scales), _ptr(self.v_scales))
+                              self.max_pages_per_seq, 0, _ptr(pt), _ptr(self.pool), None, None, None)
 
     @property
     def nbytes(self) -> int:
-        return 2 * (self.k_codes.numel() + self.k_scales.numel())
+        return self.pool.numel()
 
 
 class Fp8WindowCache:
@@ -167,6 +172,7 @@ class Fp8WindowCache:
         return KvqCacheStruct(FORMAT_FP8, self.num_kv_heads, self.head_dim, self.window, self.num_seqs, 0, 0,
                               None, _ptr(self.k_codes), _ptr(self.v_codes), _ptr(self.k_scales),
                               _ptr(self.v_scales))
+
 
 
 def append(cache, start_pos: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
@@ -229,7 +235,7 @@ def dequant(cache, seq_lens: Optional[torch.Tensor], max_len: int, dtype: torch.
     if isinstance(cache, Fp4Cache):
         batch = seq_lens.shape[0]
         s = cache.struct()
-        device = cache.k_codes.device
+        device = cache.pool.device
     else:
         batch = cache.num_seqs
         s = cache.struct()

@@ -38,25 +38,36 @@
  *     after synchronising the stream.
  *   - Key/value inputs are bf16; query heads h use kv head h / (Hq / Hkv).
  *
- * FP4 paged cache layout (format KVQ_FORMAT_FP4_E2M1_E4M3_G16), per K and V:
- *   codes : uint8 [num_pages][num_kv_heads][page_size][head_dim/2]
- *           byte j of a 16-channel block holds channel 2j in its low nibble,
- *           channel 2j+1 in its high nibble; nibble = sign<<3 | E2M1 magnitude
- *           (0..7 -> 0, .5, 1, 1.5, 2, 3, 4, 6); the sign of zero is kept.
- *   scales: uint8 [num_pages][num_kv_heads][page_size][head_dim/16], one E4M3FN
- *           byte per block (never 0x00: an all-zero block stores 0x01).
+ * FP4 paged cache layout (format KVQ_FORMAT_FP4_E2M1_E4M3_G16).
+ *   Codes: nibble = sign<<3 | E2M1 magnitude (0..7 -> 0, .5, 1, 1.5, 2, 3, 4,
+ *   6); the sign of zero is kept.  Scales: one E4M3FN byte per 16-channel
+ *   block of one token (never 0x00: an all-zero block stores 0x01).
+ *   The pool `data` is uint8 [num_pages][num_kv_heads][page_size/G][group],
+ *   G = min(page_size, 128) tokens per group, NB = head_dim/16 blocks, and one
+ *   group of G tokens of one kv head is a contiguous block of G*9*head_dim/8
+ *   bytes (4.5 bits per number), so a decode stage fetches it with one copy:
+ *     K codes  [G][head_dim/2] at 0: byte j of token t holds channels 2j (low
+ *              nibble) and 2j+1 (high nibble).
+ *     K scales [G][NB] at G*head_dim/2.
+ *     V codes  [G/2][head_dim] at G*(head_dim/2 + NB): row i holds tokens 2i
+ *              (low nibbles) and 2i+1 (high nibbles), byte c = channel c.  The
+ *              row's bytes are stored permuted so that decode reads them without
+ *              shared-memory bank conflicts: head_dim 64 moves 8-byte chunk u to
+ *              u ^ (((i >> 1) & 1) << 2); head_dim 128 and 256 move 16-byte chunk
+ *              u to u ^ ((i & 3) << 1).
+ *     V scales [NB][G] at G*(head_dim + NB).
  *   Position p of sequence b lives in page page_table[b*max_pages_per_seq +
- *   p/page_size], slot p % page_size.  With page_table == NULL the cache is
- *   contiguous: page p/page_size of sequence b is b*max_pages_per_seq +
- *   p/page_size.
+ *   p/page_size], slot p % page_size (group slot/G, token slot%G).  With
+ *   page_table == NULL the cache is contiguous: page p/page_size of sequence b
+ *   is b*max_pages_per_seq + p/page_size.
  *
- * FP8 window cache layout (format KVQ_FORMAT_FP8_E4M3_HEAD), per K and V:
- *   codes : uint8 [num_pages][num_kv_heads][page_size][head_dim], one E4M3FN
- *           byte per value; here num_pages counts rings (one per sequence b)
- *           and page_size is the window length W: position p of sequence b
- *           lives in slot p % W of ring b.
- *   scales: float [num_kv_heads], one fp32 scale per kv head (K and V apart):
- *           value = fp32(E4M3(code) * scale).
+ * FP8 window cache layout (format KVQ_FORMAT_FP8_E4M3_HEAD), K in `data`, V in
+ * `v_data`:
+ *   uint8 [num_pages][num_kv_heads][page_size][head_dim], one E4M3FN byte per
+ *   value; here num_pages counts rings (one per sequence b) and page_size is
+ *   the window length W: position p of sequence b lives in slot p % W of ring b.
+ *   k_scale, v_scale: float [num_kv_heads], one fp32 scale per kv head:
+ *   value = fp32(E4M3(code) * scale).
  */
 #ifndef KVQ_H
 #define KVQ_H
@@ -93,11 +104,12 @@ typedef enum kvq_format {
 typedef struct kvq_stream_opaque *kvq_stream; /* a cudaStream_t */
 
 /* Description of one cache (K and V of one layer).  All buffers are device
- * memory owned by the caller; see the layouts above. */
+ * memory owned by the caller; see the layouts above.  kvq_fp4_pool_bytes gives
+ * the size of an FP4 pool. */
 typedef struct kvq_cache {
     int32_t format;            /* kvq_format */
     int32_t num_kv_heads;      /* Hkv >= 1 */
-    int32_t head_dim;          /* multiple of 16, <= 512 */
+    int32_t head_dim;          /* FP4: 64, 128 or 256; FP8: multiple of 16, <= 512 */
     int32_t page_size;         /* FP4: tokens per page, one of 16, 32, 64, 128, 256;
                                   FP8: window length W, 1..1024 */
     int64_t num_pages;         /* FP4: pages in the pool; FP8: number of rings */
@@ -106,10 +118,10 @@ typedef struct kvq_cache {
     int32_t reserved;          /* must be 0 */
     const int32_t *page_table; /* FP4: device int32 [batch][max_pages_per_seq] or NULL;
                                   FP8: must be NULL */
-    void *k_codes;             /* device, see layouts */
-    void *v_codes;
-    void *k_scales;            /* FP4: uint8 E4M3 per block; FP8: float [Hkv] */
-    void *v_scales;
+    void *data;                /* FP4: the page pool; FP8: K codes (16-byte aligned) */
+    void *v_data;              /* FP8: V codes (16-byte aligned); FP4: must be NULL */
+    void *k_scale;             /* FP8: float [Hkv]; FP4: must be NULL */
+    void *v_scale;             /* FP8: float [Hkv]; FP4: must be NULL */
 } kvq_cache;
 
 /*
@@ -141,7 +153,7 @@ kvq_status kvq_append(const kvq_cache *cache, int32_t batch, int32_t n_new,
  * Bounded Replay": SWA KV stays FP8; "Quantising the KV cache" table row
  * "FP8 E4M3, one scale per tensor", here one scale per head.)
  *   k, v   device bf16 [batch][n][num_kv_heads][head_dim].
- * Writes cache->k_scales and cache->v_scales (float [Hkv]).  Device flags:
+ * Writes cache->k_scale and cache->v_scale (float [Hkv]).  Device flags:
  * NONFINITE.
  */
 kvq_status kvq_fp8_set_scales(const kvq_cache *cache, int32_t batch, int32_t n,
@@ -164,7 +176,7 @@ size_t kvq_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t nu
  * cache", section "Code": quantised K/V feed an unchanged attention;
  * "Concept": decode reads the whole cache.)
  *   out[b][h][:] = sum_t softmax_t(softmax_scale * q[b][h] . K^[b][t]) V^[b][t]
- *   global       FP4 cache, head_dim 64 or 128, page_size 16..256.
+ *   global       FP4 cache with head_dim 64 or 128.
  *   swa          FP8 window cache with the same num_kv_heads/head_dim, or NULL.
  *   batch        sequences, >= 1.
  *   num_q_heads  Hq, a multiple of num_kv_heads with Hq/Hkv <= 8.
@@ -199,6 +211,10 @@ kvq_status kvq_decode_attn(const kvq_cache *global, const kvq_cache *swa, int32_
 kvq_status kvq_dequant(const kvq_cache *cache, int32_t batch, const int32_t *d_seq_lens,
                        int32_t max_len, int32_t out_dtype, void *k_out, void *v_out,
                        int32_t *d_err_flag, kvq_stream stream);
+
+/* Bytes of an FP4 page pool: num_pages * num_kv_heads * page_size *
+ * 9 * head_dim / 8 (0 for invalid sizes). */
+size_t kvq_fp4_pool_bytes(int64_t num_pages, int32_t num_kv_heads, int32_t page_size, int32_t head_dim);
 
 /* A static, human-readable name for a status code. */
 const char *kvq_status_string(kvq_status status);

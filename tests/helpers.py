@@ -111,21 +111,45 @@ def host_kv_of(built: Built):
     return kv_of
 
 
+def unpack_pool_rows(cache: kvq.Fp4Cache, phys_pages, h: int, n: int):
+    """Positions 0..n-1 of one kv head, read from the listed physical pages of
+    the FP4 pool and rearranged (byte indexing only) into per-token rows:
+    (k_codes [n][D/2], k_scales [n][D/16], v_codes [n][D/2], v_scales [n][D/16])
+    with byte k of a code row holding channel 2k (low nibble) and 2k+1 (high
+    nibble), as the oracle's quantiser writes them."""
+    D, G = cache.head_dim, cache.group
+    nb = D // 16
+    idx = torch.as_tensor(np.asarray(phys_pages), dtype=torch.long, device=cache.pool.device)
+    blocks = cache.pool.index_select(0, idx)[:, h].reshape(-1, cache.pool.shape[-1]).cpu().numpy()
+    ng = blocks.shape[0]
+    kc = blocks[:, :G * D // 2].reshape(ng * G, D // 2)
+    ks = blocks[:, G * D // 2:G * (D // 2 + nb)].reshape(ng * G, nb)
+    vrows = blocks[:, G * (D // 2 + nb):G * (D + nb)].reshape(ng * G // 2, D)
+    vs = blocks[:, G * (D + nb):].reshape(ng, nb, G).transpose(0, 2, 1).reshape(ng * G, nb)
+    # undo the per-row chunk permutation of the pair rows
+    i = np.arange(vrows.shape[0])[:, None] % (G // 2)
+    if D == 64:
+        chunks = vrows.reshape(-1, 8, 8)
+        u = np.arange(8)[None, :] ^ (((i >> 1) & 1) << 2)
+    else:
+        chunks = vrows.reshape(-1, D // 16, 16)
+        u = np.arange(D // 16)[None, :] ^ ((i & 3) << 1)
+    logical = np.take_along_axis(chunks, u[:, :, None], axis=1).reshape(-1, D)
+    nib = np.stack([logical & 0x0F, logical >> 4], axis=1).reshape(-1, D)  # token 2i, then 2i+1
+    vc = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+    return kc[:n], ks[:n], vc[:n], vs[:n]
+
+
 def gather_unit_bytes(cache: kvq.Fp4Cache, table_row: Optional[np.ndarray], b: int, h: int, n: int):
-    """Codes and scales of positions 0..n-1 of sequence b, kv head h, from the
-    paged layout: (k_codes, k_scales, v_codes, v_scales) as numpy arrays."""
+    """Codes and scales of positions 0..n-1 of sequence b, kv head h (see
+    unpack_pool_rows)."""
     P = cache.page_size
-    pages = (n + P - 1) // P
+    pages = max(1, (n + P - 1) // P)
     if table_row is None:
         phys = np.arange(b * cache.max_pages_per_seq, b * cache.max_pages_per_seq + pages)
     else:
-        phys = table_row[:pages]
-    idx = torch.as_tensor(phys, dtype=torch.long, device=cache.k_codes.device)
-    out = []
-    for t in (cache.k_codes, cache.k_scales, cache.v_codes, cache.v_scales):
-        sel = t.index_select(0, idx)[:, h]                # [pages][P][bytes]
-        out.append(sel.reshape(pages * P, -1)[:n].cpu().numpy())
-    return out
+        phys = np.asarray(table_row[:pages])
+    return unpack_pool_rows(cache, phys, h, n)
 
 
 def softmax_scale(d: int) -> float:

@@ -30,8 +30,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
-        "kvq_append", "kvq_decode_attn", "kvq_decode_workspace_bytes", "kvq_dequant", "kvq_fp8_set_scales",
-        "kvq_status_string", "kvq_version"])
+        "kvq_append", "kvq_decode_attn", "kvq_decode_workspace_bytes", "kvq_dequant", "kvq_fp4_pool_bytes",
+        "kvq_fp8_set_scales", "kvq_status_string", "kvq_version"])
 
 
 def test_library_exports_every_declared_function(lib):
@@ -51,7 +51,7 @@ def test_struct_layout_matches_header():
 int main(void) {
   printf("%zu %zu %zu %zu %zu %zu %zu\n", sizeof(kvq_cache), offsetof(kvq_cache, num_pages),
          offsetof(kvq_cache, max_pages_per_seq), offsetof(kvq_cache, page_table),
-         offsetof(kvq_cache, k_codes), offsetof(kvq_cache, k_scales), offsetof(kvq_cache, v_scales));
+         offsetof(kvq_cache, data), offsetof(kvq_cache, k_scale), offsetof(kvq_cache, v_scale));
   return 0;
 }
 '''
@@ -63,8 +63,15 @@ int main(void) {
         got = [int(x) for x in subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()]
     S = kvq.KvqCacheStruct
     want = [ctypes.sizeof(S), S.num_pages.offset, S.max_pages_per_seq.offset, S.page_table.offset,
-            S.k_codes.offset, S.k_scales.offset, S.v_scales.offset]
+            S.data.offset, S.k_scale.offset, S.v_scale.offset]
     assert got == want
+
+
+def test_fp4_pool_bytes(lib):
+    assert lib.kvq_fp4_pool_bytes(10, 8, 64, 128) == 10 * 8 * 64 * 144
+    assert lib.kvq_fp4_pool_bytes(3, 2, 16, 64) == 3 * 2 * 16 * 72
+    assert lib.kvq_fp4_pool_bytes(3, 2, 48, 64) == 0
+    assert lib.kvq_fp4_pool_bytes(3, 2, 64, 80) == 0
 
 
 def test_status_strings_and_version(lib):
@@ -76,15 +83,16 @@ def test_status_strings_and_version(lib):
 
 def _fp4_struct(**kw):
     fields = dict(format=kvq.FORMAT_FP4, num_kv_heads=2, head_dim=128, page_size=64, num_pages=4,
-                  max_pages_per_seq=2, reserved=0, page_table=None, k_codes=4096, v_codes=8192,
-                  k_scales=12288, v_scales=16384)
+                  max_pages_per_seq=2, reserved=0, page_table=None, data=4096, v_data=None,
+                  k_scale=None, v_scale=None)
     fields.update(kw)
     return kvq.KvqCacheStruct(**fields)
 
 
 @pytest.mark.parametrize("bad", [
-    dict(head_dim=24), dict(head_dim=0), dict(page_size=48), dict(num_kv_heads=0), dict(reserved=1),
-    dict(k_codes=None), dict(k_codes=4097), dict(format=7), dict(num_pages=1)])
+    dict(head_dim=24), dict(head_dim=0), dict(head_dim=96), dict(page_size=48), dict(num_kv_heads=0),
+    dict(reserved=1), dict(data=None), dict(data=4097), dict(v_data=8192), dict(k_scale=64), dict(format=7),
+    dict(num_pages=1)])
 def test_invalid_cache_is_rejected_on_the_host(lib, bad):
     s = _fp4_struct(**bad)
     st = lib.kvq_append(ctypes.byref(s), 2, 1, 16, 32, 64, None, None)

@@ -23,7 +23,7 @@ def _lib():
     ensure_built()
 
 
-def _rows_through_gpu(blocks: np.ndarray, head_dim: int = 16):
+def _rows_through_gpu(blocks: np.ndarray, head_dim: int = 64):
     """Append rows of `head_dim` values (as K, and -rows as V) to a contiguous
     one-head cache; return (k_codes, k_scales, v_codes, v_scales) per row."""
     x = torch.from_numpy(np.ascontiguousarray(blocks, dtype=np.float32)).to(torch.bfloat16)
@@ -37,12 +37,14 @@ def _rows_through_gpu(blocks: np.ndarray, head_dim: int = 16):
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     kvq.append(cache, torch.zeros(1, dtype=torch.int32, device="cuda"), k, v, err=err)
     torch.cuda.synchronize()
-    out = [t.reshape(pages * P, -1)[:n].cpu().numpy() for t in
-           (cache.k_codes, cache.k_scales, cache.v_codes, cache.v_scales)]
+    out = gather_unit_bytes(cache, None, 0, 0, n)
     return out, int(err.item())
 
 
 def _compare_rows(blocks):
+    if blocks.shape[1] == 16:  # pack four 16-value blocks per 64-channel row
+        pad = (-blocks.shape[0]) % 4
+        blocks = np.concatenate([blocks, np.zeros((pad, 16), blocks.dtype)]).reshape(-1, 64)
     (kc, ks, vc, vs), flag = _rows_through_gpu(blocks, blocks.shape[1])
     okc, oks, _ = oracle.quantize_rows(blocks)
     ovc, ovs, _ = oracle.quantize_rows(-blocks)
@@ -128,18 +130,20 @@ def test_paged_append_ragged_starts(page_size):
             ovc, ovs, _ = oracle.quantize_rows(v[b, :, h].float().numpy())
             assert np.array_equal(kc[sl], okc) and np.array_equal(ks[sl], oks)
             assert np.array_equal(vc[sl], ovc) and np.array_equal(vs[sl], ovs)
-            # positions before the start were never written (zero-initialised cache)
+            # positions before the start keep their (zero) bytes, including the
+            # other nibble of a V byte shared with the first new token
             assert not kc[: lens[b]].any() and not ks[: lens[b]].any()
+            assert not vc[: lens[b]].any() and not vs[: lens[b]].any()
 
 
 def test_flags_page_oob_bad_start_nonfinite():
-    cache = kvq.Fp4Cache(1, 16, 16, 2, 2, page_table=torch.tensor([[0, 5]], dtype=torch.int32, device="cuda"))
+    cache = kvq.Fp4Cache(1, 64, 16, 2, 2, page_table=torch.tensor([[0, 5]], dtype=torch.int32, device="cuda"))
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    k = torch.ones(1, 20, 1, 16, dtype=torch.bfloat16, device="cuda")
+    k = torch.ones(1, 20, 1, 64, dtype=torch.bfloat16, device="cuda")
     kvq.append(cache, torch.zeros(1, dtype=torch.int32, device="cuda"), k, k, err=err)
     torch.cuda.synchronize()
     assert err.item() == kvq.FLAG_PAGE_OOB       # page id 5 >= num_pages: tokens 16.. skipped
-    assert not cache.k_codes[1].any()            # nothing written to the other page
+    assert not cache.pool[1].any()               # nothing written to the other page
     err.zero_()
     kvq.append(cache, torch.full((1,), -4, dtype=torch.int32, device="cuda"), k, k, err=err)
     torch.cuda.synchronize()
