@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(256) append_fp4_kernel(const kvq_cache c, int3
           const uint2 q = quantize_block(vb, sb);
           lo |= spread_nibbles(q.x) << (4 * half);
           hi |= spread_nibbles(q.y) << (4 * half);
-          grp[L.v_scales() + (int64_t)j * L.G + ls + half] = (uint8_t)sb;
+          grp[L.v_scale(ls + half, j)] = (uint8_t)sb;
         } else {
           const uint64_t m = half ? 0xF0F0F0F0F0F0F0F0ull : 0x0F0F0F0F0F0F0F0Full;
           keep_lo |= m;

@@ -208,7 +208,8 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
 // One group = min(page_size, 128) tokens of one kv head, stored as a
 // contiguous block: K codes [G][D/2], K scales [G][D/16], V codes [G/2][D]
 // (token pairs interleaved by nibble, 16-byte or 8-byte chunks permuted per
-// row), V scales [D/16][G].  9*D/8 bytes per token.
+// row), V scales [G/2][D/16][2] (the two tokens of a pair side by side).
+// 9*D/8 bytes per token.
 struct Fp4Layout {
   int D, P, G, nb;
   int64_t group_bytes;
@@ -222,6 +223,8 @@ struct Fp4Layout {
   __host__ __device__ int64_t group(int64_t phys, int hkv, int h, int slot) const {
     return ((phys * hkv + h) * (P / G) + slot / G) * group_bytes;
   }
+  // byte offset, inside a group, of the V scale of local token t, block j
+  __host__ __device__ int64_t v_scale(int t, int j) const { return v_scales() + (int64_t)(t >> 1) * 2 * nb + 2 * j + (t & 1); }
   // byte offset, inside a group, of the 16 V-code bytes of channels [16j, 16j+16)
   // of token pair row i (the permutation keeps these 16 bytes contiguous)
   __host__ __device__ int64_t v_block(int i, int j) const {

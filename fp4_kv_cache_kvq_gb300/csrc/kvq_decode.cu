@@ -61,6 +61,16 @@ struct Geo {
   static constexpr int kSmemBytes = kStages * kStageBytes + kFlushBytes + 2 * kStages * 8 + kStages * 4 + 16 + 1024;
 };
 
+// Compile-time view of one pool group of GT tokens (see Fp4Layout).
+template <int D, int GT>
+struct Grp {
+  static constexpr int kNB = D / 16;
+  static constexpr int kBytes = GT * 9 * D / 8;
+  static constexpr int kKS = GT * D / 2;          // K scales
+  static constexpr int kVC = GT * (D / 2 + kNB);  // V codes (token pairs)
+  static constexpr int kVS = GT * (D + kNB);      // V scales (token pairs)
+};
+
 struct DecodeParams {
   const int32_t* lens;
   const int32_t* page_table;
@@ -195,11 +205,11 @@ __device__ __forceinline__ Smem<D> carve(uint8_t* raw) {
 }
 
 // ------------------------------------------------------------------ producer
-template <int D>
+template <int D, int GT>
 __device__ void producer(const DecodeParams& p, Smem<D>& sm, Walker wk, int64_t v1) {
   using G = Geo<D>;
+  using R = Grp<D, GT>;
   const int P = p.page;
-  const Fp4Layout L(D, P);
   uint32_t it = 0;
   for (; wk.v < v1; advance(p, wk), ++it) {
     const uint32_t s = it % kStages;
@@ -215,8 +225,10 @@ __device__ void producer(const DecodeParams& p, Smem<D>& sm, Walker wk, int64_t 
     const int tok0 = wk.c * kChunk;
     const int ntok = min(kChunk, n4 - tok0);
     // one copy per pool group: a 128-token group of a larger page, or whole small pages
-    const int ncopies = P < kChunk ? (ntok + P - 1) / P : 1;
+    const int ncopies = GT < kChunk ? (ntok + GT - 1) / GT : 1;
     const int pg0 = tok0 / P;
+    const int groups_per_page = P / GT;
+    const int grp0 = GT < kChunk ? 0 : (tok0 % P) / GT;
     int64_t src[kMaxCopies];
     bool ok = true;
     for (int i = 0; i < ncopies; ++i) {
@@ -226,7 +238,7 @@ __device__ void producer(const DecodeParams& p, Smem<D>& sm, Walker wk, int64_t 
         ph = p.page_table ? (int64_t)__ldg(p.page_table + (int64_t)wk.b * p.max_pages + pg)
                           : (int64_t)wk.b * p.max_pages + pg;
       if (ph < 0 || ph >= p.num_pages) ok = false;
-      src[i] = L.group(ph, p.hkv, wk.h, P < kChunk ? 0 : tok0 % P);
+      src[i] = ((ph * p.hkv + wk.h) * groups_per_page + grp0) * (int64_t)R::kBytes;
     }
     const uint32_t full = smem_addr(&sm.full[s]);
     uint8_t* st = sm.stages + s * G::kStageBytes;
@@ -237,9 +249,8 @@ __device__ void producer(const DecodeParams& p, Smem<D>& sm, Walker wk, int64_t 
       continue;
     }
     sm.ntok[s] = ntok;
-    mbar_arrive_expect_tx(full, (uint32_t)(ncopies * L.group_bytes));
-    for (int i = 0; i < ncopies; ++i)
-      bulk_g2s(smem_addr(st + i * L.group_bytes), p.pool + src[i], (uint32_t)L.group_bytes, full);
+    mbar_arrive_expect_tx(full, (uint32_t)(ncopies * R::kBytes));
+    for (int i = 0; i < ncopies; ++i) bulk_g2s(smem_addr(st + i * R::kBytes), p.pool + src[i], R::kBytes, full);
   }
   // Wait for every copy still in flight before the CTA can retire.
   const uint32_t issued = it;
@@ -311,16 +322,22 @@ __device__ __forceinline__ void begin_unit(const DecodeParams& p, ConsumerState<
 }
 
 // One stage for one consumer warp: two 16-token slices, rows [32w, 32w+32).
-// The stage holds pool groups of `gt` = min(page_size, 128) tokens back to back
-// (see Fp4Layout); a 16-token slice never straddles two groups.
-template <int D>
-__device__ __forceinline__ void consume_stage(ConsumerState<D>& st, const uint8_t* stage, const Fp4Layout& L,
-                                              int ntok, uint32_t empty_bar) {
+// The stage holds pool groups of GT = min(page_size, 128) tokens back to back;
+// a 16-token slice never straddles two groups.
+template <int D, int GT>
+__device__ __forceinline__ void consume_stage(ConsumerState<D>& st, const uint8_t* stage, int ntok,
+                                              uint32_t empty_bar) {
+  using R = Grp<D, GT>;
   constexpr int KW = D / 32;  // words of K codes per thread per row (channels [tig*D/4, +D/4))
   constexpr int VW = D / 32;  // words of V codes per thread per token pair (channels [g*D/8, +D/8))
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int g = lane >> 2, tig = lane & 3;
+  // per-thread parts of the in-group offsets (pair rows i = lr/2 + tig have i % 8 == tig)
+  const int k_lane = g * (D / 2) + tig * (D / 8);
+  const int ks_lane = R::kKS + g * R::kNB + (D == 128 ? 2 * tig : tig);
+  const int v_lane = R::kVC + tig * D + (D == 128 ? 16 * (g ^ (tig << 1)) : 8 * (g ^ (((tig >> 1) & 1) << 2)));
+  const int vs_lane = R::kVS + tig * 2 * R::kNB + 2 * (D == 128 ? g : (g >> 1));
 
   // ---- loads from the stage, then release it
   uint32_t kw[kSlices][2][KW];  // rows g, g+8 of each slice
@@ -330,37 +347,37 @@ __device__ __forceinline__ void consume_stage(ConsumerState<D>& st, const uint8_
 #pragma unroll
   for (int sl = 0; sl < kSlices; ++sl) {
     const int r0 = 16 * (kSlices * warp + sl);
-    const uint8_t* grp = stage + (r0 / L.G) * L.group_bytes;
-    const int lr = r0 % L.G;
-    const int ra = lr + g, rb = lr + g + 8;
-    const int iA = (lr >> 1) + tig, iB = iA + 4;  // token-pair rows
-    const int blk = D == 128 ? g : (g >> 1);       // V scale block of this thread's channels
+    const uint8_t* grp = stage + (r0 / GT) * R::kBytes;
+    const int lr = r0 % GT;
+    const uint8_t* kp = grp + lr * (D / 2) + k_lane;
+    const uint8_t* ksp = grp + lr * R::kNB + ks_lane;
+    const uint8_t* vp = grp + (lr / 2) * D + v_lane;
+    const uint8_t* vsp = grp + (lr / 2) * 2 * R::kNB + vs_lane;
     if constexpr (D == 128) {
-      const uint4 a = *reinterpret_cast<const uint4*>(grp + ra * 64 + 16 * tig);
-      const uint4 b = *reinterpret_cast<const uint4*>(grp + rb * 64 + 16 * tig);
+      const uint4 a = *reinterpret_cast<const uint4*>(kp);
+      const uint4 b = *reinterpret_cast<const uint4*>(kp + 8 * (D / 2));
       kw[sl][0][0] = a.x; kw[sl][0][1] = a.y; kw[sl][0][2] = a.z; kw[sl][0][3] = a.w;
       kw[sl][1][0] = b.x; kw[sl][1][1] = b.y; kw[sl][1][2] = b.z; kw[sl][1][3] = b.w;
-      ksb[sl][0] = *reinterpret_cast<const uint16_t*>(grp + L.k_scales() + ra * 8 + 2 * tig);
-      ksb[sl][1] = *reinterpret_cast<const uint16_t*>(grp + L.k_scales() + rb * 8 + 2 * tig);
-      const uint4 x = *reinterpret_cast<const uint4*>(grp + L.v_block(iA, g));
-      const uint4 y = *reinterpret_cast<const uint4*>(grp + L.v_block(iB, g));
+      ksb[sl][0] = *reinterpret_cast<const uint16_t*>(ksp);
+      ksb[sl][1] = *reinterpret_cast<const uint16_t*>(ksp + 8 * R::kNB);
+      const uint4 x = *reinterpret_cast<const uint4*>(vp);
+      const uint4 y = *reinterpret_cast<const uint4*>(vp + 4 * D);  // pair row i + 4: same permutation
       vw[sl][0][0] = x.x; vw[sl][0][1] = x.y; vw[sl][0][2] = x.z; vw[sl][0][3] = x.w;
       vw[sl][1][0] = y.x; vw[sl][1][1] = y.y; vw[sl][1][2] = y.z; vw[sl][1][3] = y.w;
     } else {
-      const uint2 a = *reinterpret_cast<const uint2*>(grp + ra * 32 + 8 * tig);
-      const uint2 b = *reinterpret_cast<const uint2*>(grp + rb * 32 + 8 * tig);
+      const uint2 a = *reinterpret_cast<const uint2*>(kp);
+      const uint2 b = *reinterpret_cast<const uint2*>(kp + 8 * (D / 2));
       kw[sl][0][0] = a.x; kw[sl][0][1] = a.y;
       kw[sl][1][0] = b.x; kw[sl][1][1] = b.y;
-      ksb[sl][0] = grp[L.k_scales() + ra * 4 + tig];
-      ksb[sl][1] = grp[L.k_scales() + rb * 4 + tig];
-      // 8-byte chunk g of each pair row, chunk index permuted by ((i >> 1) & 1) << 2
-      const uint2 x = *reinterpret_cast<const uint2*>(grp + L.v_codes() + iA * 64 + 8 * (g ^ (((iA >> 1) & 1) << 2)));
-      const uint2 y = *reinterpret_cast<const uint2*>(grp + L.v_codes() + iB * 64 + 8 * (g ^ (((iB >> 1) & 1) << 2)));
+      ksb[sl][0] = *ksp;
+      ksb[sl][1] = *(ksp + 8 * R::kNB);
+      const uint2 x = *reinterpret_cast<const uint2*>(vp);
+      const uint2 y = *reinterpret_cast<const uint2*>(vp + 4 * D);  // (i + 4) >> 1 keeps bit 0
       vw[sl][0][0] = x.x; vw[sl][0][1] = x.y;
       vw[sl][1][0] = y.x; vw[sl][1][1] = y.y;
     }
-    vsb[sl][0] = *reinterpret_cast<const uint16_t*>(grp + L.v_scales() + blk * L.G + lr + 2 * tig);
-    vsb[sl][1] = *reinterpret_cast<const uint16_t*>(grp + L.v_scales() + blk * L.G + lr + 2 * tig + 8);
+    vsb[sl][0] = *reinterpret_cast<const uint16_t*>(vsp);
+    vsb[sl][1] = *reinterpret_cast<const uint16_t*>(vsp + 4 * 2 * R::kNB);
   }
   mbar_arrive(empty_bar);
 
@@ -534,7 +551,7 @@ __device__ void flush_unit(const DecodeParams& p, ConsumerState<D>& st, Smem<D>&
   }
 }
 
-template <int D>
+template <int D, int GT>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_fp4_kernel(const DecodeParams p) {
   using G = Geo<D>;
@@ -558,13 +575,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (warp == kConsumerWarps) {
     if (lane == 0) {
-      producer<D>(p, sm, wk, v1);
+      producer<D, GT>(p, sm, wk, v1);
     }
     return;
   }
 
   const int64_t per = (total + gridDim.x - 1) / gridDim.x;
-  const Fp4Layout lay(D, p.page);
   ConsumerState<D> st;
   bool have = false, dead = false;
   int64_t slot = 0;
@@ -595,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const int ntok = sm.ntok[s];
     if (ntok > 16 * kSlices * warp) {
-      consume_stage<D>(st, sm.stages + s * G::kStageBytes, lay, ntok, smem_addr(&sm.empty[s]));
+      consume_stage<D, GT>(st, sm.stages + s * G::kStageBytes, ntok, smem_addr(&sm.empty[s]));
     } else {
       mbar_arrive(smem_addr(&sm.empty[s]));
     }
@@ -743,13 +759,24 @@ WsLayout ws_layout(int64_t batch, int64_t hkv, int64_t g, int64_t d, int64_t cta
 
 int decode_ctas() { return 2 * device_sm_count(); }
 
+template <int D, int GT>
+kvq_status launch_decode_g(const DecodeParams& dp, cudaStream_t s, int ctas) {
+  const int smem = Geo<D>::kSmemBytes;
+  if (cudaFuncSetAttribute(decode_fp4_kernel<D, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return KVQ_ERR_CUDA;
+  decode_fp4_kernel<D, GT><<<ctas, kThreads, smem, s>>>(dp);
+  return launch_status();
+}
+
 template <int D>
 kvq_status launch_decode(const DecodeParams& dp, cudaStream_t s, int ctas) {
-  const int smem = Geo<D>::kSmemBytes;
-  if (cudaFuncSetAttribute(decode_fp4_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return KVQ_ERR_CUDA;
-  decode_fp4_kernel<D><<<ctas, kThreads, smem, s>>>(dp);
-  return launch_status();
+  switch (dp.page < kChunk ? dp.page : kChunk) {
+    case 16: return launch_decode_g<D, 16>(dp, s, ctas);
+    case 32: return launch_decode_g<D, 32>(dp, s, ctas);
+    case 64: return launch_decode_g<D, 64>(dp, s, ctas);
+    default: return launch_decode_g<D, kChunk>(dp, s, ctas);
+  }
 }
 
 }  // namespace

@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(256) dequant_fp4_kernel(const kvq_cache c, int
       }
       // V: 16 interleaved bytes of the token pair; this token's nibbles
       const uint4 vw = __ldg(reinterpret_cast<const uint4*>(grp + L.v_block(ls >> 1, j)));
-      const float sv = e4m3_to_f32(__ldg(grp + L.v_scales() + (int64_t)j * L.G + ls));
+      const float sv = e4m3_to_f32(__ldg(grp + L.v_scale(ls, j)));
       const uint32_t ws[4] = {vw.x, vw.y, vw.z, vw.w};
       const int sh = 4 * (ls & 1);
 #pragma unroll

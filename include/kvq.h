@@ -55,7 +55,8 @@
  *              shared-memory bank conflicts: head_dim 64 moves 8-byte chunk u to
  *              u ^ (((i >> 1) & 1) << 2); head_dim 128 and 256 move 16-byte chunk
  *              u to u ^ ((i & 3) << 1).
- *     V scales [NB][G] at G*(head_dim + NB).
+ *     V scales [G/2][NB][2] at G*(head_dim + NB): pair i, block j holds the
+ *              scales of tokens 2i and 2i+1.
  *   Position p of sequence b lives in page page_table[b*max_pages_per_seq +
  *   p/page_size], slot p % page_size (group slot/G, token slot%G).  With
  *   page_table == NULL the cache is contiguous: page p/page_size of sequence b

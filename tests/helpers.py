@@ -125,7 +125,7 @@ def unpack_pool_rows(cache: kvq.Fp4Cache, phys_pages, h: int, n: int):
     kc = blocks[:, :G * D // 2].reshape(ng * G, D // 2)
     ks = blocks[:, G * D // 2:G * (D // 2 + nb)].reshape(ng * G, nb)
     vrows = blocks[:, G * (D // 2 + nb):G * (D + nb)].reshape(ng * G // 2, D)
-    vs = blocks[:, G * (D + nb):].reshape(ng, nb, G).transpose(0, 2, 1).reshape(ng * G, nb)
+    vs = blocks[:, G * (D + nb):].reshape(ng * G // 2, nb, 2).transpose(0, 2, 1).reshape(ng * G, nb)
     # undo the per-row chunk permutation of the pair rows
     i = np.arange(vrows.shape[0])[:, None] % (G // 2)
     if D == 64:
