@@ -868,3 +868,50 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* global, const kvq_cache* 
   merge_kernel<<<(unsigned)(batch * hkv * g), 128, msmem, s>>>(mp);
   return launch_status();
 }
+
+// ------------------------------------------------------------------ decode without caller scratch
+// For callers that may not allocate device memory on their call path (see the
+// header).  The workspace lives in a fixed device array that every GPU loading
+// this library holds until the process exits; calls share it.
+#include <mutex>
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 256;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (host code cannot use the array's name as a device address).
+kvq_status scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return KVQ_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" kvq_status kvq_decode_attn_noalloc(const kvq_cache* global, const kvq_cache* swa, int32_t batch,
+                                              int32_t num_q_heads, const int32_t* d_seq_lens, const void* q,
+                                              float softmax_scale, float* out, int32_t* d_err_flag,
+                                              kvq_stream stream) {
+  if (global == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+  const size_t need = kvq_decode_workspace_bytes(batch, num_q_heads, global->num_kv_heads, global->head_dim);
+  if (need == 0) return KVQ_ERR_INVALID_ARGUMENT;
+  if (need > kNoAllocScratchBytes) return KVQ_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  const kvq_status st = scratch_address(&scratch);
+  if (st != KVQ_OK) return st;
+  return kvq_decode_attn(global, swa, batch, num_q_heads, d_seq_lens, q, softmax_scale, out, scratch,
+                         kNoAllocScratchBytes, d_err_flag, stream);
+}

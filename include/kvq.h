@@ -198,6 +198,29 @@ kvq_status kvq_decode_attn(const kvq_cache *global, const kvq_cache *swa, int32_
                            size_t workspace_bytes, int32_t *d_err_flag, kvq_stream stream);
 
 /*
+ * kvq_decode_attn_noalloc -- kvq_decode_attn for callers that cannot allocate
+ * device memory on their call path: a plug-in running inside a host framework
+ * that owns every device allocation through its own pool, or code under a hard
+ * memory budget where an extra cudaMalloc (which may also synchronise the
+ * device) is not allowed.  The pages describe no such entry point; it exists
+ * only for these callers.  Same arguments and results as kvq_decode_attn,
+ * without `workspace`: the scratch is a fixed 8 MiB device array inside the
+ * library, which every GPU that loads the library keeps until the process
+ * exits.  Sizes whose kvq_decode_workspace_bytes exceed 8 MiB are refused with
+ * KVQ_ERR_WORKSPACE (nothing is enqueued).  The first call on each device looks
+ * up the array's device address (cudaGetSymbolAddress), so make that first call
+ * before any stream capture.  The array needs no clearing (each call writes the
+ * scratch it reads), but all calls share it: calls whose kernels can overlap on
+ * the GPU (different streams, or a second call before the first finished on
+ * another stream) race and give wrong results; serialise them on one stream.
+ * Allocates nothing and calls no allocating routine.
+ */
+kvq_status kvq_decode_attn_noalloc(const kvq_cache *global, const kvq_cache *swa, int32_t batch,
+                                   int32_t num_q_heads, const int32_t *d_seq_lens, const void *q,
+                                   float softmax_scale, float *out, int32_t *d_err_flag,
+                                   kvq_stream stream);
+
+/*
  * kvq_dequant -- expand a cache to dense values (value = E2M1(code) * E4M3(s)
  * for FP4, exact in fp32 and bf16; fp32(E4M3(code) * s_h) for FP8).
  * ("Quantising the KV cache", section "Code": the dequantised value is the

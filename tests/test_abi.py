@@ -30,8 +30,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
-        "kvq_append", "kvq_decode_attn", "kvq_decode_workspace_bytes", "kvq_dequant", "kvq_fp4_pool_bytes",
-        "kvq_fp8_set_scales", "kvq_status_string", "kvq_version"])
+        "kvq_append", "kvq_decode_attn", "kvq_decode_attn_noalloc", "kvq_decode_workspace_bytes", "kvq_dequant",
+        "kvq_fp4_pool_bytes", "kvq_fp8_set_scales", "kvq_status_string", "kvq_version"])
 
 
 def test_library_exports_every_declared_function(lib):
