@@ -325,7 +325,7 @@ __device__ __forceinline__ void begin_unit(const DecodeParams& p, ConsumerState<
 // The stage holds pool groups of GT = min(page_size, 128) tokens back to back;
 // a 16-token slice never straddles two groups.
 template <int D, int GT>
-__device__ __forceinline__ void consume_stage(ConsumerState<D>& st, const uint8_t* stage, int ntok,
+__device__ __forceinline__ void consume_stage(ConsumerState<D>& st, uint32_t stage, int ntok,
                                               uint32_t empty_bar) {
   using R = Grp<D, GT>;
   constexpr int KW = D / 32;  // words of K codes per thread per row (channels [tig*D/4, +D/4))
@@ -334,10 +334,11 @@ __device__ __forceinline__ void consume_stage(ConsumerState<D>& st, const uint8_
   const int warp = threadIdx.x >> 5;
   const int g = lane >> 2, tig = lane & 3;
   // per-thread parts of the in-group offsets (pair rows i = lr/2 + tig have i % 8 == tig)
-  const int k_lane = g * (D / 2) + tig * (D / 8);
-  const int ks_lane = R::kKS + g * R::kNB + (D == 128 ? 2 * tig : tig);
-  const int v_lane = R::kVC + tig * D + (D == 128 ? 16 * (g ^ (tig << 1)) : 8 * (g ^ (((tig >> 1) & 1) << 2)));
-  const int vs_lane = R::kVS + tig * 2 * R::kNB + 2 * (D == 128 ? g : (g >> 1));
+  const uint32_t k_lane = g * (D / 2) + tig * (D / 8);
+  const uint32_t ks_lane = R::kKS + g * R::kNB + (D == 128 ? 2 * tig : tig);
+  const uint32_t v_lane =
+      R::kVC + tig * D + (D == 128 ? 16 * (g ^ (tig << 1)) : 8 * (g ^ (((tig >> 1) & 1) << 2)));
+  const uint32_t vs_lane = R::kVS + tig * 2 * R::kNB + 2 * (D == 128 ? g : (g >> 1));
 
   // ---- loads from the stage, then release it
   uint32_t kw[kSlices][2][KW];  // rows g, g+8 of each slice
@@ -347,37 +348,37 @@ __device__ __forceinline__ void consume_stage(ConsumerState<D>& st, const uint8_
 #pragma unroll
   for (int sl = 0; sl < kSlices; ++sl) {
     const int r0 = 16 * (kSlices * warp + sl);
-    const uint8_t* grp = stage + (r0 / GT) * R::kBytes;
-    const int lr = r0 % GT;
-    const uint8_t* kp = grp + lr * (D / 2) + k_lane;
-    const uint8_t* ksp = grp + lr * R::kNB + ks_lane;
-    const uint8_t* vp = grp + (lr / 2) * D + v_lane;
-    const uint8_t* vsp = grp + (lr / 2) * 2 * R::kNB + vs_lane;
+    const uint32_t grp = stage + (uint32_t)((r0 / GT) * R::kBytes);
+    const uint32_t lr = r0 % GT;
+    const uint32_t kp = grp + lr * (D / 2) + k_lane;
+    const uint32_t ksp = grp + lr * R::kNB + ks_lane;
+    const uint32_t vp = grp + (lr / 2) * D + v_lane;
+    const uint32_t vsp = grp + (lr / 2) * 2 * R::kNB + vs_lane;
     if constexpr (D == 128) {
-      const uint4 a = *reinterpret_cast<const uint4*>(kp);
-      const uint4 b = *reinterpret_cast<const uint4*>(kp + 8 * (D / 2));
+      const uint4 a = lds128(kp);
+      const uint4 b = lds128(kp + 8 * (D / 2));
       kw[sl][0][0] = a.x; kw[sl][0][1] = a.y; kw[sl][0][2] = a.z; kw[sl][0][3] = a.w;
       kw[sl][1][0] = b.x; kw[sl][1][1] = b.y; kw[sl][1][2] = b.z; kw[sl][1][3] = b.w;
-      ksb[sl][0] = *reinterpret_cast<const uint16_t*>(ksp);
-      ksb[sl][1] = *reinterpret_cast<const uint16_t*>(ksp + 8 * R::kNB);
-      const uint4 x = *reinterpret_cast<const uint4*>(vp);
-      const uint4 y = *reinterpret_cast<const uint4*>(vp + 4 * D);  // pair row i + 4: same permutation
+      ksb[sl][0] = lds16(ksp);
+      ksb[sl][1] = lds16(ksp + 8 * R::kNB);
+      const uint4 x = lds128(vp);
+      const uint4 y = lds128(vp + 4 * D);  // pair row i + 4: same permutation
       vw[sl][0][0] = x.x; vw[sl][0][1] = x.y; vw[sl][0][2] = x.z; vw[sl][0][3] = x.w;
       vw[sl][1][0] = y.x; vw[sl][1][1] = y.y; vw[sl][1][2] = y.z; vw[sl][1][3] = y.w;
     } else {
-      const uint2 a = *reinterpret_cast<const uint2*>(kp);
-      const uint2 b = *reinterpret_cast<const uint2*>(kp + 8 * (D / 2));
+      const uint2 a = lds64(kp);
+      const uint2 b = lds64(kp + 8 * (D / 2));
       kw[sl][0][0] = a.x; kw[sl][0][1] = a.y;
       kw[sl][1][0] = b.x; kw[sl][1][1] = b.y;
-      ksb[sl][0] = *ksp;
-      ksb[sl][1] = *(ksp + 8 * R::kNB);
-      const uint2 x = *reinterpret_cast<const uint2*>(vp);
-      const uint2 y = *reinterpret_cast<const uint2*>(vp + 4 * D);  // (i + 4) >> 1 keeps bit 0
+      ksb[sl][0] = lds8(ksp);
+      ksb[sl][1] = lds8(ksp + 8 * R::kNB);
+      const uint2 x = lds64(vp);
+      const uint2 y = lds64(vp + 4 * D);  // (i + 4) >> 1 keeps bit 0
       vw[sl][0][0] = x.x; vw[sl][0][1] = x.y;
       vw[sl][1][0] = y.x; vw[sl][1][1] = y.y;
     }
-    vsb[sl][0] = *reinterpret_cast<const uint16_t*>(vsp);
-    vsb[sl][1] = *reinterpret_cast<const uint16_t*>(vsp + 4 * 2 * R::kNB);
+    vsb[sl][0] = lds16(vsp);
+    vsb[sl][1] = lds16(vsp + 4 * 2 * R::kNB);
   }
   mbar_arrive(empty_bar);
 
@@ -431,22 +432,18 @@ __device__ __forceinline__ void consume_stage(ConsumerState<D>& st, const uint8_
   }
   m0 *= st.cs[0];
   m1 *= st.cs[1];
-  if (__any_sync(0xFFFFFFFFu, m0 > st.m[0] + kLazySlack || m1 > st.m[1] + kLazySlack)) {
+  // O is rescaled (by al) when this stage's products are added to it, below
+  float al0 = 1.0f, al1 = 1.0f;
+  const bool rescale = __any_sync(0xFFFFFFFFu, m0 > st.m[0] + kLazySlack || m1 > st.m[1] + kLazySlack);
+  if (rescale) {
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       m0 = fmaxf(m0, __shfl_xor_sync(0xFFFFFFFFu, m0, o));
       m1 = fmaxf(m1, __shfl_xor_sync(0xFFFFFFFFu, m1, o));
     }
     const float n0 = fmaxf(st.m[0], m0), n1 = fmaxf(st.m[1], m1);
-    const float al0 = (st.m[0] == -INFINITY) ? 0.0f : fast_exp2(st.m[0] - n0);
-    const float al1 = (st.m[1] == -INFINITY) ? 0.0f : fast_exp2(st.m[1] - n1);
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-      st.o[mt][0] *= al0;
-      st.o[mt][2] *= al0;
-      st.o[mt][1] *= al1;
-      st.o[mt][3] *= al1;
-    }
+    al0 = (st.m[0] == -INFINITY) ? 0.0f : fast_exp2(st.m[0] - n0);
+    al1 = (st.m[1] == -INFINITY) ? 0.0f : fast_exp2(st.m[1] - n1);
     st.l[0] *= al0;
     st.l[1] *= al1;
     st.m[0] = n0;
@@ -455,6 +452,9 @@ __device__ __forceinline__ void consume_stage(ConsumerState<D>& st, const uint8_
   const float nref0 = st.m[0] == -INFINITY ? 0.0f : -st.m[0];
   const float nref1 = st.m[1] == -INFINITY ? 0.0f : -st.m[1];
 
+  float acc[D / 16][4];  // this stage's PV products (fresh accumulators)
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
 #pragma unroll
   for (int sl = 0; sl < kSlices; ++sl) {
     const float p0 = fast_exp2(fmaf(S[sl][0], st.cs[0], nref0));
@@ -494,9 +494,23 @@ __device__ __forceinline__ void consume_stage(ConsumerState<D>& st, const uint8_
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
       // row g <-> channel (D/8) g + mt, row g+8 <-> (D/8) g + D/16 + mt
-      mma_f16_16816(st.o[mt], hmul2_u32(VA[mt], svA), hmul2_u32(VA[D / 16 + mt], svA), hmul2_u32(VB[mt], svB),
+      mma_f16_16816(acc[mt], hmul2_u32(VA[mt], svA), hmul2_u32(VA[D / 16 + mt], svA), hmul2_u32(VB[mt], svB),
                     hmul2_u32(VB[D / 16 + mt], svB), pbA, pbB);
     }
+  }
+  if (rescale) {
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      st.o[mt][0] = fmaf(st.o[mt][0], al0, acc[mt][0]);
+      st.o[mt][1] = fmaf(st.o[mt][1], al1, acc[mt][1]);
+      st.o[mt][2] = fmaf(st.o[mt][2], al0, acc[mt][2]);
+      st.o[mt][3] = fmaf(st.o[mt][3], al1, acc[mt][3]);
+    }
+  } else {
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) st.o[mt][i] += acc[mt][i];
   }
 }
 
@@ -581,6 +595,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 
   const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+  const uint32_t stages_base = smem_addr(sm.stages);
   ConsumerState<D> st;
   bool have = false, dead = false;
   int64_t slot = 0;
@@ -611,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     const int ntok = sm.ntok[s];
     if (ntok > 16 * kSlices * warp) {
-      consume_stage<D, GT>(st, sm.stages + s * G::kStageBytes, ntok, smem_addr(&sm.empty[s]));
+      consume_stage<D, GT>(st, stages_base + s * G::kStageBytes, ntok, smem_addr(&sm.empty[s]));
     } else {
       mbar_arrive(smem_addr(&sm.empty[s]));
     }
