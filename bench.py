@@ -183,6 +183,23 @@ class Setup:
                 b * max_pages, (b + 1) * max_pages, dtype=torch.int32, device=device)[None]
             kvq.append(self.cache, zero, k[None], v[None], err=self.err, page_table=row)
             del k, v
+        self.swa = None
+        if w.window > 0:
+            # FP8 window beside the FP4 cache: scales from the prefill's last W
+            # positions of every sequence, then those positions into the rings
+            W = w.window
+            tails_k, tails_v = [], []
+            for b, n in enumerate(self.lens0):
+                k, v = workloads.sequence_kv(w, b, n, seed=seed, device=device)
+                tails_k.append(k[n - W:])
+                tails_v.append(v[n - W:])
+                del k, v
+            kw, vw = torch.stack(tails_k).contiguous(), torch.stack(tails_v).contiguous()
+            self.swa = kvq.Fp8WindowCache(w.batch, w.num_kv_heads, w.head_dim, W, device=device)
+            kvq.fp8_set_scales(self.swa, kw, vw, err=self.err)
+            start = torch.tensor([n - W for n in self.lens0], dtype=torch.int32, device=device)
+            kvq.append(self.swa, start, kw, vw, err=self.err)
+            del kw, vw, tails_k, tails_v
         toks = [workloads.step_tokens(w, i, seed=seed, device=device) for i in range(CYCLE)]
         self.k_new = [t[0] for t in toks]
         self.v_new = [t[1] for t in toks]
@@ -201,12 +218,15 @@ class Setup:
     def step(self, i: int, q=None, k=None, v=None, ev=None):
         s = i % CYCLE
         kvq = self.kvq
-        kvq.append(self.cache, self.pos[s], self.k_new[s] if k is None else k, self.v_new[s] if v is None else v,
-                   err=self.err)
+        kk = self.k_new[s] if k is None else k
+        vv = self.v_new[s] if v is None else v
+        kvq.append(self.cache, self.pos[s], kk, vv, err=self.err)
+        if self.swa is not None:
+            kvq.append(self.swa, self.pos[s], kk, vv, err=self.err)
         if ev is not None:
             ev[0].record()
-        kvq.decode_attn(self.cache, self.lens[s], self.q[i % NQ] if q is None else q, self.scale, out=self.out,
-                        workspace=self.ws, err=self.err)
+        kvq.decode_attn(self.cache, self.lens[s], self.q[i % NQ] if q is None else q, self.scale, swa=self.swa,
+                        out=self.out, workspace=self.ws, err=self.err)
         if ev is not None:
             ev[1].record()
         return self.kv_tokens[s]
@@ -214,7 +234,9 @@ class Setup:
     def decode_algorithmic_bytes(self, i: int) -> int:
         w = self.w
         s = i % CYCLE
-        b = self.kv_tokens[s] * fp4_bytes_per_token(w)
+        win = min(w.window, min(self.lens0) + s + 1) if w.window else 0
+        b = (self.kv_tokens[s] - win * w.batch) * fp4_bytes_per_token(w)
+        b += win * w.batch * 2 * w.num_kv_heads * w.head_dim  # FP8 window codes (K and V)
         b += w.batch * w.num_q_heads * w.head_dim * (2 + 4)  # q in, out
         b += w.batch * 4                                      # lengths
         if self.table is not None:
@@ -302,19 +324,99 @@ def run_gpu(args, dist: Dist):
         "hbm_gbs_step": step_bytes * K / elapsed_s / 1e9,
         "hbm_gbs_decode": achieved,
         "hbm_pct_of_8tbs_decode": 100.0 * achieved / 8000.0,
-        "roofline": {"bound": "hbm", "kernel": "kvq_decode_attn (split-K decode + merge launches)",
+        "roofline": {"bound": "hbm", "kernel": "kvq_decode_attn (split-K decode + merge launches)"
+                     + (", FP8 window folded into the merge" if w.window else ""),
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_src, "traffic": profiled_traffic(),
                      "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_s * 1e3},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": Ke},
-        "gpu_launches": 3 * K,
+        "gpu_launches": (4 if w.window else 3) * K,
     }
     if clk is not None:
         result["clocks"] = clk
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(w, args.seed, st, budget_s=args.cpu_budget)
     return result
+
+
+# ----------------------------------------------------------------- append throughput (prefill)
+PREFILL_METRIC = "append (quantise-on-append) tokens/s and HBM GB/s into the FP4 cache, 1xGB300"
+
+
+def run_prefill(args, dist: Dist):
+    """A step appends a whole prefill (B16 x 16384 tokens, Hkv8, d128, bf16 K
+    and V) into the FP4 cache; value = appended tokens/s (one token = one
+    position of one sequence across all kv heads, K and V)."""
+    from fp4_kv_cache_kvq_gb300 import build, kvq
+    device = torch.device("cuda", dist.local)
+    torch.cuda.set_device(device)
+    build.build()
+    w = workloads.WORKLOADS["prefill"]
+    B, T = w.batch, w.context
+    max_pages = -(-T // w.page_size)
+    cache = kvq.Fp4Cache(w.num_kv_heads, w.head_dim, w.page_size, B * max_pages, max_pages, device=device)
+    k = torch.empty((B, T, w.num_kv_heads, w.head_dim), dtype=torch.bfloat16, device=device)
+    v = torch.empty_like(k)
+    for b in range(B):
+        k[b], v[b] = workloads.sequence_kv(w, b, T, seed=args.seed, device=device)
+    start = torch.zeros(B, dtype=torch.int32, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    K, Wm = args.steps, args.warmup
+    for _ in range(Wm):
+        kvq.append(cache, start, k, v, err=err)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(device.index)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    t0.record()
+    for _ in range(K):
+        kvq.append(cache, start, k, v, err=err)
+    t1.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    if err.item() != 0:
+        raise RuntimeError(f"device error flag {err.item()}")
+    secs = t0.elapsed_time(t1) / 1e3
+    tokens = B * T
+    value, max_s = combine_ranks(dist, tokens * K, secs)
+    nbytes = 2 * k.numel() * 2 + tokens * fp4_bytes_per_token(w)
+    achieved = nbytes * K / secs / 1e9
+    peak, peak_src = measured_hbm_peak()
+    # end to end: host K/V (pinned) copied in every step, the error word copied back
+    Ke = min(K, 10)
+    kh, vh = k.cpu().pin_memory(), v.cpu().pin_memory()
+    errh = torch.empty(1, dtype=torch.int32).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(Ke):
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        kvq.append(cache, start, k, v, err=err)
+        errh.copy_(err, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e, _ = combine_ranks(dist, tokens * Ke, e0.elapsed_time(e1) / 1e3)
+    res = {
+        "metric": PREFILL_METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": K,
+        "warmup": Wm, "ms_per_step": max_s * 1e3 / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"prefill: {w.description}", "batch": B, "tokens": T, "kv_heads": w.num_kv_heads,
+                   "head_dim": w.head_dim, "page_size": w.page_size,
+                   "l2": "inputs larger than L2 (1.07 GB of bf16 per step), no flush",
+                   "parallelism": f"replicas x{dist.world}"},
+        "roofline": {"bound": "hbm", "kernel": "append_fp4_kernel", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src, "traffic": None,
+                     "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": secs * 1e3 / K},
+        "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": 2 * k.numel() * 2, "d2h_bytes_per_step": 4,
+                "steps": Ke},
+        "gpu_launches": K,
+    }
+    if clk is not None:
+        res["clocks"] = clk
+    return res
 
 
 # ----------------------------------------------------------------- CPU oracle (baseline / reference arm)
@@ -419,7 +521,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
     ap.add_argument("--workload", default="long_context",
-                    choices=["long_context", "gqa_outliers", "paged_ragged", "tiny"])
+                    choices=["long_context", "gqa_outliers", "paged_ragged", "swa_append", "tiny", "prefill"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -428,7 +530,12 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     dist = Dist()
     try:
-        res = run_reference(args, dist) if args.impl == "reference" else run_gpu(args, dist)
+        if args.impl == "reference":
+            res = run_reference(args, dist)
+        elif args.workload == "prefill":
+            res = run_prefill(args, dist)
+        else:
+            res = run_gpu(args, dist)
         if dist.rank == 0 and res is not None:
             print(json.dumps(res), flush=True)
     finally:
