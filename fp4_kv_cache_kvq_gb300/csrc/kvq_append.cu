@@ -12,9 +12,13 @@
 // SWA KV stays FP8): code = RNE_e4m3(x / s_h) saturating with one fp32 scale
 // per kv head, s_h = amax / 448 over a calibration window (1 if amax == 0).
 //
-// Work decomposition: one thread per 16-value block (32 B of bf16 read with two
-// 16-byte loads, 8 code bytes + 1 scale byte written); consecutive threads take
-// consecutive blocks of the input, so loads and stores are coalesced.
+// FP4 work decomposition: one thread per 2 blocks of one token (K) or per
+// block of one token pair (V, whose code bytes interleave the two tokens);
+// consecutive threads take consecutive spans of the input, so loads and
+// stores coalesce.  Finite blocks take a division-free path whose codes equal
+// those of the IEEE divisions (reciprocal quotient plus one exact residual
+// correction, argued at block_quotient); blocks holding Inf or NaN take the
+// plain IEEE-division quantiser.
 #include "kvq_common.cuh"
 #include "kvq_host.cuh"
 
@@ -74,6 +78,111 @@ __device__ __forceinline__ uint2 quantize_block(const Block16& b, uint32_t& scal
   return make_uint2(w0, w1);
 }
 
+// x / s for a finite bf16 value x and an E4M3 scale s, accurate enough that
+// the saturating RNE conversion to E2M1 gives the code of the exact quotient
+// (and so of the IEEE fp32 division).  q = x * RN(1/s), then one residual
+// step q - (q*s - x) * RN(1/s) (Markstein's correction of a reciprocal
+// quotient).  Why this suffices: x has 8 significant bits and every E2M1
+// rounding midpoint tau * s at most 7, so a quotient that is not on a
+// midpoint sits at least 2^-9 (relative) away from one, far beyond the
+// error of q; on a midpoint x = tau * s the residual q*s - x is exact (a
+// one-ulp step of q times s) and the corrected value rounds to tau itself.
+// The residual is taken as q*s - x so that x = -0.0 gives -0.0 (the sign of
+// every value is kept in its nibble).
+__device__ __forceinline__ float block_quotient(float x, float s, float r) {
+  const float q = __fmul_rn(x, r);
+  return __fmaf_rn(-__fmaf_rn(q, s, -x), r, q);
+}
+
+// Four pairs of fp32 values to four E2M1 byte pairs (saturating RNE, sign
+// kept): byte i = code(a[2i]) | code(a[2i+1]) << 4.
+__device__ __forceinline__ uint32_t e2m1x8_from_f32(float a0, float a1, float a2, float a3, float a4, float a5,
+                                                    float a6, float a7) {
+  uint32_t r;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      " mov.b32 %0, {b0, b1, b2, b3};\n}\n"
+      : "=r"(r)
+      : "f"(a0), "f"(a1), "f"(a2), "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7));
+  return r;
+}
+
+// Scale byte of a block from its amax: RNE_e4m3(amax / 6) saturating, 0 -> 2^-9.
+// amax / 6 by the same corrected reciprocal quotient: every E4M3 rounding
+// midpoint has at most 5 significant bits, so 6 * midpoint has at most 7 and
+// the argument above carries over (a bf16 amax on a midpoint is exact, any
+// other sits 2^-9 away).
+__device__ __forceinline__ uint32_t block_scale_byte(float amax) {
+  constexpr float kSixth = 1.0f / 6.0f;  // RN(1/6)
+  const uint32_t sb = e4m3x2_from_f32(block_quotient(amax, 6.0f, kSixth), 0.0f) & 0xFFu;
+  return sb == 0u ? 0x01u : sb;
+}
+
+// Largest magnitude of 16 bf16 values (packed max of absolute values that
+// propagates NaN): bf16 bits, >= 0x7F80 when the block holds Inf or NaN.
+__device__ __forceinline__ uint32_t bmax_abs(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t block_amax_bits(const uint32_t (&w)[8]) {
+  const uint32_t m = bmax_abs(bmax_abs(bmax_abs(w[0], w[1]), bmax_abs(w[2], w[3])),
+                              bmax_abs(bmax_abs(w[4], w[5]), bmax_abs(w[6], w[7])));
+  return bmax_abs(m, __byte_perm(m, 0u, 0x1032u)) & 0x7FFFu;
+}
+
+// K: 8 code bytes of one finite block (channel 2i low nibble of byte i).
+__device__ __forceinline__ uint2 k_codes_finite(const uint32_t (&w)[8], float s, float r) {
+  uint32_t out[2];
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const uint32_t* u = w + 4 * half;
+    out[half] = e2m1x8_from_f32(
+        block_quotient(bf16_lo(u[0]), s, r), block_quotient(bf16_hi(u[0]), s, r),
+        block_quotient(bf16_lo(u[1]), s, r), block_quotient(bf16_hi(u[1]), s, r),
+        block_quotient(bf16_lo(u[2]), s, r), block_quotient(bf16_hi(u[2]), s, r),
+        block_quotient(bf16_lo(u[3]), s, r), block_quotient(bf16_hi(u[3]), s, r));
+  }
+  return make_uint2(out[0], out[1]);
+}
+
+// One token-pair V item: byte c holds channel c of tokens 2i (low nibble) and
+// 2i+1 (high nibble).  An absent token (not new in this call) is passed as
+// zeros and contributes zero nibbles; the caller keeps the old ones.
+__device__ __forceinline__ uint4 v_pair_codes_finite(const uint32_t (&w0)[8], float s0, float r0,
+                                                     const uint32_t (&w1)[8], float s1, float r1) {
+  uint32_t out[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t a = w0[2 * q], b = w0[2 * q + 1], c = w1[2 * q], d = w1[2 * q + 1];
+    out[q] = e2m1x8_from_f32(
+        block_quotient(bf16_lo(a), s0, r0), block_quotient(bf16_lo(c), s1, r1),
+        block_quotient(bf16_hi(a), s0, r0), block_quotient(bf16_hi(c), s1, r1),
+        block_quotient(bf16_lo(b), s0, r0), block_quotient(bf16_lo(d), s1, r1),
+        block_quotient(bf16_hi(b), s0, r0), block_quotient(bf16_hi(d), s1, r1));
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+struct Raw16 {
+  uint32_t w[8];
+  float amax;
+  bool finite;
+};
+
+__device__ __forceinline__ void load_raw16(const uint16_t* src, Raw16& b) {
+  const uint4 p = __ldg(reinterpret_cast<const uint4*>(src));
+  const uint4 q = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+  b.w[0] = p.x; b.w[1] = p.y; b.w[2] = p.z; b.w[3] = p.w;
+  b.w[4] = q.x; b.w[5] = q.y; b.w[6] = q.z; b.w[7] = q.w;
+  const uint32_t a = block_amax_bits(b.w);
+  b.amax = __uint_as_float(a << 16);
+  b.finite = a < 0x7F80u;
+}
+
 // Spread 8 nibbles (nibble c at bits 4c) to 8 bytes (nibble c in the low half
 // of byte c).
 __device__ __forceinline__ uint64_t spread_nibbles(uint32_t w) {
@@ -84,91 +193,203 @@ __device__ __forceinline__ uint64_t spread_nibbles(uint32_t w) {
   return x;
 }
 
-// Work items: first one per (sequence, new token, kv head, 16-channel block)
-// for K, then one per (sequence, token pair, kv head, block) for V.  A V item
-// owns the 16 interleaved bytes of its pair, so when only one token of the pair
-// is new it keeps the other token's nibbles (read-modify-write, one writer).
-__global__ void __launch_bounds__(256) append_fp4_kernel(const kvq_cache c, int32_t batch, int32_t n_new,
+// A block holding Inf or NaN (rare): reload it and run the plain
+// IEEE-division quantiser.  Returns the 8 code bytes and the scale byte.
+__device__ __noinline__ uint3 quantize_nonfinite(const uint16_t* src) {
+  const Block16 blk = load_bf16x16(src);
+  uint32_t sb;
+  const uint2 q = quantize_block(blk, sb);
+  return make_uint3(q.x, q.y, sb);
+}
+
+// n / d for n < 2^31 without a hardware divide: (umulhi(n, mul) + n) >> shift
+// (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994, the round-up variant with a 33-bit multiplier).
+struct DivU32 {
+  uint32_t mul, shift;
+  static DivU32 make(uint32_t d) {
+    if (d <= 1u) return DivU32{0u, 0u};
+    uint32_t sh = 0;
+    while ((1ull << sh) < d) ++sh;
+    return DivU32{(uint32_t)((((1ull << 32) * ((1ull << sh) - d)) / d) + 1u), sh};
+  }
+  __device__ __forceinline__ uint32_t div(uint32_t n) const { return (__umulhi(n, mul) + n) >> shift; }
+};
+
+// 16-channel blocks per thread (K items, V token-pair items) and the CTAs
+// per SM the register budget is set for.
+constexpr int kAppendBlocksK = 2;
+constexpr int kAppendBlocksV = 1;
+constexpr int kAppendMinCtas = 4;
+
+// Work items, one thread each: one per (sequence, new token, kv head, group
+// of kAppendBlocksK blocks) for K, in the first k_ctas CTAs; then one per
+// (sequence, token pair, kv head, group of kAppendBlocksV blocks) for V.  A V item owns the interleaved
+// bytes of its pair, so when only one token of the pair is new it keeps the
+// other token's nibbles (read-modify-write, one writer).  Consecutive threads
+// take consecutive spans of the input; the row, page and address arithmetic
+// is done once per item, not once per block.  Indices are 32-bit;
+// the host splits the batch so that every launch's item count fits.
+template <int D>
+__global__ void __launch_bounds__(256, kAppendMinCtas) append_fp4_kernel(const kvq_cache c, int32_t b_begin, uint32_t k_items,
+                                                         uint32_t v_items, uint32_t k_ctas, DivU32 div_hkv,
+                                                         DivU32 div_k_per, DivU32 div_v_per, int32_t n_new,
                                                          const int32_t* __restrict__ start_pos,
                                                          const uint16_t* __restrict__ k,
                                                          const uint16_t* __restrict__ v, int32_t* flag) {
-  const Fp4Layout L(c.head_dim, c.page_size);
-  const int nb = L.nb;
-  const int Hkv = c.num_kv_heads;
-  const int D = c.head_dim;
-  const int npair = n_new / 2 + 1;  // token pairs a call of n_new tokens can touch
-  const int64_t nk = (int64_t)batch * n_new * Hkv * nb;
-  const int64_t total = nk + (int64_t)batch * npair * Hkv * nb;
-  uint8_t* pool = static_cast<uint8_t*>(c.data);
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const bool is_k = i < nk;
-    const int64_t e = is_k ? i : i - nk;
-    const int j = (int)(e % nb);
-    int64_t r = e / nb;
-    const int h = (int)(r % Hkv);
-    r /= Hkv;
-    const int per = is_k ? n_new : npair;
-    const int t = (int)(r % per);
-    const int b = (int)(r / per);
-    const int32_t sp = __ldg(start_pos + b);
-    if (sp < 0) {
-      if (is_k) set_flag(flag, KVQ_FLAG_BAD_LENGTH);
-      continue;
-    }
-    // first position handled by this item (K: the token, V: the pair's even token)
-    const int64_t pos = is_k ? (int64_t)sp + t : 2 * (((int64_t)sp >> 1) + t);
-    if (!is_k && pos >= (int64_t)sp + n_new) continue;
-    const int64_t pg = pos / L.P;
-    const int slot = (int)(pos % L.P);
-    if (pg >= c.max_pages_per_seq) {
-      set_flag(flag, KVQ_FLAG_PAGE_OOB);
-      continue;
-    }
-    const int64_t phys = c.page_table ? (int64_t)__ldg(c.page_table + (int64_t)b * c.max_pages_per_seq + pg)
-                                      : (int64_t)b * c.max_pages_per_seq + pg;
-    if (phys < 0 || phys >= c.num_pages) {
-      set_flag(flag, KVQ_FLAG_PAGE_OOB);
-      continue;
-    }
-    uint8_t* grp = pool + L.group(phys, Hkv, h, slot);
-    const int ls = slot % L.G;
-    if (is_k) {
-      const Block16 kb = load_bf16x16(k + (((int64_t)b * n_new + t) * Hkv + h) * D + 16 * j);
-      if (!kb.finite) set_flag(flag, KVQ_FLAG_NONFINITE);
-      uint32_t sb;
-      const uint2 q = quantize_block(kb, sb);
-      *reinterpret_cast<uint2*>(grp + (int64_t)ls * (D / 2) + 8 * j) = q;
-      grp[L.k_scales() + (int64_t)ls * nb + j] = (uint8_t)sb;
-    } else {
-      uint4* dst = reinterpret_cast<uint4*>(grp + L.v_block(ls >> 1, j));
-      uint4 old = make_uint4(0u, 0u, 0u, 0u);
-      uint64_t lo = 0, hi = 0;  // interleaved bytes of channels 0-7 and 8-15
-      uint64_t keep_lo = 0, keep_hi = 0;
+  constexpr int NB = D / 16;
+  constexpr int BK = kAppendBlocksK, BV = kAppendBlocksV;
+  constexpr int NQK = NB / BK, NQV = NB / BV;  // items per (token, head) row
+  const bool is_k = blockIdx.x < k_ctas;
+  const uint32_t i = (is_k ? blockIdx.x : blockIdx.x - k_ctas) * 256u + threadIdx.x;
+  if (i >= (is_k ? k_items : v_items)) return;
+  const uint32_t hkv = (uint32_t)c.num_kv_heads;
+  const int j0 = is_k ? (int)(i % NQK) * BK : (int)(i % NQV) * BV;
+  const uint32_t r = is_k ? i / NQK : i / NQV;
+  const uint32_t r2 = div_hkv.div(r);
+  const int h = (int)(r - r2 * hkv);
+  const uint32_t per = is_k ? (uint32_t)n_new : (uint32_t)(n_new / 2 + 1);
+  const uint32_t bq = (is_k ? div_k_per : div_v_per).div(r2);
+  const uint32_t t = r2 - bq * per;
+  const int b = b_begin + (int)bq;
+  const int32_t sp = __ldg(start_pos + b);
+  if (sp < 0) {
+    if (is_k) set_flag(flag, KVQ_FLAG_BAD_LENGTH);
+    return;
+  }
+  // first position handled by this item (K: the token, V: the pair's even token)
+  const int64_t pos = is_k ? (int64_t)sp + t : 2 * (((int64_t)sp >> 1) + t);
+  const int64_t end = (int64_t)sp + n_new;
+  if (!is_k && pos >= end) return;
+  const int lg_p = __ffs(c.page_size) - 1;
+  const int lg_g = lg_p < 7 ? lg_p : 7;
+  const int G = 1 << lg_g;
+  const int64_t pg = pos >> lg_p;
+  const int slot = (int)(pos & (c.page_size - 1));
+  if (pg >= c.max_pages_per_seq) {
+    set_flag(flag, KVQ_FLAG_PAGE_OOB);
+    return;
+  }
+  const int64_t phys = c.page_table ? (int64_t)__ldg(c.page_table + (int64_t)b * c.max_pages_per_seq + pg)
+                                    : (int64_t)b * c.max_pages_per_seq + pg;
+  if (phys < 0 || phys >= c.num_pages) {
+    set_flag(flag, KVQ_FLAG_PAGE_OOB);
+    return;
+  }
+  const int64_t group_bytes = (int64_t)G * (9 * D / 8);
+  uint8_t* grp = static_cast<uint8_t*>(c.data) +
+                 ((phys * hkv + h) * (c.page_size >> lg_g) + (slot >> lg_g)) * group_bytes;
+  const int ls = slot & (G - 1);
+  const int64_t row = (int64_t)b * n_new;  // first input row of sequence b
+  if (is_k) {
+    const uint16_t* src = k + ((row + t) * hkv + h) * D + 16 * j0;
+    Raw16 kb[BK];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int64_t p = pos + half;
-        const bool mine = p >= sp && p < (int64_t)sp + n_new;
-        if (mine) {
-          const int tt = (int)(p - sp);
-          const Block16 vb = load_bf16x16(v + (((int64_t)b * n_new + tt) * Hkv + h) * D + 16 * j);
-          if (!vb.finite) set_flag(flag, KVQ_FLAG_NONFINITE);
-          uint32_t sb;
-          const uint2 q = quantize_block(vb, sb);
-          lo |= spread_nibbles(q.x) << (4 * half);
-          hi |= spread_nibbles(q.y) << (4 * half);
-          grp[L.v_scale(ls + half, j)] = (uint8_t)sb;
-        } else {
-          const uint64_t m = half ? 0xF0F0F0F0F0F0F0F0ull : 0x0F0F0F0F0F0F0F0Full;
-          keep_lo |= m;
-          keep_hi |= m;
-        }
+    for (int jb = 0; jb < BK; ++jb) load_raw16(src + 16 * jb, kb[jb]);
+    uint32_t codes[2 * BK];
+    uint32_t scales = 0;
+#pragma unroll
+    for (int jb = 0; jb < BK; ++jb) {
+      uint32_t sb;
+      uint2 q;
+      if (kb[jb].finite) {
+        sb = block_scale_byte(kb[jb].amax);
+        const float s = e4m3_to_f32(sb);
+        q = k_codes_finite(kb[jb].w, s, __frcp_rn(s));
+      } else {
+        set_flag(flag, KVQ_FLAG_NONFINITE);
+        const uint3 r3 = quantize_nonfinite(src + 16 * jb);
+        q = make_uint2(r3.x, r3.y);
+        sb = r3.z;
       }
-      if (keep_lo) old = *dst;
-      lo |= (((uint64_t)old.y << 32) | old.x) & keep_lo;
-      hi |= (((uint64_t)old.w << 32) | old.z) & keep_hi;
-      *dst = make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32));
+      codes[2 * jb] = q.x;
+      codes[2 * jb + 1] = q.y;
+      scales |= sb << (8 * jb);
     }
+    uint8_t* cdst = grp + ls * (D / 2) + 8 * j0;
+    uint8_t* sdst = grp + G * (D / 2) + ls * NB + j0;
+    if constexpr (BK == 1) {
+      *reinterpret_cast<uint2*>(cdst) = make_uint2(codes[0], codes[1]);
+      *sdst = (uint8_t)scales;
+    } else {
+#pragma unroll
+      for (int q = 0; q < BK / 2; ++q)
+        reinterpret_cast<uint4*>(cdst)[q] = make_uint4(codes[4 * q], codes[4 * q + 1], codes[4 * q + 2], codes[4 * q + 3]);
+      if constexpr (BK == 2) *reinterpret_cast<uint16_t*>(sdst) = (uint16_t)scales;
+      else *reinterpret_cast<uint32_t*>(sdst) = scales;
+    }
+    return;
+  }
+  // V: token pair row ls/2 of the group
+  const bool mine0 = pos >= sp;
+  const bool mine1 = pos + 1 < end;
+  Raw16 vb[2][BV];
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    const bool m = hf ? mine1 : mine0;
+    const uint16_t* src = v + ((row + (pos + hf - sp)) * hkv + h) * D + 16 * j0;
+#pragma unroll
+    for (int jb = 0; jb < BV; ++jb) {
+      if (m) {
+        load_raw16(src + 16 * jb, vb[hf][jb]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) vb[hf][jb].w[q] = 0u;
+        vb[hf][jb].amax = 0.0f;
+        vb[hf][jb].finite = true;
+      }
+    }
+  }
+  const int pr = ls >> 1;
+  uint8_t* vsc = grp + (int64_t)G * (D + NB) + pr * 2 * NB + 2 * j0;
+  uint64_t sc = 0;  // scale bytes of the item's blocks, token 0 in the even bytes
+#pragma unroll
+  for (int jb = 0; jb < BV; ++jb) {
+    const int j = j0 + jb;
+    const int64_t vblk = (D == 64) ? (int64_t)G * (D / 2 + NB) + pr * D + 8 * ((2 * j) ^ (((pr >> 1) & 1) << 2))
+                                   : (int64_t)G * (D / 2 + NB) + pr * D + 16 * (j ^ ((pr & 3) << 1));
+    uint4* dst = reinterpret_cast<uint4*>(grp + vblk);
+    uint4 codes;
+    uint32_t sb0 = 0, sb1 = 0;
+    if (vb[0][jb].finite && vb[1][jb].finite) {
+      sb0 = block_scale_byte(vb[0][jb].amax);
+      sb1 = block_scale_byte(vb[1][jb].amax);
+      const float s0 = e4m3_to_f32(sb0), s1 = e4m3_to_f32(sb1);
+      codes = v_pair_codes_finite(vb[0][jb].w, s0, __frcp_rn(s0), vb[1][jb].w, s1, __frcp_rn(s1));
+    } else {
+      set_flag(flag, KVQ_FLAG_NONFINITE);
+      uint64_t lo = 0, hi = 0;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        if (!(hf ? mine1 : mine0)) continue;
+        const uint3 q = quantize_nonfinite(v + ((row + (pos + hf - sp)) * hkv + h) * D + 16 * j);
+        lo |= spread_nibbles(q.x) << (4 * hf);
+        hi |= spread_nibbles(q.y) << (4 * hf);
+        (hf ? sb1 : sb0) = q.z;
+      }
+      codes = make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32));
+    }
+    sc |= (uint64_t)(sb0 | (sb1 << 8)) << (16 * jb);
+    if (!(mine0 && mine1)) {
+      // keep the nibbles of the token that is not new
+      const uint32_t keep = mine0 ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
+      const uint4 old = *dst;
+      codes.x |= old.x & keep;
+      codes.y |= old.y & keep;
+      codes.z |= old.z & keep;
+      codes.w |= old.w & keep;
+    }
+    *dst = codes;
+  }
+  if (mine0 && mine1) {
+    if constexpr (BV == 4) *reinterpret_cast<uint2*>(vsc) = make_uint2((uint32_t)sc, (uint32_t)(sc >> 32));
+    else if constexpr (BV == 2) *reinterpret_cast<uint32_t*>(vsc) = (uint32_t)sc;
+    else *reinterpret_cast<uint16_t*>(vsc) = (uint16_t)sc;
+  } else {
+    // keep the scales of the token that is not new
+    const int hf = mine0 ? 0 : 1;
+#pragma unroll
+    for (int jb = 0; jb < BV; ++jb) vsc[2 * jb + hf] = (uint8_t)(sc >> (16 * jb + 8 * hf));
   }
 }
 
@@ -278,16 +499,47 @@ extern "C" kvq_status kvq_append(const kvq_cache* cache, int32_t batch, int32_t 
   if (batch == 0 || n_new == 0) return KVQ_OK;
   if (d_start_pos == nullptr || k == nullptr || v == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
   if (!aligned_to(k, 16) || !aligned_to(v, 16)) return KVQ_ERR_INVALID_ARGUMENT;
-  const int64_t work = (int64_t)batch * (n_new + n_new / 2 + 1) * cache->num_kv_heads * (cache->head_dim / 16);
-  const unsigned grid = grid_for(work, 256);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint16_t* k16 = static_cast<const uint16_t*>(k);
+  const uint16_t* v16 = static_cast<const uint16_t*>(v);
   if (cache->format == KVQ_FORMAT_FP4_E2M1_E4M3_G16) {
-    append_fp4_kernel<<<grid, 256, 0, s>>>(*cache, batch, n_new, d_start_pos, static_cast<const uint16_t*>(k),
-                                           static_cast<const uint16_t*>(v), d_err_flag);
-  } else {
-    append_fp8_kernel<<<grid, 256, 0, s>>>(*cache, batch, n_new, d_start_pos, static_cast<const uint16_t*>(k),
-                                           static_cast<const uint16_t*>(v), d_err_flag);
+    // 32-bit item indices: one sequence's items must fit, the batch is split.
+    const int64_t nqk = cache->head_dim / 16 / kAppendBlocksK;  // items per (token, head)
+    const int64_t nqv = cache->head_dim / 16 / kAppendBlocksV;
+    const int64_t per_seq = (int64_t)n_new * cache->num_kv_heads * nqk;
+    const int64_t limit = (int64_t)1 << 30;
+    if (per_seq > limit) return KVQ_ERR_UNSUPPORTED;
+    const int64_t chunk = limit / per_seq;
+    for (int64_t b0 = 0; b0 < batch; b0 += chunk) {
+      const int64_t bc = (batch - b0 < chunk) ? batch - b0 : chunk;
+      const uint32_t k_items = (uint32_t)(bc * per_seq);
+      const uint32_t v_items = (uint32_t)(bc * (n_new / 2 + 1) * cache->num_kv_heads * nqv);
+      const uint32_t k_ctas = (k_items + 255u) / 256u;
+      const uint32_t grid = k_ctas + (v_items + 255u) / 256u;
+      const DivU32 dh = DivU32::make((uint32_t)cache->num_kv_heads);
+      const DivU32 dk = DivU32::make((uint32_t)n_new);
+      const DivU32 dv = DivU32::make((uint32_t)(n_new / 2 + 1));
+      switch (cache->head_dim) {
+        case 64:
+          append_fp4_kernel<64><<<grid, 256, 0, s>>>(*cache, (int32_t)b0, k_items, v_items, k_ctas, dh, dk, dv, n_new,
+                                                     d_start_pos, k16, v16, d_err_flag);
+          break;
+        case 128:
+          append_fp4_kernel<128><<<grid, 256, 0, s>>>(*cache, (int32_t)b0, k_items, v_items, k_ctas, dh, dk, dv, n_new,
+                                                      d_start_pos, k16, v16, d_err_flag);
+          break;
+        default:
+          append_fp4_kernel<256><<<grid, 256, 0, s>>>(*cache, (int32_t)b0, k_items, v_items, k_ctas, dh, dk, dv, n_new,
+                                                      d_start_pos, k16, v16, d_err_flag);
+          break;
+      }
+      const kvq_status ls = launch_status();
+      if (ls != KVQ_OK) return ls;
+    }
+    return KVQ_OK;
   }
+  const int64_t work = (int64_t)batch * n_new * cache->num_kv_heads * (cache->head_dim / 16);
+  append_fp8_kernel<<<grid_for(work, 256), 256, 0, s>>>(*cache, batch, n_new, d_start_pos, k16, v16, d_err_flag);
   return launch_status();
 }
 

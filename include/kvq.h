@@ -141,7 +141,9 @@ typedef struct kvq_cache {
  * tokens are written (the earlier ones would be overwritten in the same call).
  * Device flags: NONFINITE (the block's codes and scale are whatever the
  * conversion produces), PAGE_OOB (token skipped), BAD_LENGTH (negative start;
- * sequence skipped).
+ * sequence skipped).  Host errors: INVALID_ARGUMENT (bad cache or sizes, NULL
+ * or non-16-byte-aligned k/v), UNSUPPORTED (FP4: n_new * num_kv_heads *
+ * head_dim / 16 above 2^30 in one call; split the tokens over several calls).
  */
 kvq_status kvq_append(const kvq_cache *cache, int32_t batch, int32_t n_new,
                       const int32_t *d_start_pos, const void *k, const void *v,

@@ -104,6 +104,8 @@ def test_invalid_sizes_are_rejected_on_the_host(lib):
     assert lib.kvq_append(ctypes.byref(s), -1, 1, 16, 32, 64, None, None) == 1
     assert lib.kvq_append(ctypes.byref(s), 2, -3, 16, 32, 64, None, None) == 1
     assert lib.kvq_append(ctypes.byref(s), 2, 1, None, 32, 64, None, None) == 1
+    # one sequence's 16-value blocks must fit the kernel's 32-bit item index
+    assert lib.kvq_append(ctypes.byref(s), 2, 1 << 27, 16, 32, 64, None, None) == 2
     # empty work is a no-op that succeeds without a launch
     assert lib.kvq_append(ctypes.byref(s), 0, 5, None, None, None, None, None) == 0
     assert lib.kvq_append(ctypes.byref(s), 2, 0, None, None, None, None, None) == 0
