@@ -508,7 +508,7 @@ extern "C" kvq_status kvq_append(const kvq_cache* cache, int32_t batch, int32_t 
     const int64_t nqv = cache->head_dim / 16 / kAppendBlocksV;
     const int64_t per_seq = (int64_t)n_new * cache->num_kv_heads * nqk;
     const int64_t limit = (int64_t)1 << 30;
-    if (per_seq > limit) return KVQ_ERR_UNSUPPORTED;
+    if ((int64_t)n_new * cache->num_kv_heads * (cache->head_dim / 16) > limit) return KVQ_ERR_UNSUPPORTED;
     const int64_t chunk = limit / per_seq;
     for (int64_t b0 = 0; b0 < batch; b0 += chunk) {
       const int64_t bc = (batch - b0 < chunk) ? batch - b0 : chunk;
