@@ -12,17 +12,18 @@
 //
 // Work decomposition (stream-K over the whole batch).  Every (sequence b,
 // kv head h) pair is a unit; its FP4 positions are cut into chunks of 128
-// tokens.  All units' chunks are laid end to end and the persistent grid (two
-// CTAs per SM) splits that line into equal contiguous ranges, so ragged
-// lengths balance to within one chunk.  A CTA writes one partial (m, l, o) per
-// unit it touches; the merge kernel combines them.
+// tokens.  All units' chunks are laid end to end and the persistent grid
+// (three CTAs per SM) splits that line into equal contiguous ranges, so
+// ragged lengths balance to within one chunk.  A CTA writes one partial
+// (m, l, o) per unit it touches; the merge kernel combines them.
 //
-// CTA = 4 consumer warps + 1 producer warp.  The producer's lane 0 streams the
-// chunk's K codes and V codes (3-D tiled TMA loads, one per page, 64-byte
-// swizzle for head_dim 128) and K/V scale bytes (1-D bulk copies) into a
-// 4-stage ring guarded by mbarriers.  Consumer warp w takes tokens
-// [32w, 32w+32) of each chunk as two independent 16-token slices and runs,
-// per slice:
+// CTA = 4 consumer warps + 1 producer warp.  The pool stores each group of
+// min(page, 128) tokens of one kv head as one contiguous block (K codes, K
+// scales, V token-pair codes, V scales), so the producer's lane 0 fills a
+// stage of the 3-stage ring with one or two cp.async.bulk copies, guarded by
+// mbarriers (every wait bounded; a timeout sets a flag and the CTA exits in
+// order).  Consumer warp w takes tokens [32w, 32w+32) of each chunk as two
+// independent 16-token slices and runs, per slice:
 //   S^T(16 tok x 8 q-rows) = K^(16 x d) Q^T    mma.m16n8k16, K^ dequantised in
 //                                              registers (cvt e2m1x2->f16x2,
 //                                              times the block scale)
@@ -31,10 +32,12 @@
 //   O^T(d x 8) += V^T(d x 16 tok) P^T           mma.m16n8k16, P in f16 moved
 //                                              from the S^T fragment to the B
 //                                              fragment with movmatrix.trans
-// Codes are expanded a 32-bit word (8 codes) at a time.  Tokens sit on the
-// MMA's M side so a GQA group of up to 8 query heads fills
-// N = 8 without padding rows.  The query is pre-scaled per head by a power of
-// two so that its bf16 values are exact in f16; the factor is undone in fp32.
+// A stage's PV products go to fresh accumulators that are folded into O
+// (rescaled only when the running max moved).  Codes are expanded a 32-bit
+// word (8 codes) at a time.  Tokens sit on the MMA's M side so a GQA group of
+// up to 8 query heads fills N = 8 without padding rows.  The query is
+// pre-scaled per head by a power of two so that its bf16 values are exact in
+// f16; the factor is undone in fp32.
 #include "kvq_common.cuh"
 #include "kvq_host.cuh"
 
@@ -45,7 +48,7 @@ constexpr int kChunk = 128;          // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;
 constexpr int kSlices = kChunk / (16 * kConsumerWarps);  // 16-token slices per warp per stage
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kMaxCopies = kChunk / 16;  // pool groups per stage at the smallest page size
 constexpr int kNG = 8;  // query rows per kv head held by one tile (G <= 8)
 constexpr float kLazySlack = 8.0f;
@@ -566,7 +569,7 @@ __device__ void flush_unit(const DecodeParams& p, ConsumerState<D>& st, Smem<D>&
 }
 
 template <int D, int GT>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
     decode_fp4_kernel(const DecodeParams p) {
   using G = Geo<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -772,7 +775,7 @@ WsLayout ws_layout(int64_t batch, int64_t hkv, int64_t g, int64_t d, int64_t cta
   return L;
 }
 
-int decode_ctas() { return 2 * device_sm_count(); }
+int decode_ctas() { return 3 * device_sm_count(); }
 
 template <int D, int GT>
 kvq_status launch_decode_g(const DecodeParams& dp, cudaStream_t s, int ctas) {
