@@ -46,6 +46,8 @@ NQ = 8              # distinct query sets cycled through the steps
 FALLBACK_HBM_GBS = 6800.0
 DECODE_SRC = os.path.join(ROOT, "fp4_kv_cache_kvq_gb300", "csrc", "kvq_decode.cu")
 PROFILE = os.path.join(ROOT, "profiles", "decode_fp4_long_context.md")
+APPEND_SRC = os.path.join(ROOT, "fp4_kv_cache_kvq_gb300", "csrc", "kvq_append.cu")
+APPEND_PROFILE = os.path.join(ROOT, "profiles", "append_fp4_prefill.md")
 
 
 # ----------------------------------------------------------------- distributed plumbing
@@ -144,12 +146,12 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic():
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current decode source (else None)."""
+def profiled_traffic(profile=PROFILE, src=DECODE_SRC):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
     try:
-        text = open(PROFILE).read()
-        sha = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()
+        text = open(profile).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
         fields = dict(line.split(":", 1) for line in text.splitlines() if line.startswith(("traffic_", "source_")))
         if fields.get("source_sha256", "").strip() != sha:
             return None
@@ -408,7 +410,8 @@ def run_prefill(args, dist: Dist):
                    "l2": "inputs larger than L2 (1.07 GB of bf16 per step), no flush",
                    "parallelism": f"replicas x{dist.world}"},
         "roofline": {"bound": "hbm", "kernel": "append_fp4_kernel", "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src, "traffic": None,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
+                     "traffic": profiled_traffic(APPEND_PROFILE, APPEND_SRC),
                      "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": secs * 1e3 / K},
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": 2 * k.numel() * 2, "d2h_bytes_per_step": 4,
                 "steps": Ke},
