@@ -758,6 +758,51 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
   p.out[qrow * D + tid] = l > 0.0f ? o / l : 0.0f;
 }
 
+// Merge without a window: one CTA per unit, thread (row r, 4 channels) takes
+// float4 partials.  Loads of the unit's partials are independent of one
+// another (four partials in flight per step), so a unit costs a few L2 round
+// trips whatever its split count.
+template <int D>
+__global__ void __launch_bounds__(kNG * D / 4) merge_splits_kernel(const MergeParams p) {
+  const int u = blockIdx.x;
+  const int b = u / p.hkv, h = u % p.hkv;
+  const int r = threadIdx.x / (D / 4), c4 = threadIdx.x % (D / 4);
+  if (r >= p.g) return;
+  int32_t T = __ldg(p.lens + b);
+  if (T < 0) {
+    if (threadIdx.x == 0 && h == 0) set_flag(p.flag, KVQ_FLAG_BAD_LENGTH);
+    T = 0;
+  }
+  const int64_t qrow = (int64_t)b * p.hq + (int64_t)h * p.g + r;
+  float4* dst = reinterpret_cast<float4*>(p.out + qrow * D) + c4;
+  if (T == 0) {
+    *dst = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  const int2 rec = __ldg(p.unit_rec + u);
+  float mx = -INFINITY;
+#pragma unroll 4
+  for (int k = 0; k < rec.y; ++k) mx = fmaxf(mx, __ldcg(p.part_ml + ((int64_t)(rec.x + k) * p.g + r) * 2));
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  float l = 0.0f;
+  if (mx != -INFINITY) {
+#pragma unroll 4
+    for (int k = 0; k < rec.y; ++k) {
+      const int64_t sl = (int64_t)(rec.x + k) * p.g + r;
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + sl);
+      const float4 ov = __ldcg(reinterpret_cast<const float4*>(p.part_o + sl * D) + c4);
+      const float f = ml.x == -INFINITY ? 0.0f : fast_exp2(ml.x - mx);
+      o.x = fmaf(f, ov.x, o.x);
+      o.y = fmaf(f, ov.y, o.y);
+      o.z = fmaf(f, ov.z, o.z);
+      o.w = fmaf(f, ov.w, o.w);
+      l = fmaf(f, ml.y, l);
+    }
+  }
+  const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+  *dst = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+}
+
 // ------------------------------------------------------------------ host side
 struct WsLayout {
   size_t rec_off, ml_off, o_off, total;
@@ -882,7 +927,14 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* global, const kvq_cache* 
   mp.hq = num_q_heads;
   mp.head_dim = D;
   mp.qk_log2 = dp.qk_log2;
-  const int msmem = (D + (swa ? swa->page_size : 0) + 4) * (int)sizeof(float);
+  if (swa == nullptr) {
+    if (D == 128)
+      merge_splits_kernel<128><<<(unsigned)(batch * hkv), kNG * 128 / 4, 0, s>>>(mp);
+    else
+      merge_splits_kernel<64><<<(unsigned)(batch * hkv), kNG * 64 / 4, 0, s>>>(mp);
+    return launch_status();
+  }
+  const int msmem = (D + swa->page_size + 4) * (int)sizeof(float);
   merge_kernel<<<(unsigned)(batch * hkv * g), 128, msmem, s>>>(mp);
   return launch_status();
 }
