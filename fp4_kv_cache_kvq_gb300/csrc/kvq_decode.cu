@@ -825,9 +825,15 @@ int decode_ctas() { return 3 * device_sm_count(); }
 template <int D, int GT>
 kvq_status launch_decode_g(const DecodeParams& dp, cudaStream_t s, int ctas) {
   const int smem = Geo<D>::kSmemBytes;
-  if (cudaFuncSetAttribute(decode_fp4_kernel<D, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-      cudaSuccess)
-    return KVQ_ERR_CUDA;
+  static DeviceOnce attr_set;  // the shared-memory opt-in, once per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (attr_set.pending(dev)) {
+    if (cudaFuncSetAttribute(decode_fp4_kernel<D, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return KVQ_ERR_CUDA;
+    attr_set.mark(dev);
+  }
   decode_fp4_kernel<D, GT><<<ctas, kThreads, smem, s>>>(dp);
   return launch_status();
 }
@@ -950,7 +956,6 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 256;
 std::mutex g_scratch_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 

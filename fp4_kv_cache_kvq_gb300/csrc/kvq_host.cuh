@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <stdint.h>
 
 #include "../../include/kvq.h"
@@ -39,12 +41,32 @@ inline kvq_status check_cache(const kvq_cache* c, int32_t batch) {
   return KVQ_ERR_INVALID_ARGUMENT;
 }
 
+constexpr int kMaxDevices = 256;
+
+// SM count of the current device, queried once per device.
 inline int device_sm_count() {
-  int dev = 0, sms = 0;
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < kMaxDevices) cache[dev].store(sms, std::memory_order_relaxed);
   return sms;
 }
+
+// Per-device once-only flag for one-time host setup (a kernel's attributes).
+struct DeviceOnce {
+  std::atomic<bool> done[kMaxDevices];
+  // true when the setup for the current device still has to run
+  bool pending(int dev) const { return dev < 0 || dev >= kMaxDevices || !done[dev].load(std::memory_order_acquire); }
+  void mark(int dev) {
+    if (dev >= 0 && dev < kMaxDevices) done[dev].store(true, std::memory_order_release);
+  }
+};
 
 inline unsigned grid_for(int64_t work_items, int threads) {
   int64_t g = (work_items + threads - 1) / threads;

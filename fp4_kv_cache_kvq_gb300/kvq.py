@@ -215,8 +215,8 @@ def decode_attn(cache: Fp4Cache, seq_lens: torch.Tensor, q: torch.Tensor, softma
     if out is None:
         out = torch.empty((batch, hq, d), dtype=torch.float32, device=q.device)
     _need(out, torch.float32, "out")
-    need = decode_workspace_bytes(batch, hq, cache.num_kv_heads, d)
-    if workspace is None:
+    if workspace is None:  # a caller's workspace is size-checked by the library
+        need = decode_workspace_bytes(batch, hq, cache.num_kv_heads, d)
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(d)
