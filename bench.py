@@ -168,9 +168,10 @@ def fp4_bytes_per_token(w) -> int:
 class Setup:
     """The resident FP4 cache of a workload plus the per-step inputs."""
 
-    def __init__(self, w, seed: int, device):
+    def __init__(self, w, seed: int, device, layers: int = 1):
         from fp4_kv_cache_kvq_gb300 import kvq
         self.w = w
+        self.layers = layers
         self.kvq = kvq
         self.lens0 = workloads.lengths(w, seed)
         table, num_pages, max_pages = workloads.page_layout(w, self.lens0, reserve=CYCLE, seed=seed)
@@ -202,6 +203,22 @@ class Setup:
             start = torch.tensor([n - W for n in self.lens0], dtype=torch.int32, device=device)
             kvq.append(self.swa, start, kw, vw, err=self.err)
             del kw, vw, tails_k, tails_v
+        # further layers: their own copies of the cache (same contents)
+        self.caches = [self.cache]
+        self.swas = [self.swa]
+        for _ in range(1, layers):
+            c = kvq.Fp4Cache(w.num_kv_heads, w.head_dim, w.page_size, num_pages, max_pages,
+                             page_table=self.table, device=device)
+            c.pool.copy_(self.cache.pool)
+            self.caches.append(c)
+            if self.swa is not None:
+                sw = kvq.Fp8WindowCache(w.batch, w.num_kv_heads, w.head_dim, w.window, device=device)
+                for dst, src in ((sw.k_codes, self.swa.k_codes), (sw.v_codes, self.swa.v_codes),
+                                 (sw.k_scales, self.swa.k_scales), (sw.v_scales, self.swa.v_scales)):
+                    dst.copy_(src)
+                self.swas.append(sw)
+            else:
+                self.swas.append(None)
         toks = [workloads.step_tokens(w, i, seed=seed, device=device) for i in range(CYCLE)]
         self.k_new = [t[0] for t in toks]
         self.v_new = [t[1] for t in toks]
@@ -212,28 +229,35 @@ class Setup:
         self.kv_tokens = [sum(self.lens0) + (i + 1) * w.batch for i in range(CYCLE)]
         self.scale = 1.0 / math.sqrt(w.head_dim)
         B, Hq, D = w.batch, w.num_q_heads, w.head_dim
-        self.out = torch.empty((B, Hq, D), dtype=torch.float32, device=device)
+        self.outs = [torch.empty((B, Hq, D), dtype=torch.float32, device=device) for _ in range(layers)]
+        self.out = self.outs[-1]
         nbytes = kvq.decode_workspace_bytes(B, Hq, w.num_kv_heads, D)
         self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
         torch.cuda.synchronize()
 
     def step(self, i: int, q=None, k=None, v=None, ev=None):
+        """One decode step: append the new token to every layer's caches,
+        then decode attention for every layer (the same token and query per
+        layer).  Returns the KV-tokens attended (all layers)."""
         s = i % CYCLE
         kvq = self.kvq
         kk = self.k_new[s] if k is None else k
         vv = self.v_new[s] if v is None else v
-        kvq.append(self.cache, self.pos[s], kk, vv, err=self.err)
-        if self.swa is not None:
-            kvq.append(self.swa, self.pos[s], kk, vv, err=self.err)
+        for cache, swa in zip(self.caches, self.swas):
+            kvq.append(cache, self.pos[s], kk, vv, err=self.err)
+            if swa is not None:
+                kvq.append(swa, self.pos[s], kk, vv, err=self.err)
         if ev is not None:
             ev[0].record()
-        kvq.decode_attn(self.cache, self.lens[s], self.q[i % NQ] if q is None else q, self.scale, swa=self.swa,
-                        out=self.out, workspace=self.ws, err=self.err)
+        qq = self.q[i % NQ] if q is None else q
+        for cache, swa, out in zip(self.caches, self.swas, self.outs):
+            kvq.decode_attn(cache, self.lens[s], qq, self.scale, swa=swa, out=out, workspace=self.ws, err=self.err)
         if ev is not None:
             ev[1].record()
-        return self.kv_tokens[s]
+        return self.kv_tokens[s] * self.layers
 
     def decode_algorithmic_bytes(self, i: int) -> int:
+        """Algorithmic bytes of one layer's decode call at step i."""
         w = self.w
         s = i % CYCLE
         win = min(w.window, min(self.lens0) + s + 1) if w.window else 0
@@ -253,7 +277,8 @@ def run_gpu(args, dist: Dist):
     from fp4_kv_cache_kvq_gb300 import build
     build.build()
     w = workloads.WORKLOADS[args.workload]
-    st = Setup(w, args.seed, device)
+    L = args.layers
+    st = Setup(w, args.seed, device, layers=L)
     K, Wm = args.steps, args.warmup
     for i in range(Wm):
         st.step(i)
@@ -303,19 +328,19 @@ def run_gpu(args, dist: Dist):
         raise RuntimeError(f"device error flag {st.err.item()} during the timed steps")
     value, max_s = combine_ranks(dist, tokens, elapsed_s)
     dec_bytes = statistics.mean(st.decode_algorithmic_bytes(Wm + i) for i in range(K))
-    dec_s = statistics.mean(decode_ms) / 1e3
+    dec_s = statistics.mean(decode_ms) / 1e3 / L  # one layer's decode call
     achieved = dec_bytes / dec_s / 1e9
     peak, peak_src = measured_hbm_peak()
     # append: read the new bf16 K and V, write their codes and scales
     append_bytes = w.batch * (2 * w.num_kv_heads * w.head_dim * 2 + fp4_bytes_per_token(w))
-    step_bytes = dec_bytes + append_bytes
+    step_bytes = L * (dec_bytes + append_bytes)
 
     # ---- end to end through the public API with pinned host buffers
     Ke = min(K, max(50, K // 4))
     q_host = [q.cpu().pin_memory() for q in st.q]
     k_host = [k.cpu().pin_memory() for k in st.k_new]
     v_host = [v.cpu().pin_memory() for v in st.v_new]
-    out_host = torch.empty(st.out.shape, dtype=torch.float32).pin_memory()
+    outs_host = [torch.empty(st.out.shape, dtype=torch.float32).pin_memory() for _ in range(L)]
     q_dev, k_dev, v_dev = torch.empty_like(st.q[0]), torch.empty_like(st.k_new[0]), torch.empty_like(st.v_new[0])
     torch.cuda.synchronize()
     dist.barrier()
@@ -328,22 +353,24 @@ def run_gpu(args, dist: Dist):
         k_dev.copy_(k_host[s], non_blocking=True)
         v_dev.copy_(v_host[s], non_blocking=True)
         e2e_tokens += st.step(Wm + i, q=q_dev, k=k_dev, v=v_dev)
-        out_host.copy_(st.out, non_blocking=True)
+        for oh, od in zip(outs_host, st.outs):
+            oh.copy_(od, non_blocking=True)
     e1.record()
     torch.cuda.synchronize()
     dist.barrier()
     e2e_value, _ = combine_ranks(dist, e2e_tokens, e0.elapsed_time(e1) / 1e3)
     h2d = q_dev.numel() * 2 + k_dev.numel() * 2 + v_dev.numel() * 2
-    d2h = out_host.numel() * 4
+    d2h = sum(oh.numel() for oh in outs_host) * 4
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": K, "warmup": Wm,
         "ms_per_step": max_s * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16", "data": "synthetic",
-        "config": {"workload": f"{w.name}: {w.description}; step = append 1 token/seq + decode attention",
+        "config": {"workload": f"{w.name}: {w.description}; step = append 1 token/seq + decode attention"
+                   + (f", {L} layers" if L > 1 else ""), "layers": L,
                    "batch": w.batch, "kv_heads": w.num_kv_heads, "q_heads": w.num_q_heads,
                    "head_dim": w.head_dim, "context": w.context, "page_size": w.page_size,
-                   "cache_bytes": st.cache.nbytes,
+                   "cache_bytes": st.cache.nbytes * L,
                    "l2": (f"cache smaller than 2 x L2: {2 * l2_bytes} B written before every step, steps timed "
                           f"one by one (warm-L2 rate without the flush: {warm_value:.4g} {UNIT})") if small
                    else f"inputs larger than L2 (FP4 cache {st.cache.nbytes} B vs {l2_bytes} B L2), no flush",
@@ -360,7 +387,7 @@ def run_gpu(args, dist: Dist):
                      "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_s * 1e3},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": Ke},
-        "gpu_launches": (4 if w.window else 3) * K,
+        "gpu_launches": L * (4 if w.window else 3) * K,
     }
     if clk is not None:
         result["clocks"] = clk
@@ -534,7 +561,8 @@ def run_reference(args, dist: Dist):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{w.name}: {w.description}; step = append 1 token/seq + decode attention",
+        "config": {"workload": f"{w.name}: {w.description}; step = append 1 token/seq + decode attention"
+                   + (f", {args.layers} layers" if args.layers > 1 else ""), "layers": args.layers,
                    "batch": w.batch, "kv_heads": w.num_kv_heads, "q_heads": w.num_q_heads,
                    "head_dim": w.head_dim, "context": w.context, "page_size": w.page_size,
                    "parallelism": "host threads"},
@@ -553,6 +581,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="long_context",
                     choices=["long_context", "gqa_outliers", "paged_ragged", "swa_append", "tiny", "prefill"])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=1,
+                    help="layers per step, each with its own cache (long_context at 4 layers: 4.84 GB)")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
