@@ -656,108 +656,6 @@ struct MergeParams {
   float qk_log2;
 };
 
-// Block-wide reductions over 128 threads (4 warps).
-__device__ __forceinline__ float block_max128(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  return fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-}
-
-__device__ __forceinline__ float block_sum128(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  return (red[0] + red[1]) + (red[2] + red[3]);
-}
-
-// One CTA per (unit, query row of the group), one thread per channel: the FP8
-// window's softmax terms for that query row (fp32 values x^ = E4M3(c) * s_h,
-// fp32 dot products), then the log-sum-exp merge of that window with every
-// FP4 partial of the unit.
-__global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
-  extern __shared__ float msm[];
-  const int D = p.head_dim;
-  const int u = blockIdx.x / p.g, r = blockIdx.x % p.g;
-  const int b = u / p.hkv, h = u % p.hkv;
-  const int tid = threadIdx.x;
-  int32_t T = __ldg(p.lens + b);
-  if (T < 0) {
-    if (tid == 0 && h == 0 && r == 0) set_flag(p.flag, KVQ_FLAG_BAD_LENGTH);
-    T = 0;
-  }
-  const int w = (p.k8 != nullptr) ? min(p.window, T) : 0;
-  const int nch = (T - w + kChunk - 1) / kChunk;
-  const int64_t qrow = (int64_t)b * p.hq + (int64_t)h * p.g + r;
-  float mw = -INFINITY, lw = 0.0f, ow = 0.0f;
-  if (w > 0) {
-    float* qs = msm;             // [D]
-    float* sc = qs + D;          // [window]
-    float* red = sc + p.window;  // [4]
-    if (tid < D) qs[tid] = __uint_as_float((uint32_t)p.q[qrow * D + tid] << 16);
-    __syncthreads();
-    const float sk = __ldg(p.k8_scale + h), sv = __ldg(p.v8_scale + h);
-    const uint8_t* kbase = p.k8 + ((int64_t)b * p.hkv + h) * p.window * D;
-    const uint8_t* vbase = p.v8 + ((int64_t)b * p.hkv + h) * p.window * D;
-    float lmax = -INFINITY;
-    for (int t = tid; t < w; t += blockDim.x) {
-      const uint8_t* krow = kbase + (int64_t)((T - w + t) % p.window) * D;
-      float acc = 0.0f;
-      for (int ch = 0; ch < D; ch += 16) {
-        const uint4 cw = *reinterpret_cast<const uint4*>(krow + ch);
-        const uint32_t ws[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float2 f = f16x2_to_float2(f16x2_from_e4m3x2((ws[q >> 1] >> (16 * (q & 1))) & 0xFFFFu));
-          acc = fmaf(qs[ch + 2 * q], f.x * sk, acc);
-          acc = fmaf(qs[ch + 2 * q + 1], f.y * sk, acc);
-        }
-      }
-      sc[t] = acc * p.qk_log2;
-      lmax = fmaxf(lmax, sc[t]);
-    }
-    mw = block_max128(lmax, red);
-    float lsum = 0.0f;
-    for (int t = tid; t < w; t += blockDim.x) {
-      const float e = fast_exp2(sc[t] - mw);
-      sc[t] = e;
-      lsum += e;
-    }
-    lw = block_sum128(lsum, red);  // its barriers also publish sc[]
-    if (tid < D) {
-      for (int t = 0; t < w; ++t) {
-        const float x = e4m3_to_f32(vbase[(int64_t)((T - w + t) % p.window) * D + tid]) * sv;
-        ow = fmaf(sc[t], x, ow);
-      }
-    }
-  }
-  if (tid >= D) return;
-  const int2 rec = nch > 0 ? p.unit_rec[u] : make_int2(0, 0);
-  float mx = mw;
-  for (int k = 0; k < rec.y; ++k) mx = fmaxf(mx, p.part_ml[((int64_t)(rec.x + k) * p.g + r) * 2]);
-  float o = 0.0f, l = 0.0f;
-  if (mx != -INFINITY) {
-    if (w > 0 && mw != -INFINITY) {
-      const float f = fast_exp2(mw - mx);
-      o = f * ow;
-      l = f * lw;
-    }
-    for (int k = 0; k < rec.y; ++k) {
-      const int64_t sl = (int64_t)(rec.x + k) * p.g + r;
-      const float m = p.part_ml[sl * 2];
-      if (m == -INFINITY) continue;
-      const float f = fast_exp2(m - mx);
-      o = fmaf(f, p.part_o[sl * D + tid], o);
-      l = fmaf(f, p.part_ml[sl * 2 + 1], l);
-    }
-  }
-  p.out[qrow * D + tid] = l > 0.0f ? o / l : 0.0f;
-}
-
 // Merge without a window: one CTA per unit, thread (row r, 4 channels) takes
 // float4 partials.  Loads of the unit's partials are independent of one
 // another (four partials in flight per step), so a unit costs a few L2 round
@@ -803,7 +701,176 @@ __global__ void __launch_bounds__(kNG * D / 4) merge_splits_kernel(const MergePa
   *dst = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
 }
 
+// Merge with the FP8 window: CTAs of 256 threads, one per (unit, slice of
+// the group's query rows: 2 rows at head_dim 128, 4 at 64).
+//   scores: thread (token t, row half) takes window token t for its rows (its
+//           K row read once as uint4s; fp32 x^ = E4M3(c) * s_h, fp32 dot
+//           products in channel order);
+//   softmax per row, a warp each;
+//   PV:     the window's V is staged 128 tokens at a time in shared memory
+//           (coalesced uint4 loads, token order); thread (channel c, row
+//           group) accumulates its rows over the tile;
+// then the log-sum-exp merge of the window with the unit's FP4 partials.
+constexpr int kWinThreads = 256;
+// CTAs per unit, each a slice of the query rows (every thread keeps at least
+// one row in the scores and in PV)
+template <int D>
+__host__ __device__ constexpr int win_row_split() { return D == 128 ? 4 : 2; }
+constexpr int kWinTile = 128;  // window tokens staged per V tile
+
+template <int D>
+__global__ void __launch_bounds__(kWinThreads) merge_window_kernel(const MergeParams p) {
+  constexpr int kRows = kNG / win_row_split<D>();             // query rows of this CTA
+  constexpr int kRowsQK = kRows / (kWinThreads / kWinTile);  // query rows per thread in the scores
+  constexpr int kGroupsPV = kWinThreads / D;                 // row groups in PV
+  constexpr int kRowsPV = kRows / kGroupsPV;                 // query rows per thread in PV
+  static_assert(kRowsQK >= 1 && kRowsPV >= 1, "row split");
+  extern __shared__ float wsm[];
+  const int W = p.window;
+  float* qs = wsm;                                   // [kRows][D] fp32 query rows
+  float* sc = qs + kRows * D;                        // [kRows][W] scores, then probabilities
+  float* stat = sc + kRows * W;                      // [kRows] max, [kRows] sum
+  uint8_t* vt = reinterpret_cast<uint8_t*>(stat + 2 * kRows);  // [kWinTile][D] V codes
+  const int g = max(0, min(kRows, p.g - (int)blockIdx.y * kRows));  // rows of this CTA
+  const int u = blockIdx.x;
+  const int b = u / p.hkv, h = u % p.hkv;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int32_t T = __ldg(p.lens + b);
+  if (T < 0) {
+    if (tid == 0 && h == 0) set_flag(p.flag, KVQ_FLAG_BAD_LENGTH);
+    T = 0;
+  }
+  const int w = min(W, T);
+  const int nch = (T - w + kChunk - 1) / kChunk;
+  if (g == 0) return;
+  const int rbase = blockIdx.y * kRows;  // first row of the group handled here
+  const int64_t qrow0 = (int64_t)b * p.hq + (int64_t)h * p.g + rbase;
+  for (int i = tid; i < kRows * D; i += kWinThreads)
+    qs[i] = i < g * D ? __uint_as_float((uint32_t)p.q[qrow0 * D + i] << 16) : 0.0f;
+  __syncthreads();
+  const int64_t ring = ((int64_t)b * p.hkv + h) * W;
+  const int first = ((T - w) % W + W) % W;  // ring slot of the window's first token
+  if (w > 0) {
+    const float sk = __ldg(p.k8_scale + h);
+    const int r0 = (tid / kWinTile) * kRowsQK;
+    for (int t = tid % kWinTile; t < w; t += kWinTile) {
+      const int slot = first + t < W ? first + t : first + t - W;
+      const uint4* krow = reinterpret_cast<const uint4*>(p.k8 + (ring + slot) * D);
+      uint4 kc[D / 16];
+#pragma unroll
+      for (int c16 = 0; c16 < D / 16; ++c16) kc[c16] = __ldg(krow + c16);
+      float acc[kRowsQK];
+#pragma unroll
+      for (int r = 0; r < kRowsQK; ++r) acc[r] = 0.0f;
+#pragma unroll
+      for (int c16 = 0; c16 < D / 16; ++c16) {
+        const uint32_t ws4[4] = {kc[c16].x, kc[c16].y, kc[c16].z, kc[c16].w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float2 f = f16x2_to_float2(f16x2_from_e4m3x2((ws4[j >> 1] >> (16 * (j & 1))) & 0xFFFFu));
+          const float x0 = f.x * sk, x1 = f.y * sk;
+          const int ch = 16 * c16 + 2 * j;
+#pragma unroll
+          for (int r = 0; r < kRowsQK; ++r)
+            acc[r] = fmaf(qs[(r0 + r) * D + ch + 1], x1, fmaf(qs[(r0 + r) * D + ch], x0, acc[r]));
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kRowsQK; ++r)
+        if (r0 + r < g) sc[(r0 + r) * W + t] = acc[r] * p.qk_log2;
+    }
+    __syncthreads();
+    for (int r = warp; r < g; r += kWinThreads / 32) {
+      float mx = -INFINITY;
+      for (int t = lane; t < w; t += 32) mx = fmaxf(mx, sc[r * W + t]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+      float sum = 0.0f;
+      for (int t = lane; t < w; t += 32) {
+        const float e = fast_exp2(sc[r * W + t] - mx);
+        sc[r * W + t] = e;
+        sum += e;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+      if (lane == 0) {
+        stat[r] = mx;
+        stat[kRows + r] = sum;
+      }
+    }
+  }
+  const int c = tid % D, rp = (tid / D) * kRowsPV;
+  float ow[kRowsPV];
+#pragma unroll
+  for (int r = 0; r < kRowsPV; ++r) ow[r] = 0.0f;
+  if (w > 0) {
+    const float sv = __ldg(p.v8_scale + h);
+    for (int t0 = 0; t0 < w; t0 += kWinTile) {
+      const int n = min(kWinTile, w - t0);
+      __syncthreads();  // scores and stats published; the previous tile consumed
+      for (int i = tid; i < n * (D / 16); i += kWinThreads) {
+        const int t = i / (D / 16), c16 = i % (D / 16);
+        const int slot = first + t0 + t < W ? first + t0 + t : first + t0 + t - W;
+        reinterpret_cast<uint4*>(vt + t * D)[c16] = __ldg(reinterpret_cast<const uint4*>(p.v8 + (ring + slot) * D) + c16);
+      }
+      __syncthreads();
+#pragma unroll 8
+      for (int t = 0; t < n; ++t) {
+        const float x = e4m3_to_f32(vt[t * D + c]) * sv;
+#pragma unroll
+        for (int r = 0; r < kRowsPV; ++r) ow[r] = fmaf(sc[(rp + r) * W + t0 + t], x, ow[r]);
+      }
+    }
+  }
+  const int2 rec = nch > 0 ? __ldg(p.unit_rec + u) : make_int2(0, 0);
+#pragma unroll
+  for (int r = 0; r < kRowsPV; ++r) {
+    const int row = rp + r;
+    if (row >= g) break;
+    const float mw = w > 0 ? stat[row] : -INFINITY;
+    float mx = mw;
+    for (int k = 0; k < rec.y; ++k) mx = fmaxf(mx, __ldcg(p.part_ml + ((int64_t)(rec.x + k) * p.g + rbase + row) * 2));
+    float o = 0.0f, l = 0.0f;
+    if (mx != -INFINITY) {
+      if (mw != -INFINITY) {
+        const float f = fast_exp2(mw - mx);
+        o = f * ow[r];
+        l = f * stat[kRows + row];
+      }
+      for (int k = 0; k < rec.y; ++k) {
+        const int64_t sl = (int64_t)(rec.x + k) * p.g + rbase + row;
+        const float m = __ldcg(p.part_ml + sl * 2);
+        if (m == -INFINITY) continue;
+        const float f = fast_exp2(m - mx);
+        o = fmaf(f, __ldcg(p.part_o + sl * D + c), o);
+        l = fmaf(f, __ldcg(p.part_ml + sl * 2 + 1), l);
+      }
+    }
+    p.out[(qrow0 + row) * D + c] = l > 0.0f ? o / l : 0.0f;
+  }
+}
+
 // ------------------------------------------------------------------ host side
+int window_smem_bytes(int d, int window) {
+  const int rows = kNG / (d == 128 ? win_row_split<128>() : win_row_split<64>());
+  return (rows * d + rows * window + 2 * rows) * (int)sizeof(float) + kWinTile * d;
+}
+
+template <int D>
+kvq_status launch_window_merge(const MergeParams& mp, cudaStream_t s, int smem, int64_t units) {
+  static DeviceOnce attr_set;  // opt in to the largest window's shared memory, once per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (attr_set.pending(dev)) {
+    if (cudaFuncSetAttribute(merge_window_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             window_smem_bytes(D, kMaxWindow)) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+    attr_set.mark(dev);
+  }
+  merge_window_kernel<D><<<dim3((unsigned)units, win_row_split<D>()), kWinThreads, smem, s>>>(mp);
+  return launch_status();
+}
+
 struct WsLayout {
   size_t rec_off, ml_off, o_off, total;
 };
@@ -940,9 +1007,10 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* global, const kvq_cache* 
       merge_splits_kernel<64><<<(unsigned)(batch * hkv), kNG * 64 / 4, 0, s>>>(mp);
     return launch_status();
   }
-  const int msmem = (D + swa->page_size + 4) * (int)sizeof(float);
-  merge_kernel<<<(unsigned)(batch * hkv * g), 128, msmem, s>>>(mp);
-  return launch_status();
+  const int wsmem = window_smem_bytes(D, swa->page_size);
+  st = D == 128 ? launch_window_merge<128>(mp, s, wsmem, batch * hkv)
+                : launch_window_merge<64>(mp, s, wsmem, batch * hkv);
+  return st;
 }
 
 // ------------------------------------------------------------------ decode without caller scratch

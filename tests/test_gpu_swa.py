@@ -88,6 +88,16 @@ def test_small_window_many_steps():
     run_loop(w, [40] * 2, steps=40, check_steps=set(range(1, 41, 3)), units_of_step=every)
 
 
+@pytest.mark.parametrize("W,T0", [(1024, 1500), (1024, 700), (200, 450)])
+def test_large_and_odd_windows(W, T0):
+    """Windows spanning several 128-token V tiles (a ragged last tile), the
+    largest window the library takes, and a window still filling up."""
+    w = workloads.scaled(workloads.WORKLOADS["swa_append"], batch=2, num_kv_heads=2, num_q_heads=16,
+                         context=T0, window=W)
+    every = lambda s: [(b, h) for b in range(2) for h in range(2)]  # noqa: E731
+    run_loop(w, [T0] * 2, steps=2, check_steps={1, 2}, units_of_step=every)
+
+
 def test_swa_append_workload_full_size_sampled():
     w = workloads.WORKLOADS["swa_append"]
     rng = np.random.default_rng(3)
