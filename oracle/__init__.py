@@ -17,6 +17,10 @@ tests compare against:
   * ``attend`` -- fp64 softmax attention over dequantised K/V ("Quantising the
     KV cache", section "Code": the quantised K and V replace the real ones
     ahead of an unchanged attention).
+  * ``fp16_encode`` / ``int_quantize`` / ``int_dequantize`` -- the
+    symmetric INT-b quantisers with one FP16 scale per token or per channel
+    of the bit-width sweep ("Quantising the KV cache", table and section
+    "Per token or per channel?").
   * ``decode_unit`` -- one (sequence, kv head) decode: FP4 for positions
     [0, T - W'), FP8 for the last W' = min(W, T) positions, one softmax over
     the union.
@@ -42,6 +46,8 @@ _lib = None
 _u8p = ctypes.POINTER(ctypes.c_uint8)
 _f32p = ctypes.POINTER(ctypes.c_float)
 _f64p = ctypes.POINTER(ctypes.c_double)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_i8p = ctypes.POINTER(ctypes.c_int8)
 
 
 def build(force: bool = False) -> str:
@@ -86,6 +92,18 @@ def lib() -> ctypes.CDLL:
             L.oq_fp8_quantize.argtypes = [_f32p, ctypes.c_int64, ctypes.c_float, _u8p]
             L.oq_fp8_dequantize.restype = None
             L.oq_fp8_dequantize.argtypes = [_u8p, ctypes.c_int64, ctypes.c_float, _f64p]
+            L.oq_fp16_value.restype = ctypes.c_double
+            L.oq_fp16_value.argtypes = [ctypes.c_uint16]
+            L.oq_fp16_encode.restype = ctypes.c_uint16
+            L.oq_fp16_encode.argtypes = [ctypes.c_float]
+            L.oq_fp16_encode_array.restype = None
+            L.oq_fp16_encode_array.argtypes = [_f32p, ctypes.c_int64, _u16p]
+            L.oq_int_quantize_group.restype = ctypes.c_int64
+            L.oq_int_quantize_group.argtypes = [_f32p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, _i8p, _u16p]
+            for name in ("oq_int_quantize_per_token", "oq_int_quantize_per_channel"):
+                getattr(L, name).restype = ctypes.c_int64
+                getattr(L, name).argtypes = [_f32p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                             ctypes.c_int, _i8p, _u16p]
             L.oq_attend.restype = None
             L.oq_attend.argtypes = [_f64p, _f64p, _f64p, ctypes.c_int, ctypes.c_int64,
                                     ctypes.c_int, ctypes.c_double, _f64p, _f64p, _f64p, _f64p]
@@ -170,6 +188,57 @@ def fp8_dequantize(c: np.ndarray, s: float) -> np.ndarray:
     out = np.empty(c.shape, np.float64)
     lib().oq_fp8_dequantize(_p(c, _u8p), c.size, ctypes.c_float(s), _p(out, _f64p))
     return out
+
+
+# ---------------------------------------------------------------- bit-width sweep
+def fp16_value(bits: int) -> float:
+    return lib().oq_fp16_value(int(bits) & 0xFFFF)
+
+
+def fp16_encode(x) -> np.ndarray:
+    """binary16 bit patterns, RNE, saturating at 65504 (NaN -> 0x7E00)."""
+    x = _f32(x).ravel()
+    out = np.empty(x.size, np.uint16)
+    lib().oq_fp16_encode_array(_p(x, _f32p), x.size, _p(out, _u16p))
+    return out
+
+
+def int_quantize_group(x, bits: int):
+    """One group: (codes int8 (n,), fp16 scale bits, non-finite count)."""
+    x = _f32(x).ravel()
+    codes = np.empty(x.size, np.int8)
+    sb = np.zeros(1, np.uint16)
+    bad = lib().oq_int_quantize_group(_p(x, _f32p), x.size, 1, int(bits), _p(codes, _i8p), _p(sb, _u16p))
+    return codes, int(sb[0]), int(bad)
+
+
+def int_quantize(x, bits: int, per: str):
+    """x: (batch, tokens, heads, d).  per == "token": one FP16 scale per
+    (b, t, head); per == "channel": one per (b, head, channel) over the
+    tokens.  Returns (codes int8 like x, scale bits uint16, non-finite
+    count)."""
+    x = _f32(x)
+    B, T, H, d = x.shape
+    codes = np.empty(x.shape, np.int8)
+    if per == "token":
+        scales = np.empty((B, T, H), np.uint16)
+        fn = lib().oq_int_quantize_per_token
+    elif per == "channel":
+        scales = np.empty((B, H, d), np.uint16)
+        fn = lib().oq_int_quantize_per_channel
+    else:
+        raise ValueError(per)
+    bad = fn(_p(x, _f32p), B, T, H, d, int(bits), _p(codes, _i8p), _p(scales, _u16p))
+    return codes, scales, int(bad)
+
+
+def int_dequantize(codes: np.ndarray, scales: np.ndarray, per: str) -> np.ndarray:
+    """Values code * s (exact), fp64, shaped like codes."""
+    s = np.vectorize(fp16_value, otypes=[np.float64])(scales)
+    if per == "token":
+        return codes.astype(np.float64) * s[..., None]
+    B, T, H, d = codes.shape
+    return codes.astype(np.float64) * s[:, None, :, :]
 
 
 # ---------------------------------------------------------------- attention

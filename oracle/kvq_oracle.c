@@ -315,6 +315,136 @@ void oq_fp8_dequantize(const uint8_t *c, int64_t n, float s, double *out)
 }
 
 /* ------------------------------------------------------------------ */
+/* Bit-width sweep: symmetric INT-b with an FP16 scale per group        */
+/* ("Quantising the KV cache": table rows INT8 / INT4 / INT2 per token  */
+/* and "K per channel, V per token"; section "Per token or per          */
+/* channel?"; section "Maths": b + s/g bits with a 16-bit scale).       */
+/* ------------------------------------------------------------------ */
+
+/* Value of an IEEE binary16 bit pattern. */
+double oq_fp16_value(uint16_t h)
+{
+    int s = (h >> 15) & 1;
+    int e = (h >> 10) & 31;
+    int m = h & 1023;
+    double mag;
+    if (e == 31)
+        return m ? NAN : (s ? -INFINITY : INFINITY);
+    if (e == 0)
+        mag = ldexp((double)m, -24); /* m/1024 * 2^-14 */
+    else
+        mag = ldexp(1.0 + m / 1024.0, e - 15);
+    return s ? -mag : mag;
+}
+
+/* binary16 of x, round to nearest even, saturating: magnitudes that would
+ * round above the largest finite value (65504) give 65504; NaN gives 0x7E00. */
+uint16_t oq_fp16_encode(float x)
+{
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    double m = fabs((double)x);
+    int e, k;
+    if (isnan(x))
+        return 0x7E00u;
+    if (m == 0.0)
+        return sign;
+    if (m < ldexp(1.0, -14)) { /* subnormal range: multiples of 2^-24 */
+        k = rne_int(ldexp(m, 24));
+        return (uint16_t)(sign | (uint16_t)k); /* k == 1024 is the smallest normal */
+    }
+    e = (int)floor(log2(m));
+    if (ldexp(1.0, e) > m) /* guard log2 rounding */
+        e--;
+    if (ldexp(1.0, e + 1) <= m)
+        e++;
+    if (e > 15)
+        return (uint16_t)(sign | 0x7BFFu);
+    k = rne_int(ldexp(m, 10 - e)); /* 1024 .. 2048 */
+    if (k == 2048) {
+        k = 1024;
+        e++;
+    }
+    if (e > 15)
+        return (uint16_t)(sign | 0x7BFFu);
+    return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)(k - 1024));
+}
+
+/* One group of n values at stride `stride`: amax over the group (exact),
+ * s = fp16_RNE(amax / qmax) with qmax = 2^(bits-1) - 1 and an fp32 division,
+ * a zero scale replaced by the smallest fp16 subnormal 2^-24; then each code
+ * q = clamp(RNE(x / s), -qmax, qmax) with an fp32 division (NaN -> 0).
+ * Writes the codes (one int8 each, at the same stride) and the scale's bit
+ * pattern; returns the number of non-finite inputs. */
+int64_t oq_int_quantize_group(const float *x, int64_t n, int64_t stride, int bits, int8_t *codes,
+                              uint16_t *scale_bits)
+{
+    const int qmax = (1 << (bits - 1)) - 1;
+    float amax = 0.0f;
+    int64_t bad = 0;
+    uint16_t sb;
+    float s;
+    for (int64_t i = 0; i < n; i++) {
+        float a = fabsf(x[i * stride]);
+        if (!isfinite(x[i * stride]))
+            bad++;
+        if (a > amax)
+            amax = a;
+    }
+    sb = oq_fp16_encode(amax / (float)qmax);
+    if ((sb & 0x7FFFu) == 0)
+        sb = 0x0001u;
+    s = (float)oq_fp16_value(sb);
+    for (int64_t i = 0; i < n; i++) {
+        float y = x[i * stride] / s;
+        int q;
+        if (isnan(y))
+            q = 0;
+        else if (y >= (float)qmax)
+            q = qmax;
+        else if (y <= -(float)qmax)
+            q = -qmax;
+        else
+            q = (y < 0.0f) ? -rne_int(-(double)y) : rne_int((double)y);
+        codes[i * stride] = (int8_t)q;
+    }
+    *scale_bits = sb;
+    return bad;
+}
+
+void oq_fp16_encode_array(const float *x, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = oq_fp16_encode(x[i]);
+}
+
+/* x: [batch][tokens][heads][d].  Per token: one group per (b, t, head), its d
+ * channels; scales [batch][tokens][heads]. */
+int64_t oq_int_quantize_per_token(const float *x, int64_t batch, int64_t tokens, int64_t heads, int64_t d,
+                                  int bits, int8_t *codes, uint16_t *scales)
+{
+    int64_t bad = 0;
+    for (int64_t gidx = 0; gidx < batch * tokens * heads; gidx++)
+        bad += oq_int_quantize_group(x + gidx * d, d, 1, bits, codes + gidx * d, scales + gidx);
+    return bad;
+}
+
+/* Per channel: one group per (b, head, channel), over the sequence's tokens;
+ * scales [batch][heads][d]. */
+int64_t oq_int_quantize_per_channel(const float *x, int64_t batch, int64_t tokens, int64_t heads, int64_t d,
+                                    int bits, int8_t *codes, uint16_t *scales)
+{
+    int64_t bad = 0;
+    for (int64_t b = 0; b < batch; b++)
+        for (int64_t h = 0; h < heads; h++)
+            for (int64_t c = 0; c < d; c++) {
+                const int64_t off = (b * tokens * heads + h) * d + c;
+                bad += oq_int_quantize_group(x + off, tokens, heads * d, bits, codes + off,
+                                             scales + (b * heads + h) * d + c);
+            }
+    return bad;
+}
+
+/* ------------------------------------------------------------------ */
 /* Attention, fp64 ("an otherwise unchanged copy of the attention")    */
 /* ------------------------------------------------------------------ */
 
