@@ -346,6 +346,8 @@ uint16_t oq_fp16_encode(float x)
     int e, k;
     if (isnan(x))
         return 0x7E00u;
+    if (isinf(x)) /* saturating: above the largest finite value */
+        return (uint16_t)(sign | 0x7BFFu);
     if (m == 0.0)
         return sign;
     if (m < ldexp(1.0, -14)) { /* subnormal range: multiples of 2^-24 */

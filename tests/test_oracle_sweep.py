@@ -52,6 +52,11 @@ def test_fp16_encode_ties_and_specials():
                  np.float32)
     assert [int(v) for v in oracle.fp16_encode(x)] == [0x0000, 0x0002, 0x3C00, 0x3C02, 0x7BFF, 0x7BFF, 0x8000]
     assert int(oracle.fp16_encode(np.array([np.nan], np.float32))[0]) == 0x7E00
+    # infinities saturate like every other magnitude above 65504
+    assert [int(v) for v in oracle.fp16_encode(np.array([np.inf, -np.inf, 3.0e38], np.float32))] == \
+        [0x7BFF, 0xFBFF, 0x7BFF]
+    codes, sb, bad = oracle.int_quantize_group(np.array([np.inf, 1.0, -2.0], np.float32), 4)
+    assert sb == 0x7BFF and bad == 1 and codes.tolist() == [7, 0, 0]
 
 
 def _brute_codes(x: np.ndarray, s: float, qmax: int) -> np.ndarray:
