@@ -27,6 +27,10 @@ FLAG_NONFINITE = 0x1
 FLAG_PAGE_OOB = 0x2
 FLAG_TIMEOUT = 0x4
 FLAG_BAD_LENGTH = 0x8
+LAYOUT_FP8_TENSOR = 1
+LAYOUT_INT_PER_TOKEN = 2
+LAYOUT_INT_PER_CHANNEL = 3
+LAYOUT_FP4_G16 = 4
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -84,6 +88,10 @@ def load() -> ctypes.CDLL:
             L.kvq_status_string.argtypes = [ctypes.c_int]
             L.kvq_version.restype = ctypes.c_int32
             L.kvq_version.argtypes = []
+            L.kvq_fake_quant.restype = ctypes.c_int
+            L.kvq_fake_quant.argtypes = [ctypes.c_int32] * 6 + [_P] * 6
+            L.kvq_attn_dense.restype = ctypes.c_int
+            L.kvq_attn_dense.argtypes = [ctypes.c_int32] * 5 + [_P, _P, _P, ctypes.c_float, _P, _P, _P]
             L.kvq_fp4_pool_bytes.restype = ctypes.c_size_t
             L.kvq_fp4_pool_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
             _lib = L
@@ -248,3 +256,46 @@ def dequant(cache, seq_lens: Optional[torch.Tensor], max_len: int, dtype: torch.
                             _stream(stream))
     _check(st, "kvq_dequant")
     return k, v
+
+
+# ---------------------------------------------------------------- bit-width sweep
+def fake_quant(x: torch.Tensor, layout: int, bits: int, want_codes: bool = False,
+               err: Optional[torch.Tensor] = None, stream=None):
+    """kvq_fake_quant: x bf16 [batch][tokens][heads][head_dim] -> (x_hat float
+    like x, codes int8 like x or None, scales or None).  Scales: FP8 tensor ->
+    float[2] (s in [1]); INT per token -> uint16-as-int16 [batch][tokens][heads];
+    INT per channel -> [batch][heads][head_dim]; FP4 -> uint8 [numel/16]."""
+    _need(x, torch.bfloat16, "x")
+    B, T, H, d = x.shape
+    xh = torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    codes = torch.empty(x.shape, dtype=torch.int8, device=x.device) if want_codes else None
+    if layout == LAYOUT_FP8_TENSOR:
+        scales = torch.empty(2, dtype=torch.float32, device=x.device)
+    elif layout == LAYOUT_INT_PER_TOKEN:
+        scales = torch.empty((B, T, H), dtype=torch.int16, device=x.device)
+    elif layout == LAYOUT_INT_PER_CHANNEL:
+        scales = torch.empty((B, H, d), dtype=torch.int16, device=x.device)
+    else:
+        scales = torch.empty(x.numel() // 16, dtype=torch.uint8, device=x.device)
+    st = load().kvq_fake_quant(layout, bits, B, T, H, d, _ptr(x), _ptr(xh), _ptr(codes), _ptr(scales), _ptr(err),
+                               _stream(stream))
+    _check(st, "kvq_fake_quant")
+    return xh, codes, scales
+
+
+def attn_dense(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, softmax_scale: Optional[float] = None,
+               want_top: bool = False, stream=None):
+    """kvq_attn_dense: q bf16 [batch][Hq][d], k, v float [batch][T][Hkv][d] ->
+    (out float [batch][Hq][d], top int32 [batch][Hq] or None)."""
+    _need(q, torch.bfloat16, "q")
+    _need(k, torch.float32, "k")
+    _need(v, torch.float32, "v")
+    B, Hq, d = q.shape
+    T, Hkv = k.shape[1], k.shape[2]
+    out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    top = torch.empty((B, Hq), dtype=torch.int32, device=q.device) if want_top else None
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else softmax_scale
+    st = load().kvq_attn_dense(B, T, Hq, Hkv, d, _ptr(q), _ptr(k), _ptr(v), float(scale), _ptr(out), _ptr(top),
+                               _stream(stream))
+    _check(st, "kvq_attn_dense")
+    return out, top

@@ -238,6 +238,70 @@ kvq_status kvq_dequant(const kvq_cache *cache, int32_t batch, const int32_t *d_s
                        int32_t max_len, int32_t out_dtype, void *k_out, void *v_out,
                        int32_t *d_err_flag, kvq_stream stream);
 
+/* ------------------------------------------------------------------ bit-width sweep
+ * Layouts of the formats compared in the results table of "Quantising the KV
+ * cache" (section "Concept"; storage b + s/g bits per number, section
+ * "Maths"), for measuring what each does to attention -- not cache formats.
+ * Readings (the pages give the INT formats' storage, not their rounding):
+ *   FP8_TENSOR       E4M3, one scale per tensor: s = amax/448 in fp32 over the
+ *                    whole tensor (1 if amax == 0), code RNE_e4m3(x/s)
+ *                    saturating, x^ = E4M3(code) * s in fp32.
+ *   INT_PER_TOKEN    symmetric INT-b, one FP16 scale per (sequence, token,
+ *                    head) group of head_dim channels;
+ *   INT_PER_CHANNEL  ... one FP16 scale per (sequence, head, channel) group
+ *                    over the tokens (section "Per token or per channel?").
+ *                    Both: s = FP16_RNE(amax/qmax), qmax = 2^(bits-1)-1, fp32
+ *                    division, saturating at 65504, 0 -> 2^-24; code
+ *                    clamp(RNE(x/s), -qmax, qmax) (fp32 division, NaN -> 0);
+ *                    x^ = code * s.
+ *   FP4_G16          the cache's E2M1 + E4M3-per-16 block quantiser. */
+enum {
+  KVQ_LAYOUT_FP8_TENSOR = 1,
+  KVQ_LAYOUT_INT_PER_TOKEN = 2,
+  KVQ_LAYOUT_INT_PER_CHANNEL = 3,
+  KVQ_LAYOUT_FP4_G16 = 4
+};
+
+/*
+ * kvq_fake_quant -- quantise x in one sweep layout and write the dequantised
+ * values ("Quantising the KV cache", section "Code": the quantised K and V
+ * replace the real ones ahead of the attention).
+ *   layout, bits  FP8_TENSOR: 8; INT_*: 2..8; FP4_G16: 4.
+ *   x       device bf16 [batch][tokens][heads][head_dim], head_dim % 16 == 0,
+ *           16-byte aligned.
+ *   x_hat   device float, same shape (required).
+ *   codes   device int8, same shape, or NULL: INT codes; E4M3 bytes (FP8);
+ *           E2M1 nibbles 0..15 (FP4).
+ *   scales  FP8_TENSOR: device float[2], required (scales[0] is scratch,
+ *           scales[1] receives s); INT_PER_TOKEN: uint16 FP16 bit patterns
+ *           [batch][tokens][heads] or NULL; INT_PER_CHANNEL: uint16
+ *           [batch][heads][head_dim] or NULL; FP4_G16: uint8 E4M3 bytes, one
+ *           per 16 values in order, or NULL.
+ * Host errors: INVALID_ARGUMENT (sizes, layout/bits, pointers).  Device flag:
+ * NONFINITE.  No counterpart on the pages for the entry point itself.
+ */
+kvq_status kvq_fake_quant(int32_t layout, int32_t bits, int32_t batch, int32_t tokens, int32_t heads,
+                          int32_t head_dim, const void *x, float *x_hat, int8_t *codes, void *scales,
+                          int32_t *d_err_flag, kvq_stream stream);
+
+/*
+ * kvq_attn_dense -- decode attention over dense float K and V with every
+ * product, the softmax and the sums in fp64 (the measuring stick of the
+ * sweep: "Quantising the KV cache", section "Code", the attention the
+ * quantised K and V feed is unchanged).
+ *   out[b][h] = sum_t softmax_t(softmax_scale * q[b][h] . k[b][t][h/G]) v[b][t][h/G]
+ *   q    device bf16 [batch][num_q_heads][head_dim].
+ *   k, v device float [batch][tokens][num_kv_heads][head_dim].
+ *   out  device float [batch][num_q_heads][head_dim].
+ *   top  device int32 [batch][num_q_heads] or NULL: the position with the
+ *        largest score (the lowest on a tie; -1 when tokens == 0).
+ * Host errors: INVALID_ARGUMENT; UNSUPPORTED for tokens > 16384 or head_dim
+ * > 512.
+ */
+kvq_status kvq_attn_dense(int32_t batch, int32_t tokens, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_dim, const void *q, const float *k, const float *v,
+                          float softmax_scale, float *out, int32_t *top, kvq_stream stream);
+
 /* Bytes of an FP4 page pool: num_pages * num_kv_heads * page_size *
  * 9 * head_dim / 8 (0 for invalid sizes). */
 size_t kvq_fp4_pool_bytes(int64_t num_pages, int32_t num_kv_heads, int32_t page_size, int32_t head_dim);

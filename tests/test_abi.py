@@ -30,8 +30,9 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
-        "kvq_append", "kvq_decode_attn", "kvq_decode_attn_noalloc", "kvq_decode_workspace_bytes", "kvq_dequant",
-        "kvq_fp4_pool_bytes", "kvq_fp8_set_scales", "kvq_status_string", "kvq_version"])
+        "kvq_append", "kvq_attn_dense", "kvq_decode_attn", "kvq_decode_attn_noalloc", "kvq_decode_workspace_bytes",
+        "kvq_dequant", "kvq_fake_quant", "kvq_fp4_pool_bytes", "kvq_fp8_set_scales", "kvq_status_string",
+        "kvq_version"])
 
 
 def test_library_exports_every_declared_function(lib):
@@ -65,6 +66,18 @@ int main(void) {
     want = [ctypes.sizeof(S), S.num_pages.offset, S.max_pages_per_seq.offset, S.page_table.offset,
             S.data.offset, S.k_scale.offset, S.v_scale.offset]
     assert got == want
+
+
+def test_sweep_entry_points_refuse_bad_arguments_on_the_host(lib):
+    # layout / bits / head_dim are checked before anything is enqueued
+    assert lib.kvq_fake_quant(9, 4, 1, 2, 1, 64, 16, 32, None, None, None, None) == 1
+    assert lib.kvq_fake_quant(2, 1, 1, 2, 1, 64, 16, 32, None, None, None, None) == 1
+    assert lib.kvq_fake_quant(2, 4, 1, 2, 1, 24, 16, 32, None, None, None, None) == 1
+    assert lib.kvq_fake_quant(1, 8, 1, 2, 1, 64, 16, 32, None, None, None, None) == 1  # FP8 needs its scale pair
+    assert lib.kvq_fake_quant(2, 4, 0, 2, 1, 64, None, None, None, None, None, None) == 0  # empty: no-op
+    assert lib.kvq_attn_dense(1, 16385, 2, 1, 64, 16, 32, 64, 0.1, 128, None, None) == 2
+    assert lib.kvq_attn_dense(1, 8, 3, 2, 64, 16, 32, 64, 0.1, 128, None, None) == 1
+    assert lib.kvq_attn_dense(1, 8, 2, 1, 64, 16, 32, 64, -1.0, 128, None, None) == 1
 
 
 def test_fp4_pool_bytes(lib):
