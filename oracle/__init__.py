@@ -17,6 +17,10 @@ tests compare against:
   * ``attend`` -- fp64 softmax attention over dequantised K/V ("Quantising the
     KV cache", section "Code": the quantised K and V replace the real ones
     ahead of an unchanged attention).
+  * ``nvfp4_global_scale`` / ``nvfp4_quantize_rows`` /
+    ``nvfp4_dequantize_rows`` -- NVFP4: the FP4 block quantiser over x / S
+    with one fp32 second-level scale S ("KV Cache Quantisation": FP8 or
+    NVFP4 with the scales handled at read time).
   * ``fp16_encode`` / ``int_quantize`` / ``int_dequantize`` -- the
     symmetric INT-b quantisers with one FP16 scale per token or per channel
     of the bit-width sweep ("Quantising the KV cache", table and section
@@ -92,6 +96,12 @@ def lib() -> ctypes.CDLL:
             L.oq_fp8_quantize.argtypes = [_f32p, ctypes.c_int64, ctypes.c_float, _u8p]
             L.oq_fp8_dequantize.restype = None
             L.oq_fp8_dequantize.argtypes = [_u8p, ctypes.c_int64, ctypes.c_float, _f64p]
+            L.oq_nvfp4_global_scale.restype = ctypes.c_float
+            L.oq_nvfp4_global_scale.argtypes = [_f32p, ctypes.c_int64]
+            L.oq_nvfp4_quantize_rows.restype = ctypes.c_int64
+            L.oq_nvfp4_quantize_rows.argtypes = [_f32p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, _u8p, _u8p]
+            L.oq_nvfp4_dequantize_rows.restype = None
+            L.oq_nvfp4_dequantize_rows.argtypes = [_u8p, _u8p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, _f64p]
             L.oq_fp16_value.restype = ctypes.c_double
             L.oq_fp16_value.argtypes = [ctypes.c_uint16]
             L.oq_fp16_encode.restype = ctypes.c_uint16
@@ -190,6 +200,36 @@ def fp8_dequantize(c: np.ndarray, s: float) -> np.ndarray:
     return out
 
 
+# ---------------------------------------------------------------- NVFP4
+def nvfp4_global_scale(x) -> float:
+    """S = amax / (6 * 448) in fp32 over every value (1 when amax == 0)."""
+    x = _f32(x).ravel()
+    return float(lib().oq_nvfp4_global_scale(_p(x, _f32p), x.size))
+
+
+def nvfp4_quantize_rows(x, S: float):
+    """The FP4 block quantiser over x / S (fp32 division): (codes, scales,
+    non-finite block count), shaped like quantize_rows."""
+    x = _f32(x)
+    d = x.shape[-1]
+    n = x.size // d
+    codes = np.empty(x.shape[:-1] + (d // 2,), np.uint8)
+    scales = np.empty(x.shape[:-1] + (d // 16,), np.uint8)
+    bad = lib().oq_nvfp4_quantize_rows(_p(x, _f32p), n, d, ctypes.c_float(S), _p(codes, _u8p), _p(scales, _u8p))
+    return codes, scales, int(bad)
+
+
+def nvfp4_dequantize_rows(codes: np.ndarray, scales: np.ndarray, S: float) -> np.ndarray:
+    """fp32(fp32(e2m1 * e4m3) * S), widened to fp64."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    d = codes.shape[-1] * 2
+    n = codes.size // (d // 2)
+    out = np.empty(codes.shape[:-1] + (d,), np.float64)
+    lib().oq_nvfp4_dequantize_rows(_p(codes, _u8p), _p(scales, _u8p), n, d, ctypes.c_float(S), _p(out, _f64p))
+    return out
+
+
 # ---------------------------------------------------------------- bit-width sweep
 def fp16_value(bits: int) -> float:
     return lib().oq_fp16_value(int(bits) & 0xFFFF)
@@ -260,14 +300,16 @@ def attend(q, k, v, scale: float):
     return out, m, l
 
 
-def decode_unit(q, k, v, scale: float, window: int = 0, swa_scales=None):
+def decode_unit(q, k, v, scale: float, window: int = 0, swa_scales=None, nvfp4_scales=None):
     """One (sequence, kv head) decode step over T cached positions.
 
     q: (G, d) query rows of the group; k, v: (T, d) the unquantised cached
     keys/values in position order.  With window == 0 every position is read
     from the FP4 cache.  With window W > 0 the last W' = min(W, T) positions
     are read from the FP8 cache with per-head scales swa_scales = (s_k, s_v)
-    and the rest from the FP4 cache.  Returns (out (G, d) fp64, vmax) where
+    and the rest from the FP4 cache.  nvfp4_scales = (S_k, S_v) reads the
+    global positions as NVFP4 (second-level scales) instead of plain FP4.
+    Returns (out (G, d) fp64, vmax) where
     vmax = max |V^| over the attended dequantised values.
     """
     k = _f32(k)
@@ -275,10 +317,17 @@ def decode_unit(q, k, v, scale: float, window: int = 0, swa_scales=None):
     T, d = k.shape
     w = min(window, T) if window > 0 else 0
     n4 = T - w
-    kc, ks, _ = quantize_rows(k[:n4])
-    vc, vs, _ = quantize_rows(v[:n4])
-    kh = dequantize_rows(kc, ks)
-    vh = dequantize_rows(vc, vs)
+    if nvfp4_scales is None:
+        kc, ks, _ = quantize_rows(k[:n4])
+        vc, vs, _ = quantize_rows(v[:n4])
+        kh = dequantize_rows(kc, ks)
+        vh = dequantize_rows(vc, vs)
+    else:
+        Sk, Sv = nvfp4_scales
+        kc, ks, _ = nvfp4_quantize_rows(k[:n4], Sk)
+        vc, vs, _ = nvfp4_quantize_rows(v[:n4], Sv)
+        kh = nvfp4_dequantize_rows(kc, ks, Sk)
+        vh = nvfp4_dequantize_rows(vc, vs, Sv)
     if w > 0:
         sk, sv = swa_scales
         k8, _ = fp8_quantize(k[n4:], sk)

@@ -315,6 +315,52 @@ void oq_fp8_dequantize(const uint8_t *c, int64_t n, float s, double *out)
 }
 
 /* ------------------------------------------------------------------ */
+/* NVFP4: the FP4 block quantiser applied to x / S, with one fp32        */
+/* second-level scale S ("KV Cache Quantisation": store the cache in FP8  */
+/* or NVFP4 and handle the scales at read time).  Reading: S = amax /     */
+/* (6 * 448) over a calibration tensor (1 when amax == 0), so the largest */
+/* block lands on the top E4M3 scale; x / S is an fp32 division; a value  */
+/* reads back as fp32(fp32(e2m1 * e4m3) * S).                             */
+/* ------------------------------------------------------------------ */
+
+float oq_nvfp4_global_scale(const float *x, int64_t n)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; i++) {
+        float a = fabsf(x[i]);
+        if (a > amax || isnan(a))
+            amax = a;
+    }
+    if (amax == 0.0f)
+        return 1.0f;
+    return amax / 2688.0f; /* 6 * 448 */
+}
+
+int64_t oq_nvfp4_quantize_rows(const float *x, int64_t n, int d, float S, uint8_t *codes, uint8_t *scales)
+{
+    int64_t bad = 0;
+    float tmp[16];
+    for (int64_t r = 0; r < n; r++)
+        for (int b = 0; b < d / 16; b++) {
+            for (int i = 0; i < 16; i++)
+                tmp[i] = x[r * d + 16 * b + i] / S;
+            bad += oq_quantize_block(tmp, codes + r * (d / 2) + 8 * b, scales + r * (d / 16) + b);
+        }
+    return bad;
+}
+
+void oq_nvfp4_dequantize_rows(const uint8_t *codes, const uint8_t *scales, int64_t n, int d, float S, double *out)
+{
+    for (int64_t r = 0; r < n; r++)
+        for (int c = 0; c < d; c++) {
+            uint8_t byte = codes[r * (d / 2) + c / 2];
+            uint8_t nib = (c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+            float v = (float)(oq_e2m1_value(nib) * oq_e4m3_value(scales[r * (d / 16) + c / 16]));
+            out[r * d + c] = (double)(v * S);
+        }
+}
+
+/* ------------------------------------------------------------------ */
 /* Bit-width sweep: symmetric INT-b with an FP16 scale per group        */
 /* ("Quantising the KV cache": table rows INT8 / INT4 / INT2 per token  */
 /* and "K per channel, V per token"; section "Per token or per          */
