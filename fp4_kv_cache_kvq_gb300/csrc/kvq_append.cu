@@ -141,13 +141,21 @@ __device__ __forceinline__ uint64_t spread_nibbles(uint32_t w) {
   return x;
 }
 
-// A block holding Inf or NaN (rare): reload it and run the plain
-// IEEE-division quantiser.  Returns the 8 code bytes and the scale byte.
-__device__ __noinline__ uint3 quantize_nonfinite(const uint16_t* src) {
-  const Block16 blk = load_bf16x16(src);
+// The plain IEEE-division quantiser on x / S (S = 1: the block itself, an
+// exact division), for blocks holding Inf or NaN and for NVFP4 caches.
+// Returns the 8 code bytes, the scale byte and whether a value was not finite.
+__device__ __noinline__ uint4 quantize_plain(const uint16_t* src, float S) {
+  Block16 blk = load_bf16x16(src);
+  bool ok = blk.finite;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    blk.x[i] = __fdiv_rn(blk.x[i], S);
+    ok &= isfinite(blk.x[i]);
+  }
+  blk.finite = ok;
   uint32_t sb;
   const uint2 q = quantize_block(blk, sb);
-  return make_uint3(q.x, q.y, sb);
+  return make_uint4(q.x, q.y, sb, ok ? 0u : 1u);
 }
 
 // n / d for n < 2^31 without a hardware divide: (umulhi(n, mul) + n) >> shift
@@ -178,7 +186,8 @@ constexpr int kAppendMinCtas = 4;
 // take consecutive spans of the input; the row, page and address arithmetic
 // is done once per item, not once per block.  Indices are 32-bit;
 // the host splits the batch so that every launch's item count fits.
-template <int D>
+// NV: an NVFP4 cache (codes of x / S_h, the IEEE path for every block).
+template <int D, bool NV>
 __global__ void __launch_bounds__(256, kAppendMinCtas) append_fp4_kernel(const kvq_cache c, int32_t b_begin, uint32_t k_items,
                                                          uint32_t v_items, uint32_t k_ctas, DivU32 div_hkv,
                                                          DivU32 div_k_per, DivU32 div_v_per, int32_t n_new,
@@ -231,28 +240,40 @@ __global__ void __launch_bounds__(256, kAppendMinCtas) append_fp4_kernel(const k
   const int64_t row = (int64_t)b * n_new;  // first input row of sequence b
   if (is_k) {
     const uint16_t* src = k + ((row + t) * hkv + h) * D + 16 * j0;
-    Raw16 kb[BK];
-#pragma unroll
-    for (int jb = 0; jb < BK; ++jb) load_raw16(src + 16 * jb, kb[jb]);
     uint32_t codes[2 * BK];
     uint32_t scales = 0;
+    if constexpr (NV) {
+      const float S = __ldg(static_cast<const float*>(c.k_scale) + h);
 #pragma unroll
-    for (int jb = 0; jb < BK; ++jb) {
-      uint32_t sb;
-      uint2 q;
-      if (kb[jb].finite) {
-        sb = block_scale_byte(kb[jb].amax);
-        const float s = e4m3_to_f32(sb);
-        q = k_codes_finite(kb[jb].w, s, __frcp_rn(s));
-      } else {
-        set_flag(flag, KVQ_FLAG_NONFINITE);
-        const uint3 r3 = quantize_nonfinite(src + 16 * jb);
-        q = make_uint2(r3.x, r3.y);
-        sb = r3.z;
+      for (int jb = 0; jb < BK; ++jb) {
+        const uint4 r4 = quantize_plain(src + 16 * jb, S);
+        if (r4.w) set_flag(flag, KVQ_FLAG_NONFINITE);
+        codes[2 * jb] = r4.x;
+        codes[2 * jb + 1] = r4.y;
+        scales |= r4.z << (8 * jb);
       }
-      codes[2 * jb] = q.x;
-      codes[2 * jb + 1] = q.y;
-      scales |= sb << (8 * jb);
+    } else {
+      Raw16 kb[BK];
+#pragma unroll
+      for (int jb = 0; jb < BK; ++jb) load_raw16(src + 16 * jb, kb[jb]);
+#pragma unroll
+      for (int jb = 0; jb < BK; ++jb) {
+        uint32_t sb;
+        uint2 q;
+        if (kb[jb].finite) {
+          sb = block_scale_byte(kb[jb].amax);
+          const float s = e4m3_to_f32(sb);
+          q = k_codes_finite(kb[jb].w, s, __frcp_rn(s));
+        } else {
+          set_flag(flag, KVQ_FLAG_NONFINITE);
+          const uint4 r4 = quantize_plain(src + 16 * jb, 1.0f);
+          q = make_uint2(r4.x, r4.y);
+          sb = r4.z;
+        }
+        codes[2 * jb] = q.x;
+        codes[2 * jb + 1] = q.y;
+        scales |= sb << (8 * jb);
+      }
     }
     uint8_t* cdst = grp + ls * (D / 2) + 8 * j0;
     uint8_t* sdst = grp + G * (D / 2) + ls * NB + j0;
@@ -278,7 +299,7 @@ __global__ void __launch_bounds__(256, kAppendMinCtas) append_fp4_kernel(const k
     const uint16_t* src = v + ((row + (pos + hf - sp)) * hkv + h) * D + 16 * j0;
 #pragma unroll
     for (int jb = 0; jb < BV; ++jb) {
-      if (m) {
+      if (m && !NV) {
         load_raw16(src + 16 * jb, vb[hf][jb]);
       } else {
 #pragma unroll
@@ -299,18 +320,19 @@ __global__ void __launch_bounds__(256, kAppendMinCtas) append_fp4_kernel(const k
     uint4* dst = reinterpret_cast<uint4*>(grp + vblk);
     uint4 codes;
     uint32_t sb0 = 0, sb1 = 0;
-    if (vb[0][jb].finite && vb[1][jb].finite) {
+    if (!NV && vb[0][jb].finite && vb[1][jb].finite) {
       sb0 = block_scale_byte(vb[0][jb].amax);
       sb1 = block_scale_byte(vb[1][jb].amax);
       const float s0 = e4m3_to_f32(sb0), s1 = e4m3_to_f32(sb1);
       codes = v_pair_codes_finite(vb[0][jb].w, s0, __frcp_rn(s0), vb[1][jb].w, s1, __frcp_rn(s1));
     } else {
-      set_flag(flag, KVQ_FLAG_NONFINITE);
+      const float S = NV ? __ldg(static_cast<const float*>(c.v_scale) + h) : 1.0f;
       uint64_t lo = 0, hi = 0;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         if (!(hf ? mine1 : mine0)) continue;
-        const uint3 q = quantize_nonfinite(v + ((row + (pos + hf - sp)) * hkv + h) * D + 16 * j);
+        const uint4 q = quantize_plain(v + ((row + (pos + hf - sp)) * hkv + h) * D + 16 * j, S);
+        if (q.w) set_flag(flag, KVQ_FLAG_NONFINITE);
         lo |= spread_nibbles(q.x) << (4 * hf);
         hi |= spread_nibbles(q.y) << (4 * hf);
         (hf ? sb1 : sb0) = q.z;
@@ -384,10 +406,12 @@ __global__ void __launch_bounds__(256) append_fp8_kernel(const kvq_cache c, int3
 }
 
 // One CTA per (kv head, K/V): amax over every value of that head, then
-// s_h = amax / 448 (IEEE fp32), 1 if amax == 0.
+// s_h = amax / divisor (IEEE fp32; 448 for an FP8 cache, 6 * 448 for the
+// NVFP4 second level), 1 if amax == 0.
 __global__ void __launch_bounds__(256) fp8_scales_kernel(const kvq_cache c, int64_t rows,
                                                          const uint16_t* __restrict__ k,
-                                                         const uint16_t* __restrict__ v, int32_t* flag) {
+                                                         const uint16_t* __restrict__ v, float divisor,
+                                                         int32_t* flag) {
   const int h = blockIdx.x;
   const int side = blockIdx.y;
   const uint16_t* src = side ? v : k;
@@ -417,7 +441,7 @@ __global__ void __launch_bounds__(256) fp8_scales_kernel(const kvq_cache c, int6
     float a = 0.0f;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) a = fmaxf(a, red[w]);
     if (bad) set_flag(flag, KVQ_FLAG_NONFINITE);
-    const float s = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 448.0f);
+    const float s = (a == 0.0f) ? 1.0f : __fdiv_rn(a, divisor);
     static_cast<float*>(side ? c.v_scale : c.k_scale)[h] = s;
   }
 }
@@ -438,7 +462,8 @@ extern "C" kvq_status kvq_append(const kvq_cache* cache, int32_t batch, int32_t 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const uint16_t* k16 = static_cast<const uint16_t*>(k);
   const uint16_t* v16 = static_cast<const uint16_t*>(v);
-  if (cache->format == KVQ_FORMAT_FP4_E2M1_E4M3_G16) {
+  if (is_fp4_layout(cache)) {
+    const bool nv = cache->format == KVQ_FORMAT_NVFP4;
     // 32-bit item indices: one sequence's items must fit, the batch is split.
     const int64_t nqk = cache->head_dim / 16 / kAppendBlocksK;  // items per (token, head)
     const int64_t nqv = cache->head_dim / 16 / kAppendBlocksV;
@@ -457,15 +482,18 @@ extern "C" kvq_status kvq_append(const kvq_cache* cache, int32_t batch, int32_t 
       const DivU32 dv = DivU32::make((uint32_t)(n_new / 2 + 1));
       switch (cache->head_dim) {
         case 64:
-          append_fp4_kernel<64><<<grid, 256, 0, s>>>(*cache, (int32_t)b0, k_items, v_items, k_ctas, dh, dk, dv, n_new,
+          (nv ? append_fp4_kernel<64, true> : append_fp4_kernel<64, false>)<<<grid, 256, 0, s>>>(
+              *cache, (int32_t)b0, k_items, v_items, k_ctas, dh, dk, dv, n_new,
                                                      d_start_pos, k16, v16, d_err_flag);
           break;
         case 128:
-          append_fp4_kernel<128><<<grid, 256, 0, s>>>(*cache, (int32_t)b0, k_items, v_items, k_ctas, dh, dk, dv, n_new,
+          (nv ? append_fp4_kernel<128, true> : append_fp4_kernel<128, false>)<<<grid, 256, 0, s>>>(
+              *cache, (int32_t)b0, k_items, v_items, k_ctas, dh, dk, dv, n_new,
                                                       d_start_pos, k16, v16, d_err_flag);
           break;
         default:
-          append_fp4_kernel<256><<<grid, 256, 0, s>>>(*cache, (int32_t)b0, k_items, v_items, k_ctas, dh, dk, dv, n_new,
+          (nv ? append_fp4_kernel<256, true> : append_fp4_kernel<256, false>)<<<grid, 256, 0, s>>>(
+              *cache, (int32_t)b0, k_items, v_items, k_ctas, dh, dk, dv, n_new,
                                                       d_start_pos, k16, v16, d_err_flag);
           break;
       }
@@ -484,12 +512,14 @@ extern "C" kvq_status kvq_fp8_set_scales(const kvq_cache* cache, int32_t batch, 
   if (batch < 0 || n < 0) return KVQ_ERR_INVALID_ARGUMENT;
   const kvq_status st = check_cache(cache, batch);
   if (st != KVQ_OK) return st;
-  if (cache->format != KVQ_FORMAT_FP8_E4M3_HEAD) return KVQ_ERR_INVALID_ARGUMENT;
+  if (cache->format != KVQ_FORMAT_FP8_E4M3_HEAD && cache->format != KVQ_FORMAT_NVFP4) return KVQ_ERR_INVALID_ARGUMENT;
+  const float divisor = cache->format == KVQ_FORMAT_NVFP4 ? 2688.0f : 448.0f;  // 6 * 448 for NVFP4
   if ((int64_t)batch * n > 0 && (k == nullptr || v == nullptr)) return KVQ_ERR_INVALID_ARGUMENT;
   if (!aligned_to(k, 16) || !aligned_to(v, 16)) return KVQ_ERR_INVALID_ARGUMENT;
   dim3 grid(cache->num_kv_heads, 2);
   fp8_scales_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      *cache, (int64_t)batch * n, static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), d_err_flag);
+      *cache, (int64_t)batch * n, static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), divisor,
+      d_err_flag);
   return launch_status();
 }
 

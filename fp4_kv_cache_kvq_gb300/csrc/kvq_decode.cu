@@ -83,6 +83,8 @@ struct DecodeParams {
   float* part_ml;
   int2* unit_rec;
   int32_t* flag;
+  const float* k_gscale;  // NVFP4 second-level scales [Hkv] (nullptr: plain FP4)
+  const float* v_gscale;
   int64_t num_pages;
   int32_t batch, hkv, g, hq, page, max_pages, window;
   float qk_log2;  // softmax_scale * log2(e)
@@ -314,8 +316,10 @@ __device__ __forceinline__ void begin_unit(const DecodeParams& p, ConsumerState<
   for (int i = 0; i < D / 8; ++i) st.qf[i] = pack_f16x2(v[2 * i] * up, v[2 * i + 1] * up);
   const int k0 = __shfl_sync(0xFFFFFFFFu, k, (2 * tig) * 4);
   const int k1 = __shfl_sync(0xFFFFFFFFu, k, (2 * tig + 1) * 4);
-  st.cs[0] = p.qk_log2 * __uint_as_float((uint32_t)(127 - k0) << 23);
-  st.cs[1] = p.qk_log2 * __uint_as_float((uint32_t)(127 - k1) << 23);
+  // NVFP4: the keys' second-level scale multiplies every score of the head
+  const float sk = p.k_gscale ? __ldg(p.k_gscale + h) : 1.0f;
+  st.cs[0] = p.qk_log2 * sk * __uint_as_float((uint32_t)(127 - k0) << 23);
+  st.cs[1] = p.qk_log2 * sk * __uint_as_float((uint32_t)(127 - k1) << 23);
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt)
 #pragma unroll
@@ -519,7 +523,7 @@ __device__ __forceinline__ void consume_stage(ConsumerState<D>& st, uint32_t sta
 
 // Combine the four warps' states for one unit and write the CTA's partial.
 template <int D>
-__device__ void flush_unit(const DecodeParams& p, ConsumerState<D>& st, Smem<D>& sm, int64_t slot) {
+__device__ void flush_unit(const DecodeParams& p, ConsumerState<D>& st, Smem<D>& sm, int64_t slot, float vscale) {
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, tig = lane & 3;
@@ -560,7 +564,7 @@ __device__ void flush_unit(const DecodeParams& p, ConsumerState<D>& st, Smem<D>&
         l += f * sm.flush_l[w * kNG + r];
       }
     }
-    p.part_o[(slot * p.g + r) * D + ch] = o;
+    p.part_o[(slot * p.g + r) * D + ch] = o * vscale;  // NVFP4: the values' second-level scale
     if (ch == 0) {
       p.part_ml[(slot * p.g + r) * 2 + 0] = mx;
       p.part_ml[(slot * p.g + r) * 2 + 1] = l;
@@ -602,11 +606,13 @@ __global__ void __launch_bounds__(kThreads, 3)
   ConsumerState<D> st;
   bool have = false, dead = false;
   int64_t slot = 0;
+  float vscale = 1.0f;
   uint32_t it = 0;
   for (; wk.v < v1; advance(p, wk), ++it) {
     if (!have || wk.c == 0) {
-      if (have) flush_unit<D>(p, st, sm, slot);
+      if (have) flush_unit<D>(p, st, sm, slot, vscale);
       const int64_t u = (int64_t)wk.b * p.hkv + wk.h;
+      vscale = p.v_gscale ? __ldg(p.v_gscale + wk.h) : 1.0f;
       slot = u + blockIdx.x;
       begin_unit<D>(p, st, wk.b, wk.h);
       have = true;
@@ -634,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       mbar_arrive(smem_addr(&sm.empty[s]));
     }
   }
-  if (have) flush_unit<D>(p, st, sm, slot);
+  if (have) flush_unit<D>(p, st, sm, slot, vscale);
 }
 
 // ------------------------------------------------------------------ merge (+ FP8 window)
@@ -937,7 +943,7 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* global, const kvq_cache* 
   if (batch < 1) return KVQ_ERR_INVALID_ARGUMENT;
   kvq_status st = check_cache(global, batch);
   if (st != KVQ_OK) return st;
-  if (global->format != KVQ_FORMAT_FP4_E2M1_E4M3_G16) return KVQ_ERR_INVALID_ARGUMENT;
+  if (!is_fp4_layout(global)) return KVQ_ERR_INVALID_ARGUMENT;
   const int hkv = global->num_kv_heads, D = global->head_dim;
   if (num_q_heads < hkv || num_q_heads % hkv != 0) return KVQ_ERR_INVALID_ARGUMENT;
   const int g = num_q_heads / hkv;
@@ -970,6 +976,9 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* global, const kvq_cache* 
   dp.part_ml = reinterpret_cast<float*>(ws + L.ml_off);
   dp.unit_rec = reinterpret_cast<int2*>(ws + L.rec_off);
   dp.flag = d_err_flag;
+  const bool nv = global->format == KVQ_FORMAT_NVFP4;
+  dp.k_gscale = nv ? static_cast<const float*>(global->k_scale) : nullptr;
+  dp.v_gscale = nv ? static_cast<const float*>(global->v_scale) : nullptr;
   dp.num_pages = global->num_pages;
   dp.batch = batch;
   dp.hkv = hkv;

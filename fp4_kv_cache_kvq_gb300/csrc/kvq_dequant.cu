@@ -98,6 +98,15 @@ __global__ void __launch_bounds__(256) dequant_fp4_kernel(const kvq_cache c, int
         vx[2 * q] = f.x * sv;
         vx[2 * q + 1] = f.y * sv;
       }
+      if (c.format == KVQ_FORMAT_NVFP4) {  // second-level scales: fp32(value * S)
+        const float Sk = __ldg(static_cast<const float*>(c.k_scale) + h);
+        const float Sv = __ldg(static_cast<const float*>(c.v_scale) + h);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          kx[q] *= Sk;
+          vx[q] *= Sv;
+        }
+      }
     }
     store16(k_out, i * 16, kx, out_dtype);
     store16(v_out, i * 16, vx, out_dtype);
@@ -153,7 +162,7 @@ extern "C" kvq_status kvq_dequant(const kvq_cache* cache, int32_t batch, const i
     return KVQ_ERR_INVALID_ARGUMENT;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int64_t work = (int64_t)batch * max_len * cache->num_kv_heads * (cache->head_dim / 16);
-  if (cache->format == KVQ_FORMAT_FP4_E2M1_E4M3_G16) {
+  if (is_fp4_layout(cache)) {
     if (d_seq_lens == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
     dequant_fp4_kernel<<<grid_for(work, 256), 256, 0, s>>>(*cache, batch, d_seq_lens, max_len, out_dtype, k_out,
                                                            v_out, d_err_flag);

@@ -16,14 +16,24 @@ inline bool is_pow2_page(int32_t p) { return p == 16 || p == 32 || p == 64 || p 
 inline bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Validates a cache description for `batch` sequences.
+inline bool is_fp4_layout(const kvq_cache* c) {
+  return c->format == KVQ_FORMAT_FP4_E2M1_E4M3_G16 || c->format == KVQ_FORMAT_NVFP4;
+}
+
 inline kvq_status check_cache(const kvq_cache* c, int32_t batch) {
   if (c == nullptr || c->reserved != 0 || c->num_kv_heads < 1 || c->data == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
   if (!aligned_to(c->data, 16)) return KVQ_ERR_INVALID_ARGUMENT;
-  if (c->format == KVQ_FORMAT_FP4_E2M1_E4M3_G16) {
+  if (c->format == KVQ_FORMAT_FP4_E2M1_E4M3_G16 || c->format == KVQ_FORMAT_NVFP4) {
     if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return KVQ_ERR_INVALID_ARGUMENT;
     if (!is_pow2_page(c->page_size) || c->num_pages < 1 || c->max_pages_per_seq < 1)
       return KVQ_ERR_INVALID_ARGUMENT;
-    if (c->v_data != nullptr || c->k_scale != nullptr || c->v_scale != nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+    if (c->v_data != nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+    if (c->format == KVQ_FORMAT_NVFP4) {  // second-level scales: float [Hkv] each
+      if (c->k_scale == nullptr || c->v_scale == nullptr || !aligned_to(c->k_scale, 4) || !aligned_to(c->v_scale, 4))
+        return KVQ_ERR_INVALID_ARGUMENT;
+    } else if (c->k_scale != nullptr || c->v_scale != nullptr) {
+      return KVQ_ERR_INVALID_ARGUMENT;
+    }
     if (c->page_table == nullptr && (int64_t)batch * c->max_pages_per_seq > c->num_pages)
       return KVQ_ERR_INVALID_ARGUMENT;
     if (c->num_pages * (int64_t)c->num_kv_heads > (int64_t)INT32_MAX) return KVQ_ERR_UNSUPPORTED;

@@ -23,6 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libkvq.so")
 
 FORMAT_FP4 = 1
 FORMAT_FP8 = 2
+FORMAT_NVFP4 = 3
 FLAG_NONFINITE = 0x1
 FLAG_PAGE_OOB = 0x2
 FLAG_TIMEOUT = 0x4
@@ -133,10 +134,13 @@ class Fp4Cache:
           of one kv head (K codes, K scales, V codes in token pairs, V scales;
           the byte layout is documented in include/kvq.h).
     page_table int32 [batch][max_pages_per_seq] or None (contiguous).
+    nvfp4=True adds one fp32 second-level scale per kv head for K and for V
+    (k_gscale, v_gscale: float [num_kv_heads], 1 until set by fp8_set_scales).
     """
 
     def __init__(self, num_kv_heads: int, head_dim: int, page_size: int, num_pages: int,
-                 max_pages_per_seq: int, page_table: Optional[torch.Tensor] = None, device="cuda"):
+                 max_pages_per_seq: int, page_table: Optional[torch.Tensor] = None, device="cuda",
+                 nvfp4: bool = False):
         self.num_kv_heads, self.head_dim, self.page_size = num_kv_heads, head_dim, page_size
         self.num_pages, self.max_pages_per_seq = num_pages, max_pages_per_seq
         self.group = min(page_size, 128)
@@ -149,11 +153,15 @@ class Fp4Cache:
         if page_table is not None:
             _need(page_table, torch.int32, "page_table")
         self.page_table = page_table
+        self.nvfp4 = nvfp4
+        self.k_gscale = torch.ones(num_kv_heads, dtype=torch.float32, device=device) if nvfp4 else None
+        self.v_gscale = torch.ones(num_kv_heads, dtype=torch.float32, device=device) if nvfp4 else None
 
     def struct(self, page_table: Optional[torch.Tensor] = None) -> KvqCacheStruct:
         pt = self.page_table if page_table is None else page_table
-        return KvqCacheStruct(FORMAT_FP4, self.num_kv_heads, self.head_dim, self.page_size, self.num_pages,
-                              self.max_pages_per_seq, 0, _ptr(pt), _ptr(self.pool), None, None, None)
+        return KvqCacheStruct(FORMAT_NVFP4 if self.nvfp4 else FORMAT_FP4, self.num_kv_heads, self.head_dim,
+                              self.page_size, self.num_pages, self.max_pages_per_seq, 0, _ptr(pt), _ptr(self.pool),
+                              None, _ptr(self.k_gscale), _ptr(self.v_gscale))
 
     @property
     def nbytes(self) -> int:
@@ -197,9 +205,11 @@ def append(cache, start_pos: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
     _check(st, "kvq_append")
 
 
-def fp8_set_scales(cache: Fp8WindowCache, k: torch.Tensor, v: torch.Tensor,
+def fp8_set_scales(cache, k: torch.Tensor, v: torch.Tensor,
                    err: Optional[torch.Tensor] = None, stream=None) -> None:
-    """kvq_fp8_set_scales: per-head s_h = amax/448 over k, v bf16 [batch][n][Hkv][D]."""
+    """kvq_fp8_set_scales over k, v bf16 [batch][n][Hkv][D]: an FP8 window
+    cache gets s_h = amax/448 per head, an NVFP4 cache its second-level
+    scales S_h = amax/(6*448)."""
     _need(k, torch.bfloat16, "k")
     _need(v, torch.bfloat16, "v")
     s = cache.struct()

@@ -62,6 +62,15 @@
  *   page_table == NULL the cache is contiguous: page p/page_size of sequence b
  *   is b*max_pages_per_seq + p/page_size.
  *
+ * NVFP4 cache (format KVQ_FORMAT_NVFP4): the FP4 layout above plus one fp32
+ *   second-level scale per kv head, k_scale and v_scale: float [num_kv_heads]
+ *   ("KV Cache Quantisation": FP8 or NVFP4 with the scales handled at read
+ *   time).  Codes and block scales are those of x / S (fp32 division), and a
+ *   value reads back as fp32(fp32(E2M1(code) * E4M3(s)) * S).  S is set from
+ *   calibration tokens by kvq_fp8_set_scales (S = amax / (6*448), so the
+ *   largest block lands on the top E4M3 scale and small tensors keep their
+ *   resolution instead of underflowing the E4M3 scale).
+ *
  * FP8 window cache layout (format KVQ_FORMAT_FP8_E4M3_HEAD), K in `data`, V in
  * `v_data`:
  *   uint8 [num_pages][num_kv_heads][page_size][head_dim], one E4M3FN byte per
@@ -99,7 +108,8 @@ typedef enum kvq_status {
 
 typedef enum kvq_format {
     KVQ_FORMAT_FP4_E2M1_E4M3_G16 = 1,
-    KVQ_FORMAT_FP8_E4M3_HEAD = 2
+    KVQ_FORMAT_FP8_E4M3_HEAD = 2,
+    KVQ_FORMAT_NVFP4 = 3
 } kvq_format;
 
 typedef struct kvq_stream_opaque *kvq_stream; /* a cudaStream_t */
@@ -121,17 +131,18 @@ typedef struct kvq_cache {
                                   FP8: must be NULL */
     void *data;                /* FP4: the page pool; FP8: K codes (16-byte aligned) */
     void *v_data;              /* FP8: V codes (16-byte aligned); FP4: must be NULL */
-    void *k_scale;             /* FP8: float [Hkv]; FP4: must be NULL */
-    void *v_scale;             /* FP8: float [Hkv]; FP4: must be NULL */
+    void *k_scale;             /* FP8, NVFP4: float [Hkv]; FP4: must be NULL */
+    void *v_scale;             /* FP8, NVFP4: float [Hkv]; FP4: must be NULL */
 } kvq_cache;
 
 /*
  * kvq_append -- quantise n_new new tokens per sequence into `cache`.
  * ("Quantising the KV cache", section "Code": per 16-channel block, scale
  * RNE_e4m3(amax/6) saturating with 0 -> 2^-9, codes RNE_e2m1(v/s) saturating,
- * IEEE fp32 divisions; FP8 caches: code RNE_e4m3(x / s_h) saturating.)
- *   cache       FP4 or FP8 cache (an FP8 cache needs its scales set first,
- *               e.g. by kvq_fp8_set_scales).
+ * IEEE fp32 divisions; NVFP4 caches: the same on x / S_h; FP8 caches: code
+ * RNE_e4m3(x / s_h) saturating.)
+ *   cache       FP4, NVFP4 or FP8 cache (NVFP4 and FP8 caches need their
+ *               scales set first, e.g. by kvq_fp8_set_scales).
  *   batch       number of sequences (rows of page_table / rings), >= 0.
  *   n_new       new tokens per sequence, >= 0.
  *   d_start_pos device int32 [batch]: position of each sequence's first new
@@ -150,11 +161,13 @@ kvq_status kvq_append(const kvq_cache *cache, int32_t batch, int32_t n_new,
                       int32_t *d_err_flag, kvq_stream stream);
 
 /*
- * kvq_fp8_set_scales -- set an FP8 window cache's per-head scales from a
- * calibration set of tokens: s_h = amax / 448 in fp32 over every value of kv
- * head h in k (resp. v), 1 where amax == 0.  ("Week 6 -- FP4 KV Caches and
- * Bounded Replay": SWA KV stays FP8; "Quantising the KV cache" table row
- * "FP8 E4M3, one scale per tensor", here one scale per head.)
+ * kvq_fp8_set_scales -- set a cache's per-head fp32 scales from a calibration
+ * set of tokens, over every value of kv head h in k (resp. v), 1 where
+ * amax == 0: an FP8 window cache gets s_h = amax / 448 ("Week 6 -- FP4 KV
+ * Caches and Bounded Replay": SWA KV stays FP8; "Quantising the KV cache"
+ * table row "FP8 E4M3, one scale per tensor", here one scale per head); an
+ * NVFP4 cache gets its second-level scales S_h = amax / (6*448).  Both are
+ * fp32 divisions.
  *   k, v   device bf16 [batch][n][num_kv_heads][head_dim].
  * Writes cache->k_scale and cache->v_scale (float [Hkv]).  Device flags:
  * NONFINITE.
@@ -179,7 +192,8 @@ size_t kvq_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t nu
  * cache", section "Code": quantised K/V feed an unchanged attention;
  * "Concept": decode reads the whole cache.)
  *   out[b][h][:] = sum_t softmax_t(softmax_scale * q[b][h] . K^[b][t]) V^[b][t]
- *   global       FP4 cache with head_dim 64 or 128.
+ *   global       FP4 or NVFP4 cache with head_dim 64 or 128 (NVFP4: the
+ *                second-level scales multiply the scores and the values).
  *   swa          FP8 window cache with the same num_kv_heads/head_dim, or NULL.
  *   batch        sequences, >= 1.
  *   num_q_heads  Hq, a multiple of num_kv_heads with Hq/Hkv <= 8.
@@ -224,10 +238,11 @@ kvq_status kvq_decode_attn_noalloc(const kvq_cache *global, const kvq_cache *swa
 
 /*
  * kvq_dequant -- expand a cache to dense values (value = E2M1(code) * E4M3(s)
- * for FP4, exact in fp32 and bf16; fp32(E4M3(code) * s_h) for FP8).
+ * for FP4, exact in fp32 and bf16; fp32(that * S) for NVFP4;
+ * fp32(E4M3(code) * s_h) for FP8).
  * ("Quantising the KV cache", section "Code": the dequantised value is the
  * code times its scale.)
- *   FP4: k_out, v_out [batch][max_len][num_kv_heads][head_dim]; positions
+ *   FP4, NVFP4: k_out, v_out [batch][max_len][num_kv_heads][head_dim]; positions
  *        >= d_seq_lens[b] are written as 0.
  *   FP8: max_len must equal the window W; the rings are written in slot order
  *        [batch][W][num_kv_heads][head_dim] and d_seq_lens is ignored (NULL ok).
