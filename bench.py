@@ -168,7 +168,7 @@ def fp4_bytes_per_token(w) -> int:
 class Setup:
     """The resident FP4 cache of a workload plus the per-step inputs."""
 
-    def __init__(self, w, seed: int, device, layers: int = 1):
+    def __init__(self, w, seed: int, device, layers: int = 1, nvfp4: bool = False):
         from fp4_kv_cache_kvq_gb300 import kvq
         self.w = w
         self.layers = layers
@@ -177,8 +177,12 @@ class Setup:
         table, num_pages, max_pages = workloads.page_layout(w, self.lens0, reserve=CYCLE, seed=seed)
         self.table = table.to(device) if table is not None else None
         self.cache = kvq.Fp4Cache(w.num_kv_heads, w.head_dim, w.page_size, num_pages, max_pages,
-                                  page_table=self.table, device=device)
+                                  page_table=self.table, device=device, nvfp4=nvfp4)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        if nvfp4:  # second-level scales from the first sequence's prefill (calibration)
+            k0, v0 = workloads.sequence_kv(w, 0, min(self.lens0[0], 8192), seed=seed, device=device)
+            kvq.fp8_set_scales(self.cache, k0[None], v0[None], err=self.err)
+            del k0, v0
         zero = torch.zeros(1, dtype=torch.int32, device=device)
         for b, n in enumerate(self.lens0):
             k, v = workloads.sequence_kv(w, b, n, seed=seed, device=device)
@@ -208,8 +212,11 @@ class Setup:
         self.swas = [self.swa]
         for _ in range(1, layers):
             c = kvq.Fp4Cache(w.num_kv_heads, w.head_dim, w.page_size, num_pages, max_pages,
-                             page_table=self.table, device=device)
+                             page_table=self.table, device=device, nvfp4=nvfp4)
             c.pool.copy_(self.cache.pool)
+            if nvfp4:
+                c.k_gscale.copy_(self.cache.k_gscale)
+                c.v_gscale.copy_(self.cache.v_gscale)
             self.caches.append(c)
             if self.swa is not None:
                 sw = kvq.Fp8WindowCache(w.batch, w.num_kv_heads, w.head_dim, w.window, device=device)
@@ -278,7 +285,7 @@ def run_gpu(args, dist: Dist):
     build.build()
     w = workloads.WORKLOADS[args.workload]
     L = args.layers
-    st = Setup(w, args.seed, device, layers=L)
+    st = Setup(w, args.seed, device, layers=L, nvfp4=args.format == "nvfp4")
     K, Wm = args.steps, args.warmup
     for i in range(Wm):
         st.step(i)
@@ -367,7 +374,8 @@ def run_gpu(args, dist: Dist):
         "ms_per_step": max_s * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16", "data": "synthetic",
         "config": {"workload": f"{w.name}: {w.description}; step = append 1 token/seq + decode attention"
-                   + (f", {L} layers" if L > 1 else ""), "layers": L,
+                   + (f", {L} layers" if L > 1 else "") + (", NVFP4 cache" if args.format == "nvfp4" else ""),
+                   "layers": L, "format": args.format,
                    "batch": w.batch, "kv_heads": w.num_kv_heads, "q_heads": w.num_q_heads,
                    "head_dim": w.head_dim, "context": w.context, "page_size": w.page_size,
                    "cache_bytes": st.cache.nbytes * L,
@@ -392,7 +400,8 @@ def run_gpu(args, dist: Dist):
     if clk is not None:
         result["clocks"] = clk
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, args.seed, st, budget_s=args.cpu_budget)
+        result["cpu_baseline"] = cpu_baseline(w, args.seed, st, budget_s=args.cpu_budget,
+                                              nvfp4=args.format == "nvfp4")
     return result
 
 
@@ -411,13 +420,16 @@ def run_prefill(args, dist: Dist):
     w = workloads.WORKLOADS["prefill"]
     B, T = w.batch, w.context
     max_pages = -(-T // w.page_size)
-    cache = kvq.Fp4Cache(w.num_kv_heads, w.head_dim, w.page_size, B * max_pages, max_pages, device=device)
+    nv = args.format == "nvfp4"
+    cache = kvq.Fp4Cache(w.num_kv_heads, w.head_dim, w.page_size, B * max_pages, max_pages, device=device, nvfp4=nv)
     k = torch.empty((B, T, w.num_kv_heads, w.head_dim), dtype=torch.bfloat16, device=device)
     v = torch.empty_like(k)
     for b in range(B):
         k[b], v[b] = workloads.sequence_kv(w, b, T, seed=args.seed, device=device)
     start = torch.zeros(B, dtype=torch.int32, device=device)
     err = torch.zeros(1, dtype=torch.int32, device=device)
+    if nv:  # second-level scales from the whole prefill (calibration, outside the timed region)
+        kvq.fp8_set_scales(cache, k, v, err=err)
     K, Wm = args.steps, args.warmup
     for _ in range(Wm):
         kvq.append(cache, start, k, v, err=err)
@@ -459,7 +471,8 @@ def run_prefill(args, dist: Dist):
         "metric": PREFILL_METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": K,
         "warmup": Wm, "ms_per_step": max_s * 1e3 / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"prefill: {w.description}", "batch": B, "tokens": T, "kv_heads": w.num_kv_heads,
+        "config": {"workload": f"prefill: {w.description}" + (", NVFP4 cache" if nv else ""), "format": args.format,
+                   "batch": B, "tokens": T, "kv_heads": w.num_kv_heads,
                    "head_dim": w.head_dim, "page_size": w.page_size,
                    "l2": "inputs larger than L2 (1.07 GB of bf16 per step), no flush",
                    "parallelism": f"replicas x{dist.world}"},
@@ -481,12 +494,13 @@ class OracleSample:
     """Host copies of some (sequence, kv head) units of the workload, already
     quantised by the oracle (the cache is resident state, not step work)."""
 
-    def __init__(self, w, seed: int, n_units: int, max_tokens=None, device="cpu"):
+    def __init__(self, w, seed: int, n_units: int, max_tokens=None, device="cpu", nvfp4: bool = False):
         import numpy as np
 
         import oracle
         self.o = oracle
         self.w = w
+        self.nvfp4 = nvfp4
         rng = np.random.default_rng(seed + 99)
         lens = workloads.lengths(w, seed)
         self.units = []
@@ -498,17 +512,25 @@ class OracleSample:
             kh = k[:T, h].float().cpu().numpy()
             vh = v[:T, h].float().cpu().numpy()
             q = workloads.queries(w, seed=seed, device=device)[b, h * w.group:(h + 1) * w.group].float().cpu()
-            kc, ks, _ = oracle.quantize_rows(kh)
-            vc, vs, _ = oracle.quantize_rows(vh)
-            self.units.append((q.numpy(), kc, ks, vc, vs, kh[-1:].copy(), vh[-1:].copy(), T))
+            sk = oracle.nvfp4_global_scale(kh) if nvfp4 else 1.0
+            sv = oracle.nvfp4_global_scale(vh) if nvfp4 else 1.0
+            kc, ks, _ = oracle.nvfp4_quantize_rows(kh, sk) if nvfp4 else oracle.quantize_rows(kh)
+            vc, vs, _ = oracle.nvfp4_quantize_rows(vh, sv) if nvfp4 else oracle.quantize_rows(vh)
+            self.units.append((q.numpy(), kc, ks, vc, vs, kh[-1:].copy(), vh[-1:].copy(), T, sk, sv))
 
     def run_unit(self, u):
-        q, kc, ks, vc, vs, knew, vnew, T = u
+        q, kc, ks, vc, vs, knew, vnew, T, sk, sv = u
         o = self.o
-        o.quantize_rows(knew)   # the step's append of this unit's new token
-        o.quantize_rows(vnew)
-        kd = o.dequantize_rows(kc, ks)
-        vd = o.dequantize_rows(vc, vs)
+        if self.nvfp4:  # the step's append of this unit's new token, then the cache read back
+            o.nvfp4_quantize_rows(knew, sk)
+            o.nvfp4_quantize_rows(vnew, sv)
+            kd = o.nvfp4_dequantize_rows(kc, ks, sk)
+            vd = o.nvfp4_dequantize_rows(vc, vs, sv)
+        else:
+            o.quantize_rows(knew)
+            o.quantize_rows(vnew)
+            kd = o.dequantize_rows(kc, ks)
+            vd = o.dequantize_rows(vc, vs)
         o.attend(q, kd, vd, 1.0 / math.sqrt(self.w.head_dim))
         return T
 
@@ -518,10 +540,10 @@ class OracleSample:
         return toks / self.w.num_kv_heads, time.perf_counter() - t
 
 
-def cpu_baseline(w, seed, st=None, budget_s=20.0):
+def cpu_baseline(w, seed, st=None, budget_s=20.0, nvfp4=False):
     cores = os.cpu_count() or 1
     n_units = max(cores, 8)
-    sample = OracleSample(w, seed, n_units, device="cuda" if torch.cuda.is_available() else "cpu")
+    sample = OracleSample(w, seed, n_units, device="cuda" if torch.cuda.is_available() else "cpu", nvfp4=nvfp4)
     with cf.ThreadPoolExecutor(max_workers=cores) as pool:
         kv, secs = sample.run(pool)
         reps = 1
@@ -542,13 +564,14 @@ def run_reference(args, dist: Dist):
     cores = os.cpu_count() or 1
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     # size each step so the whole warm-up + timed run stays around a minute
-    probe = OracleSample(w, args.seed, 1, max_tokens=4096, device=dev)
+    nv = args.format == "nvfp4"
+    probe = OracleSample(w, args.seed, 1, max_tokens=4096, device=dev, nvfp4=nv)
     with cf.ThreadPoolExecutor(max_workers=cores) as pool:
         _, t_probe = probe.run(pool)
         per_token_s = t_probe / 4096
         budget_per_step = 60.0 / max(1, args.steps + args.warmup)
         max_tokens = int(min(w.context or 131072, max(64, budget_per_step * cores / per_token_s)))
-        sample = OracleSample(w, args.seed, cores, max_tokens=max_tokens, device=dev)
+        sample = OracleSample(w, args.seed, cores, max_tokens=max_tokens, device=dev, nvfp4=nv)
         for _ in range(args.warmup):
             sample.run(pool)
         kv, secs = 0.0, 0.0
@@ -562,7 +585,8 @@ def run_reference(args, dist: Dist):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{w.name}: {w.description}; step = append 1 token/seq + decode attention"
-                   + (f", {args.layers} layers" if args.layers > 1 else ""), "layers": args.layers,
+                   + (f", {args.layers} layers" if args.layers > 1 else "")
+                   + (", NVFP4 cache" if args.format == "nvfp4" else ""), "layers": args.layers, "format": args.format,
                    "batch": w.batch, "kv_heads": w.num_kv_heads, "q_heads": w.num_q_heads,
                    "head_dim": w.head_dim, "context": w.context, "page_size": w.page_size,
                    "parallelism": "host threads"},
@@ -581,6 +605,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="long_context",
                     choices=["long_context", "gqa_outliers", "paged_ragged", "swa_append", "tiny", "prefill"])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--format", choices=["fp4", "nvfp4"], default="fp4",
+                    help="cache format: FP4 (E4M3 scale per 16) or NVFP4 (plus an fp32 scale per kv head)")
     ap.add_argument("--layers", type=int, default=1,
                     help="layers per step, each with its own cache (long_context at 4 layers: 4.84 GB)")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
