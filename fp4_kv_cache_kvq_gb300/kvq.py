@@ -89,6 +89,9 @@ def load() -> ctypes.CDLL:
             L.kvq_status_string.argtypes = [ctypes.c_int]
             L.kvq_version.restype = ctypes.c_int32
             L.kvq_version.argtypes = []
+            L.kvq_prefill_attn.restype = ctypes.c_int
+            L.kvq_prefill_attn.argtypes = [_CP, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P,
+                                           ctypes.c_float, _P, _P, _P]
             L.kvq_fake_quant.restype = ctypes.c_int
             L.kvq_fake_quant.argtypes = [ctypes.c_int32] * 6 + [_P] * 6
             L.kvq_attn_dense.restype = ctypes.c_int
@@ -244,6 +247,25 @@ def decode_attn(cache: Fp4Cache, seq_lens: torch.Tensor, q: torch.Tensor, softma
                                 _ptr(seq_lens), _ptr(q), float(softmax_scale), _ptr(out), _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream))
     _check(st, "kvq_decode_attn")
+    return out
+
+
+def prefill_attn(cache: Fp4Cache, seq_lens: torch.Tensor, q: torch.Tensor, softmax_scale: Optional[float] = None,
+                 out: Optional[torch.Tensor] = None, err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """kvq_prefill_attn: q bf16 [batch][chunk][Hq][head_dim] (their keys and
+    values already appended) -> out float32, same shape; causal over the cache."""
+    _need(q, torch.bfloat16, "q")
+    _need(seq_lens, torch.int32, "seq_lens")
+    batch, chunk, hq, d = q.shape
+    if out is None:
+        out = torch.empty((batch, chunk, hq, d), dtype=torch.float32, device=q.device)
+    _need(out, torch.float32, "out")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    c = cache.struct()
+    st = load().kvq_prefill_attn(ctypes.byref(c), batch, hq, chunk, _ptr(seq_lens), _ptr(q), float(softmax_scale),
+                                 _ptr(out), _ptr(err), _stream(stream))
+    _check(st, "kvq_prefill_attn")
     return out
 
 

@@ -237,6 +237,29 @@ kvq_status kvq_decode_attn_noalloc(const kvq_cache *global, const kvq_cache *swa
                                    kvq_stream stream);
 
 /*
+ * kvq_prefill_attn -- attention of a chunk of new query tokens over the FP4 or
+ * NVFP4 cache that already holds their keys and values (chunked prefill):
+ * query token i of sequence b (0 <= i < chunk) sits at position
+ * T_b - chunk + i and attends positions 0..T_b - chunk + i (causal), every
+ * one dequantised from the cache.  ("Quantising the KV cache", section
+ * "Code": the quantised K and V feed an unchanged attention.)  Runs on the
+ * tensor cores: one CTA per 128 query rows (G query heads x 128/G tokens),
+ * cache tiles of 128 positions dequantised once into shared memory.
+ *   cache        FP4 or NVFP4 cache, head_dim 64 or 128.
+ *   num_q_heads  Hq, a multiple of num_kv_heads with G = Hq/Hkv in {1,2,4,8}.
+ *   d_seq_lens   device int32 [batch]: T_b >= chunk, the positions in the
+ *                cache including the chunk's.
+ *   q            device bf16 [batch][chunk][num_q_heads][head_dim].
+ *   out          device float [batch][chunk][num_q_heads][head_dim].
+ * Host errors: INVALID_ARGUMENT; UNSUPPORTED (head_dim, G).  Device flags:
+ * BAD_LENGTH (T_b < chunk: the sequence's rows are written as 0), PAGE_OOB,
+ * TIMEOUT.
+ */
+kvq_status kvq_prefill_attn(const kvq_cache *cache, int32_t batch, int32_t num_q_heads, int32_t chunk,
+                            const int32_t *d_seq_lens, const void *q, float softmax_scale, float *out,
+                            int32_t *d_err_flag, kvq_stream stream);
+
+/*
  * kvq_dequant -- expand a cache to dense values (value = E2M1(code) * E4M3(s)
  * for FP4, exact in fp32 and bf16; fp32(that * S) for NVFP4;
  * fp32(E4M3(code) * s_h) for FP8).

@@ -31,8 +31,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "kvq_append", "kvq_attn_dense", "kvq_decode_attn", "kvq_decode_attn_noalloc", "kvq_decode_workspace_bytes",
-        "kvq_dequant", "kvq_fake_quant", "kvq_fp4_pool_bytes", "kvq_fp8_set_scales", "kvq_status_string",
-        "kvq_version"])
+        "kvq_dequant", "kvq_fake_quant", "kvq_fp4_pool_bytes", "kvq_fp8_set_scales", "kvq_prefill_attn",
+        "kvq_status_string", "kvq_version"])
 
 
 def test_library_exports_every_declared_function(lib):
@@ -78,6 +78,14 @@ def test_sweep_entry_points_refuse_bad_arguments_on_the_host(lib):
     assert lib.kvq_attn_dense(1, 16385, 2, 1, 64, 16, 32, 64, 0.1, 128, None, None) == 2
     assert lib.kvq_attn_dense(1, 8, 3, 2, 64, 16, 32, 64, 0.1, 128, None, None) == 1
     assert lib.kvq_attn_dense(1, 8, 2, 1, 64, 16, 32, 64, -1.0, 128, None, None) == 1
+
+
+def test_prefill_refuses_bad_arguments_on_the_host(lib):
+    s = _fp4_struct()
+    assert lib.kvq_prefill_attn(ctypes.byref(s), 2, 16, 0, 16, 32, 0.1, 64, None, None) == 1   # chunk 0
+    assert lib.kvq_prefill_attn(ctypes.byref(s), 2, 3, 4, 16, 32, 0.1, 64, None, None) == 1    # Hq % Hkv
+    assert lib.kvq_prefill_attn(ctypes.byref(s), 2, 32, 4, 16, 32, 0.1, 64, None, None) == 2   # G = 16
+    assert lib.kvq_prefill_attn(ctypes.byref(s), 2, 16, 4, None, 32, 0.1, 64, None, None) == 1  # no lengths
 
 
 def test_fp4_pool_bytes(lib):
