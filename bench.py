@@ -489,6 +489,106 @@ def run_prefill(args, dist: Dist):
     return res
 
 
+PREFILL_ATTN_METRIC = "chunked-prefill attention over the FP4 cache: query tokens/s (tensor-core TFLOP/s), 1xGB300"
+
+
+def measured_tensor_peak():
+    """Dense bf16 (= f16) tensor peak in TFLOP/s: the measured burst figure,
+    else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "MEASURED_PEAKS.json bf16_tflops (burst), of measured"
+    except Exception:
+        return 1900.0, "fallback 1.9 PFLOP/s bf16 burst"
+
+
+def run_prefill_attn(args, dist: Dist):
+    """A step is one kvq_prefill_attn call: B4 x 1024 query tokens (Hq64, d128)
+    attending causally over 16384 cached FP4 positions each.  value = query
+    tokens/s; the roofline counts the causally attended multiply-adds
+    (4 flop per query head, position and channel: QK^T and PV)."""
+    from fp4_kv_cache_kvq_gb300 import build, kvq
+    device = torch.device("cuda", dist.local)
+    torch.cuda.set_device(device)
+    build.build()
+    w = workloads.WORKLOADS["prefill_attn"]
+    B, T, C = w.batch, w.context, w.chunk
+    max_pages = -(-T // w.page_size)
+    nv = args.format == "nvfp4"
+    cache = kvq.Fp4Cache(w.num_kv_heads, w.head_dim, w.page_size, B * max_pages, max_pages, device=device, nvfp4=nv)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    k = torch.empty((B, T, w.num_kv_heads, w.head_dim), dtype=torch.bfloat16, device=device)
+    v = torch.empty_like(k)
+    for b in range(B):
+        k[b], v[b] = workloads.sequence_kv(w, b, T, seed=args.seed, device=device)
+    if nv:
+        kvq.fp8_set_scales(cache, k, v, err=err)
+    kvq.append(cache, torch.zeros(B, dtype=torch.int32, device=device), k, v, err=err)
+    del k, v
+    g = torch.Generator(device=device)
+    g.manual_seed(args.seed * 1_000_003 + 4242)
+    q = torch.randn((B, C, w.num_q_heads, w.head_dim), generator=g, device=device).to(torch.bfloat16)
+    lens = torch.full((B,), T, dtype=torch.int32, device=device)
+    out = torch.empty((B, C, w.num_q_heads, w.head_dim), dtype=torch.float32, device=device)
+    K, Wm = args.steps, args.warmup
+    for _ in range(Wm):
+        kvq.prefill_attn(cache, lens, q, out=out, err=err)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(device.index)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    t0.record()
+    for _ in range(K):
+        kvq.prefill_attn(cache, lens, q, out=out, err=err)
+    t1.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    if err.item() != 0:
+        raise RuntimeError(f"device error flag {err.item()}")
+    secs = t0.elapsed_time(t1) / 1e3
+    tokens = B * C
+    value, max_s = combine_ranks(dist, tokens * K, secs)
+    positions = B * w.num_q_heads * sum(T - C + i + 1 for i in range(C))  # causally attended (row, position)
+    flops = 4 * positions * w.head_dim
+    achieved = flops * K / secs / 1e12
+    peak, peak_src = measured_tensor_peak()
+    # end to end: the chunk's queries in from pinned host memory, the output back
+    qh = q.cpu().pin_memory()
+    oh = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    Ke = min(K, 10)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(Ke):
+        q.copy_(qh, non_blocking=True)
+        kvq.prefill_attn(cache, lens, q, out=out, err=err)
+        oh.copy_(out, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e, _ = combine_ranks(dist, tokens * Ke, e0.elapsed_time(e1) / 1e3)
+    res = {
+        "metric": PREFILL_ATTN_METRIC, "value": value, "unit": "query tokens/s", "n_gpus": dist.world, "steps": K,
+        "warmup": Wm, "ms_per_step": max_s * 1e3 / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": f"prefill_attn: {w.description}" + (", NVFP4 cache" if nv else ""),
+                   "format": args.format, "batch": B, "context": T, "chunk": C, "kv_heads": w.num_kv_heads,
+                   "q_heads": w.num_q_heads, "head_dim": w.head_dim, "page_size": w.page_size,
+                   "l2": "each kv head's cache (2.36 MB) is read by the 64 query-block CTAs of its chunk; no flush",
+                   "parallelism": f"replicas x{dist.world}"},
+        "roofline": {"bound": "tensor", "kernel": "prefill_fp4_kernel (tcgen05.mma f16, TMEM accumulators)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": peak_src, "traffic": None, "algorithmic_flops_per_launch": flops,
+                     "avg_launch_ms": secs * 1e3 / K},
+        "e2e": {"value": e2e, "unit": "query tokens/s", "h2d_bytes_per_step": q.numel() * 2,
+                "d2h_bytes_per_step": out.numel() * 4, "steps": Ke},
+        "gpu_launches": K,
+    }
+    if clk is not None:
+        res["clocks"] = clk
+    return res
+
+
 # ----------------------------------------------------------------- CPU oracle (baseline / reference arm)
 class OracleSample:
     """Host copies of some (sequence, kv head) units of the workload, already
@@ -603,7 +703,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
     ap.add_argument("--workload", default="long_context",
-                    choices=["long_context", "gqa_outliers", "paged_ragged", "swa_append", "tiny", "prefill"])
+                    choices=["long_context", "gqa_outliers", "paged_ragged", "swa_append", "tiny", "prefill",
+                             "prefill_attn"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--format", choices=["fp4", "nvfp4"], default="fp4",
                     help="cache format: FP4 (E4M3 scale per 16) or NVFP4 (plus an fp32 scale per kv head)")
@@ -620,6 +721,8 @@ def main(argv=None):
             res = run_reference(args, dist)
         elif args.workload == "prefill":
             res = run_prefill(args, dist)
+        elif args.workload == "prefill_attn":
+            res = run_prefill_attn(args, dist)
         else:
             res = run_gpu(args, dist)
         if dist.rank == 0 and res is not None:

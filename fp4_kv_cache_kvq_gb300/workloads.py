@@ -19,6 +19,8 @@ Workloads (one layer each):
   swa_append     B16, Hkv8, Hq64 (G8), d128, FP4 context 65536 plus an FP8
                  window of 128; each step appends one N(0,1) token per sequence.
   prefill        B16 x 16384 new tokens, Hkv8, d128 (append throughput).
+  prefill_attn   B4, Hkv8, Hq64 (G8), d128: the last 1024 of 16384 cached
+                 positions are a chunk of new queries attending causally.
 
 Draw order per sequence b: K then V (then the i.i.d. outlier mask), from a
 generator seeded with (seed, b), so any subset of sequences can be redrawn.
@@ -48,6 +50,7 @@ class Workload:
     k_outlier_prob: float = 0.0
     k_outlier_prob_factor: float = 1.0
     window: int = 0                        # FP8 sliding window (0 = none)
+    chunk: int = 0                         # chunked prefill: new query tokens per sequence
     description: str = field(default="", compare=False)
 
     @property
@@ -70,6 +73,9 @@ WORKLOADS = {
                            description="B16 Hkv8 Hq64 d128 FP4 T65536 + FP8 window 128, append 1/step"),
     "prefill": Workload("prefill", 16, 8, 8, 128, context=16384,
                         description="B16 x 16384-token bf16 prefill, Hkv8 d128"),
+    "prefill_attn": Workload("prefill_attn", 4, 8, 64, 128, context=16384, chunk=1024,
+                             description="B4 Hkv8 Hq64 d128: a 1024-token chunk attending causally over a "
+                                         "16384-position FP4 cache (the chunk's own tokens included)"),
 }
 
 _MIX = 1_000_003
