@@ -105,50 +105,84 @@ __device__ __forceinline__ void dequant_tile(uint32_t stage, uint32_t kdst, uint
   constexpr int NB = D / 16;
   constexpr int kGroupBytes = GT * 9 * D / 8;
   const int tid = threadIdx.x;
-  // K^: item (position n, 8-channel chunk kc); 8 consecutive threads take 8
-  // consecutive positions, so their 16-byte stores fill one core matrix
-#pragma unroll 4
-  for (int it = tid; it < kPTile * (D / 8); it += kPThreads) {
-    const int n = ((it >> 3) / (D / 8)) * 8 + (it & 7);
-    const int kc = (it >> 3) % (D / 8);
-    uint32_t r[4] = {0u, 0u, 0u, 0u};
-    if (n < valid) {
-      const uint32_t grp = stage + (uint32_t)((n / GT) * kGroupBytes);
-      const int ln = n % GT;
-      const uint32_t w = lds32(grp + (uint32_t)(ln * (D / 2) + kc * 4));
-      const uint32_t sb = lds8(grp + (uint32_t)(GT * (D / 2) + ln * NB + (kc >> 1)));
-      const uint32_t s2 = f16x2_from_e4m3x2(sb * 0x0101u);
-      f16x2x4_from_e2m1x8(w, r);
+  // K^: thread n takes position n, one 32-channel quarter per step: a 16-byte
+  // code load, the quarter's two block scales, four 16-byte stores.  The
+  // quarter order is rotated by position so that the 8 lanes of a load phase
+  // (8 consecutive positions, D/2 bytes apart) hit 8 different bank groups.
+  static_assert(kPThreads == kPTile, "one thread per tile position");
+  constexpr int kQuarters = D / 32;
+  constexpr int kRotShift = D == 128 ? 1 : 2;  // log2(positions per 128 code bytes)
+  {
+    const int n = tid;
+    const uint32_t grp = stage + (uint32_t)((n / GT) * kGroupBytes);
+    const int ln = n % GT;
+#pragma unroll 2
+    for (int m = 0; m < kQuarters; ++m) {
+      const int qq = (m + (n >> kRotShift)) & (kQuarters - 1);
+      uint32_t r[16];
+      if (n < valid) {
+        const uint4 w = lds128(grp + (uint32_t)(ln * (D / 2) + qq * 16));
+        const uint32_t s2 = f16x2_from_e4m3x2(lds16(grp + (uint32_t)(GT * (D / 2) + ln * NB + 2 * qq)));
+        const uint32_t sA = prmt(s2, 0u, 0x1010u), sB = prmt(s2, 0u, 0x3232u);  // each block's scale, twice
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) r[i] = hmul2_u32(r[i], s2);
+        for (int k = 0; k < 4; ++k) {
+          uint32_t t[4];
+          f16x2x4_from_e2m1x8(ws[k], t);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) r[4 * k + i] = hmul2_u32(t[i], k < 2 ? sA : sB);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        sts128(kdst + core_offset((uint32_t)n, (uint32_t)(qq * 32 + 8 * k), kPTile),
+               make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]));
     }
-    sts128(kdst + core_offset((uint32_t)n, (uint32_t)(kc * 8), kPTile), make_uint4(r[0], r[1], r[2], r[3]));
   }
-  // V^: item (channel c, 8-position block kb) = 4 token-pair rows of one
-  // channel; their code bytes pair the two tokens of a row
-#pragma unroll 4
-  for (int it = tid; it < D * (kPTile / 8); it += kPThreads) {
-    const int c = ((it >> 3) / (kPTile / 8)) * 8 + (it & 7);
-    const int kb = (it >> 3) % (kPTile / 8);
+  // V^: item (4 channels c..c+3, 8 positions = 4 token-pair rows): a 4-byte
+  // code load per pair row (each byte pairs the row's two positions), the
+  // pair's scales, one 16-byte store per channel
+#pragma unroll 2
+  for (int it = tid; it < (D / 4) * (kPTile / 8); it += kPThreads) {
+    const int c = (it % (D / 4)) * 4;
+    const int kb = it / (D / 4);
     const int n0 = kb * 8;
     const uint32_t grp = stage + (uint32_t)((n0 / GT) * kGroupBytes);
-    uint32_t r[4];
+    uint32_t words[4], sc[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int n = n0 + 2 * q;  // even position of the pair
       const int i = (n % GT) >> 1;
-      uint32_t v = 0u;
+      words[q] = 0u;
+      sc[q] = 0u;
       if (n < valid) {
         const int phys = (D == 64) ? 8 * ((c >> 3) ^ (((i >> 1) & 1) << 2)) + (c & 7)
                                    : 16 * ((c >> 4) ^ ((i & 3) << 1)) + (c & 15);
-        const uint32_t byte = lds8(grp + (uint32_t)(GT * (D / 2 + NB) + i * D + phys));
+        words[q] = lds32(grp + (uint32_t)(GT * (D / 2 + NB) + i * D + phys));
         uint32_t s2 = lds16(grp + (uint32_t)(GT * (D + NB) + i * 2 * NB + 2 * (c >> 4)));
         if (n + 1 >= valid) s2 &= 0x00FFu;  // the pair's second position is past the end: scale 0
-        v = hmul2_u32(f16x2_from_e2m1x2(byte), f16x2_from_e4m3x2(s2));
+        sc[q] = f16x2_from_e4m3x2(s2);
       }
-      r[q] = v;
     }
-    sts128(vdst + core_offset((uint32_t)c, (uint32_t)n0, D), make_uint4(r[0], r[1], r[2], r[3]));
+    // the 8 lanes of a store phase write channels 4t + cc: rotating each
+    // thread's byte order by (c / 8) mod 4 spreads them over 8 bank groups
+    const uint32_t rot = (uint32_t)(c >> 3) & 3u;
+    const uint32_t sel = (0x3210u + rot * 0x1111u) & 0x3333u;
+    uint32_t r[4][4];  // [rotated channel][pair]
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t t[4];
+      f16x2x4_from_e2m1x8(prmt(words[q], 0u, sel), t);  // t[cc]: channel c + (cc + rot) % 4, positions (n, n+1)
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) r[cc][q] = hmul2_u32(t[cc], sc[q]);
+    }
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc)
+      sts128(vdst + core_offset((uint32_t)c + ((cc + rot) & 3u), (uint32_t)n0, D),
+             make_uint4(r[cc][0], r[cc][1], r[cc][2], r[cc][3]));
   }
 }
 
@@ -273,21 +307,69 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
     tc_fence_after();
     if (!ok) break;
 
-    // ---- softmax of row tid over this tile
+    // ---- softmax of row tid over this tile, in one pass against the running
+    // reference m_run; a row whose tile maximum passes it by the slack (and
+    // every row on its first tile) redoes the pass with the raised reference
     const int64_t p0 = (int64_t)j * kPTile;
-    float mt = -INFINITY;
+    const bool all_in = row_ok && p0 + kPTile - 1 <= pos_r;  // no position of the tile masked
+    const bool none_in = !row_ok || p0 > pos_r;
+    float mt = -INFINITY, lt = 0.0f;
+    {
+      const float nref = m_run == -INFINITY ? 0.0f : -m_run;
 #pragma unroll
-    for (int c0 = 0; c0 < kPTile; c0 += 32) {
-      uint32_t v[32];
-      tmem_ld32(t_row + (uint32_t)c0, v);
+      for (int c0 = 0; c0 < kPTile; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(t_row + (uint32_t)c0, v);
+        uint32_t f[16];
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (p0 + c0 + i <= pos_r) mt = fmaxf(mt, __uint_as_float(v[i]) * cs);
+        for (int i = 0; i < 16; ++i) {
+          float xa = __uint_as_float(v[2 * i]) * cs, xb = __uint_as_float(v[2 * i + 1]) * cs;
+          if (!all_in) {
+            if (none_in || p0 + c0 + 2 * i > pos_r) xa = -INFINITY;
+            if (none_in || p0 + c0 + 2 * i + 1 > pos_r) xb = -INFINITY;
+          }
+          mt = fmaxf(mt, fmaxf(xa, xb));
+          const float pa = fast_exp2(xa + nref), pb = fast_exp2(xb + nref);
+          lt += pa + pb;
+          f[i] = pack_f16x2(pa, pb);
+        }
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8)
+          sts128(sb + G::kP + core_offset((uint32_t)tid, (uint32_t)(c0 + 8 * c8), kPRows),
+                 make_uint4(f[4 * c8], f[4 * c8 + 1], f[4 * c8 + 2], f[4 * c8 + 3]));
+      }
     }
-    // lazy max: raise the reference only when a score passes it by the slack;
-    // then rescale l and this row of O (TMEM accesses are warp-collective, so
-    // the warp rescales together, by 1 in the rows that keep their reference)
     const bool raise = row_ok && mt > m_run + kPSlack;
+    if (__any_sync(0xFFFFFFFFu, raise)) {
+      const float nref = -mt;
+#pragma unroll
+      for (int c0 = 0; c0 < kPTile; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(t_row + (uint32_t)c0, v);
+        if (raise) {
+          uint32_t f[16];
+          float l2 = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float xa = __uint_as_float(v[2 * i]) * cs, xb = __uint_as_float(v[2 * i + 1]) * cs;
+            if (!all_in) {
+              if (p0 + c0 + 2 * i > pos_r) xa = -INFINITY;
+              if (p0 + c0 + 2 * i + 1 > pos_r) xb = -INFINITY;
+            }
+            const float pa = fast_exp2(xa + nref), pb = fast_exp2(xb + nref);
+            l2 += pa + pb;
+            f[i] = pack_f16x2(pa, pb);
+          }
+          lt = c0 == 0 ? l2 : lt + l2;
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8)
+            sts128(sb + G::kP + core_offset((uint32_t)tid, (uint32_t)(c0 + 8 * c8), kPRows),
+                   make_uint4(f[4 * c8], f[4 * c8 + 1], f[4 * c8 + 2], f[4 * c8 + 3]));
+        }
+      }
+    }
+    // rows that raised their reference: rescale l and their row of O (TMEM
+    // accesses are warp-collective; the other rows multiply by 1)
     const float al = (raise && m_run != -INFINITY) ? fast_exp2(m_run - mt) : 1.0f;
     if (__any_sync(0xFFFFFFFFu, al != 1.0f)) {
 #pragma unroll
@@ -303,26 +385,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
       l_run *= al;
       m_run = mt;
     }
-    const float nref = m_run == -INFINITY ? 0.0f : -m_run;
-#pragma unroll
-    for (int c0 = 0; c0 < kPTile; c0 += 32) {
-      uint32_t v[32];
-      tmem_ld32(t_row + (uint32_t)c0, v);
-      uint32_t f[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const bool a = row_ok && p0 + c0 + 2 * i <= pos_r;
-        const bool bb = row_ok && p0 + c0 + 2 * i + 1 <= pos_r;
-        const float pa = a ? fast_exp2(fmaf(__uint_as_float(v[2 * i]), cs, nref)) : 0.0f;
-        const float pb = bb ? fast_exp2(fmaf(__uint_as_float(v[2 * i + 1]), cs, nref)) : 0.0f;
-        l_run += pa + pb;
-        f[i] = pack_f16x2(pa, pb);
-      }
-#pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8)
-        sts128(sb + G::kP + core_offset((uint32_t)tid, (uint32_t)(c0 + 8 * c8), kPRows),
-               make_uint4(f[4 * c8], f[4 * c8 + 1], f[4 * c8 + 2], f[4 * c8 + 3]));
-    }
+    l_run += lt;
     fence_async_smem();
     tc_fence_before();
     __syncthreads();  // P written; O rescales done
