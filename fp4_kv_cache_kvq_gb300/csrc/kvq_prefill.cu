@@ -10,20 +10,30 @@
 // run on the tensor cores; the cache is dequantised once per tile into shared
 // memory and shared by the CTA's 128 query rows.
 //
-// CTA = 128 threads, one per query row: the G query heads of one kv head times
-// 128/G consecutive query tokens of one sequence.  Per 128-position tile:
-//   bulk copy of the tile's FP4 groups (double-buffered, thread 0)
-//   dequantise K^ [128 pos][d] and V^ [d][128 pos] into shared memory in the
-//     tensor core's K-major core-matrix layout (f16, E2M1 code times E4M3
-//     scale; positions past the sequence end are zero)
-//   S = Q K^T            tcgen05.mma M=128 N=128 K=d, into TMEM
-//   online softmax, thread r owns row r: S from TMEM, scale, causal mask,
-//     lazy max (raised only past +8 in the log2 domain; O rescaled in TMEM
-//     then), P in f16 to shared memory
-//   O += P V             tcgen05.mma M=128 N=d K=128, into TMEM
-// Finally O / l (times the NVFP4 value scale) to global memory.  Every wait is
-// bounded; a timeout sets a flag, and the CTA waits (bounded) for its copies,
-// frees its TMEM and returns.
+// CTA = the G query heads of one kv head times 128/G consecutive query tokens
+// of one sequence (128 query rows), ten warps in four roles that run as a
+// pipeline over the sequence's 128-position cache tiles:
+//   loader (1 thread)   bulk copies of the FP4 tiles, 3 in flight
+//   dequant (4 warps)   K^ [128 pos][d] and V^ [d][128 pos] into shared memory
+//                       in the tensor core's K-major core-matrix layout (f16,
+//                       E2M1 code times E4M3 scale; positions past the end 0),
+//                       2 slots each
+//   MMA (1 thread)      S(j) = Q K^(j)^T     tcgen05.mma M=128 N=128 K=d into
+//                                           one of 3 TMEM S buffers
+//                       O += P(j-1) V^(j-1) tcgen05.mma M=128 N=d K=128, P read
+//                                           from TMEM, O accumulated in TMEM
+//   softmax (4 warps)   thread r owns row r: the tile's row max from TMEM, the
+//                       lazy reference (raised only past +8 in the log2 domain;
+//                       O rescaled in TMEM then), causal mask on the diagonal
+//                       tiles only, P = 2^(S - m) as f16 pairs written back over
+//                       the first half of its S buffer
+// so the tensor cores compute S(j+1) and O += P(j-1) V while the softmax warps
+// work on tile j and the dequantisers on tile j+1.  mbarriers hand each buffer
+// from producer to consumer and back (MMA completions arrive via
+// tcgen05.commit).  Finally O / l (times the NVFP4 value scale) goes to global
+// memory.  Every wait is bounded; a timeout raises the CTA's abort word, every
+// role leaves its loop, copies and MMAs still in flight are waited for
+// (bounded), the TMEM is freed and the timeout flag set.
 #include "kvq_common.cuh"
 #include "kvq_host.cuh"
 #include "kvq_tc.cuh"
@@ -33,9 +43,32 @@ namespace {
 
 constexpr int kPTile = 128;     // cache positions per tile
 constexpr int kPRows = 128;     // query rows per CTA
-constexpr int kPThreads = 128;  // one thread per row
-constexpr int kTmemCols = 256;  // S: columns [0, 128), O: [128, 128 + d)
+constexpr int kSoftWarps = 4;   // warps 0-3: softmax, thread = query row; also Q and the output
+constexpr int kDeqWarps = 4;    // warps 4-7: FP4 -> f16 dequantisation of K^ and V^
+constexpr int kLoadWarp = 8;    // lane 0: bulk copies of the FP4 tiles
+constexpr int kMmaWarp = 9;     // lane 0: tensor-core issue
+constexpr int kPThreads = 32 * (kMmaWarp + 1);
+constexpr int kSBufs = 3;       // S tiles in TMEM (128 columns each); P overwrites its S
+constexpr int kOCol = kSBufs * kPTile;  // O: TMEM columns [384, 384 + d)
+constexpr int kTmemCols = 512;
+constexpr int kFp4Stages = 3;   // FP4 tiles in flight
+constexpr int kRing = 2;        // K^ and V^ slots
 constexpr float kPSlack = 8.0f;
+constexpr uint32_t kPollNs = 20000;  // suspend hint of a barrier poll
+
+// mbarriers, by index
+enum : int {
+  kBFp4Full = 0,                        // [kFp4Stages] tile landed (bulk-copy bytes)
+  kBFp4Empty = kBFp4Full + kFp4Stages,  // [kFp4Stages] dequantisers done with the tile (128 arrivals)
+  kBKFull = kBFp4Empty + kFp4Stages,    // [kRing] K^ slot written (128 arrivals)
+  kBKEmpty = kBKFull + kRing,           // [kRing] S = Q K^T done reading it (MMA commit)
+  kBVFull = kBKEmpty + kRing,           // [kRing] V^ slot written
+  kBVEmpty = kBVFull + kRing,           // [kRing] O += P V done reading it
+  kBSFull = kBVEmpty + kRing,           // [kSBufs] S in TMEM
+  kBPFull = kBSFull + kSBufs,           // [kSBufs] P in TMEM, O rescaled (128 arrivals)
+  kBPvDone = kBPFull + kSBufs,          // [kSBufs] O += P V done (P's TMEM free again)
+  kNumBars = kBPvDone + kSBufs
+};
 
 struct PrefillParams {
   const int32_t* lens;
@@ -54,15 +87,59 @@ struct PrefillParams {
 template <int D>
 struct PGeo {
   static constexpr int kTileBytes = kPTile * 9 * D / 8;  // FP4 bytes of 128 positions of one kv head
-  static constexpr int kQ = 0;                           // Q  [128 rows][D]        f16, core layout
-  static constexpr int kK = kQ + kPRows * D * 2;         // K^ [128 positions][D]
-  static constexpr int kV = kK + kPTile * D * 2;         // V^ [D channels][128 positions]
-  static constexpr int kP = kV + D * kPTile * 2;         // P  [128 rows][128 positions]
-  static constexpr int kStage = kP + kPRows * kPTile * 2;
-  static constexpr int kBars = kStage + 2 * kTileBytes;  // full[2], mma, tmem slot, abort
-  static constexpr int kBytes = kBars + 64 + 128;        // + alignment slack
+  static constexpr int kOpBytes = kPTile * D * 2;        // Q, one K^ slot or one V^ slot (f16, core layout)
+  static constexpr int kQ = 0;                           // Q  [128 rows][D]
+  static constexpr int kK = kQ + kOpBytes;               // K^ [kRing][128 positions][D]
+  static constexpr int kV = kK + kRing * kOpBytes;       // V^ [kRing][D channels][128 positions]
+  static constexpr int kStage = kV + kRing * kOpBytes;   // FP4 tiles [kFp4Stages]
+  static constexpr int kBars = kStage + kFp4Stages * kTileBytes;
+  static constexpr int kUsed = kBars + 8 * kNumBars + 8 + 128;  // + TMEM slot, abort word, alignment slack
+  // at least half an SM's shared memory, so that one CTA (holding all 512
+  // TMEM columns) runs per SM
+  static constexpr int kBytes = kUsed > 116 * 1024 ? kUsed : 116 * 1024;
   static_assert(kTileBytes % 16 == 0 && kStage % 128 == 0 && kBars % 16 == 0, "shared-memory layout alignment");
+  static_assert(kBytes <= 227 * 1024, "shared memory per CTA");
 };
+
+// Bounded wait on an mbarrier phase that also gives up once another role has
+// given up; the first to time out raises the CTA's abort word.
+__device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait_hint(bar, parity, kPollNs)) return true;
+    if (*abort) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+// pwait with one outcome for the whole warp (TMEM accesses are warp-collective).
+__device__ __forceinline__ bool wwait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  return __all_sync(0xFFFFFFFFu, pwait(bar, parity, abort));
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1), one packed instruction
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                      float c1) {
+  asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mov.b64 c, {%6, %7};\n"
+      " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n .reg .b64 a, d;\n mov.b64 a, {%2, %3};\n mov.b64 d, {%0, %1};\n add.rn.f32x2 d, d, a;\n"
+      " mov.b64 {%0, %1}, d;\n}\n"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
 
 // Issue the bulk copies of tile j (its groups that start before position T)
 // into a stage buffer, arming `bar` with their byte count.
@@ -98,55 +175,57 @@ __device__ void issue_tile(const PrefillParams& p, int b, int h, int j, int T, u
     if (src[gi] >= 0) bulk_g2s(dst + gi * kGroupBytes, p.pool + src[gi], kGroupBytes, bar);
 }
 
-// K^ and V^ of one staged tile into the operand layouts; positions >= valid
-// (past the sequence end) are written as 0.
+// K^ of one staged tile into its operand layout ([position][channel],
+// K-major); positions >= valid (past the sequence end) are written as 0.
+// Thread n (of 128) takes position n, one 32-channel quarter per step: a
+// 16-byte code load, the quarter's two block scales, four 16-byte stores.  The
+// quarter order is rotated by position so that the 8 lanes of a load phase
+// (8 consecutive positions, D/2 bytes apart) hit 8 different bank groups.
 template <int D, int GT>
-__device__ __forceinline__ void dequant_tile(uint32_t stage, uint32_t kdst, uint32_t vdst, int valid) {
+__device__ __forceinline__ void dequant_k(uint32_t stage, uint32_t kdst, int valid, int n) {
   constexpr int NB = D / 16;
   constexpr int kGroupBytes = GT * 9 * D / 8;
-  const int tid = threadIdx.x;
-  // K^: thread n takes position n, one 32-channel quarter per step: a 16-byte
-  // code load, the quarter's two block scales, four 16-byte stores.  The
-  // quarter order is rotated by position so that the 8 lanes of a load phase
-  // (8 consecutive positions, D/2 bytes apart) hit 8 different bank groups.
-  static_assert(kPThreads == kPTile, "one thread per tile position");
   constexpr int kQuarters = D / 32;
   constexpr int kRotShift = D == 128 ? 1 : 2;  // log2(positions per 128 code bytes)
-  {
-    const int n = tid;
-    const uint32_t grp = stage + (uint32_t)((n / GT) * kGroupBytes);
-    const int ln = n % GT;
+  const uint32_t grp = stage + (uint32_t)((n / GT) * kGroupBytes);
+  const int ln = n % GT;
 #pragma unroll 2
-    for (int m = 0; m < kQuarters; ++m) {
-      const int qq = (m + (n >> kRotShift)) & (kQuarters - 1);
-      uint32_t r[16];
-      if (n < valid) {
-        const uint4 w = lds128(grp + (uint32_t)(ln * (D / 2) + qq * 16));
-        const uint32_t s2 = f16x2_from_e4m3x2(lds16(grp + (uint32_t)(GT * (D / 2) + ln * NB + 2 * qq)));
-        const uint32_t sA = prmt(s2, 0u, 0x1010u), sB = prmt(s2, 0u, 0x3232u);  // each block's scale, twice
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  for (int m = 0; m < kQuarters; ++m) {
+    const int qq = (m + (n >> kRotShift)) & (kQuarters - 1);
+    uint32_t r[16];
+    if (n < valid) {
+      const uint4 w = lds128(grp + (uint32_t)(ln * (D / 2) + qq * 16));
+      const uint32_t s2 = f16x2_from_e4m3x2(lds16(grp + (uint32_t)(GT * (D / 2) + ln * NB + 2 * qq)));
+      const uint32_t sA = prmt(s2, 0u, 0x1010u), sB = prmt(s2, 0u, 0x3232u);  // each block's scale, twice
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint32_t t[4];
-          f16x2x4_from_e2m1x8(ws[k], t);
+      for (int k = 0; k < 4; ++k) {
+        uint32_t t[4];
+        f16x2x4_from_e2m1x8(ws[k], t);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) r[4 * k + i] = hmul2_u32(t[i], k < 2 ? sA : sB);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] = 0u;
+        for (int i = 0; i < 4; ++i) r[4 * k + i] = hmul2_u32(t[i], k < 2 ? sA : sB);
       }
+    } else {
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        sts128(kdst + core_offset((uint32_t)n, (uint32_t)(qq * 32 + 8 * k), kPTile),
-               make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]));
+      for (int i = 0; i < 16; ++i) r[i] = 0u;
     }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      sts128(kdst + core_offset((uint32_t)n, (uint32_t)(qq * 32 + 8 * k), kPTile),
+             make_uint4(r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3]));
   }
-  // V^: item (4 channels c..c+3, 8 positions = 4 token-pair rows): a 4-byte
-  // code load per pair row (each byte pairs the row's two positions), the
-  // pair's scales, one 16-byte store per channel
+}
+
+// V^ of one staged tile into its operand layout ([channel][position],
+// K-major over positions).  Item (4 channels c..c+3, 8 positions = 4
+// token-pair rows): a 4-byte code load per pair row (each byte pairs the
+// row's two positions), the pair's scales, one 16-byte store per channel.
+template <int D, int GT>
+__device__ __forceinline__ void dequant_v(uint32_t stage, uint32_t vdst, int valid, int dt) {
+  constexpr int NB = D / 16;
+  constexpr int kGroupBytes = GT * 9 * D / 8;
 #pragma unroll 2
-  for (int it = tid; it < (D / 4) * (kPTile / 8); it += kPThreads) {
+  for (int it = dt; it < (D / 4) * (kPTile / 8); it += 32 * kDeqWarps) {
     const int c = (it % (D / 4)) * 4;
     const int kb = it / (D / 4);
     const int n0 = kb * 8;
@@ -186,27 +265,56 @@ __device__ __forceinline__ void dequant_tile(uint32_t stage, uint32_t kdst, uint
   }
 }
 
+// Row max of 32 raw scores of a tile (positions >= lim masked when !fast).
+__device__ __forceinline__ float chunk_max(const uint32_t (&v)[32], bool fast, int c0, int lim, float m) {
+  if (fast) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) m = fmax3(m, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (c0 + i < lim) m = fmaxf(m, __uint_as_float(v[i]));
+  }
+  return m;
+}
+
+// P = exp2(S * cs - m) for 32 scores, as 16 f16 pairs; adds the row sum.
+__device__ __forceinline__ void chunk_p(const uint32_t (&v)[32], uint32_t* w, bool fast, int c0, int lim, float cs,
+                                        float nref, float& l0, float& l1) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float y0, y1;
+    ffma2(y0, y1, __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), cs, cs, nref, nref);
+    float e0 = fast_exp2(y0), e1 = fast_exp2(y1);
+    if (!fast) {
+      if (c0 + 2 * i >= lim) e0 = 0.0f;
+      if (c0 + 2 * i + 1 >= lim) e1 = 0.0f;
+    }
+    fadd2(l0, l1, e0, e1);
+    w[i] = pack_f16x2(e0, e1);
+  }
+}
+
 template <int D, int GT>
 __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const PrefillParams p) {
   using G = PGeo<D>;
   extern __shared__ uint8_t psm_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(psm_raw) + 127) & ~uintptr_t(127));
   const uint32_t sb = smem_addr(base);
-  uint64_t* full = reinterpret_cast<uint64_t*>(base + G::kBars);
-  const uint32_t full0 = smem_addr(full), mma_bar = smem_addr(full + 2);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(full + 3);
-  int* abort = reinterpret_cast<int*>(tslot + 1);
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const uint32_t bars = sb + G::kBars;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(base + G::kBars + 8 * kNumBars);
+  volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qpb = kPRows / p.g;  // query tokens per CTA
   const int nqb = (p.chunk + qpb - 1) / qpb;
   const int qb = (int)(blockIdx.x % nqb);
   const int bh = (int)(blockIdx.x / nqb);
   const int h = bh % p.hkv, b = bh / p.hkv;
   const int32_t T = __ldg(p.lens + b);
-  // this thread's row: query token ti of the chunk, query head hh
+  // softmax threads: query token ti of the chunk, query head hh
   const int ti = qb * qpb + tid / p.g;
   const int hh = h * p.g + tid % p.g;
-  const bool row_ok = ti < p.chunk;
+  const bool row_ok = tid < kPRows && ti < p.chunk;
   float* orow = p.out + (((int64_t)b * p.chunk + ti) * p.hq + hh) * D;
   if (T < p.chunk) {  // the chunk's own tokens must be in the cache
     if (tid == 0) set_flag(p.flag, KVQ_FLAG_BAD_LENGTH);
@@ -214,14 +322,27 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
       for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
-  const int64_t pos_r = (int64_t)T - p.chunk + ti;  // last position this row attends
+  const int64_t pos_r = (int64_t)T - p.chunk + ti;     // last position this row attends
+  const int64_t pos_min = (int64_t)T - p.chunk + qb * qpb;  // ... the CTA's first query token
   const int last_ti = min(p.chunk, (qb + 1) * qpb) - 1;
   const int ntiles = (int)(((int64_t)T - p.chunk + last_ti) / kPTile) + 1;
 
   if (tid == 0) {
-    mbar_init(full0, 1);
-    mbar_init(full0 + 8, 1);
-    mbar_init(mma_bar, 1);
+    for (int i = 0; i < kFp4Stages; ++i) {
+      mbar_init(bars + 8 * (kBFp4Full + i), 1);
+      mbar_init(bars + 8 * (kBFp4Empty + i), 32 * kDeqWarps);
+    }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(bars + 8 * (kBKFull + i), 32 * kDeqWarps);
+      mbar_init(bars + 8 * (kBKEmpty + i), 1);
+      mbar_init(bars + 8 * (kBVFull + i), 32 * kDeqWarps);
+      mbar_init(bars + 8 * (kBVEmpty + i), 1);
+    }
+    for (int i = 0; i < kSBufs; ++i) {
+      mbar_init(bars + 8 * (kBSFull + i), 1);
+      mbar_init(bars + 8 * (kBPFull + i), 32 * kSoftWarps);
+      mbar_init(bars + 8 * (kBPvDone + i), 1);
+    }
     *abort = 0;
     fence_barrier_init();
   }
@@ -230,7 +351,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
   // query row -> f16 with a power-of-two prescale (exact for bf16 values in
   // range), into the A-operand layout; the factor returns in the score scale
   float cs = 0.0f;
-  {
+  if (warp < kSoftWarps) {
     float v[D];
     float amax = 0.0f;
     if (row_ok) {
@@ -266,167 +387,189 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
     }
     const float sk = p.k_gscale ? __ldg(p.k_gscale + h) : 1.0f;
     cs = p.qk_log2 * sk * __uint_as_float((uint32_t)(127 - k) << 23);
+    fence_async_smem();
   }
-  fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tslot);
-  const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
 
-  if (tid == 0) {
-    issue_tile<D, GT>(p, b, h, 0, T, sb + G::kStage, full0);
-    if (ntiles > 1) issue_tile<D, GT>(p, b, h, 1, T, sb + G::kStage + G::kTileBytes, full0 + 8);
-  }
-
-  float m_run = -INFINITY, l_run = 0.0f;
-  uint32_t mma_phase = 0;
-  bool ok = true;
-  for (int j = 0; j < ntiles && ok; ++j) {
-    const int s = j & 1;
-    const uint32_t stage = sb + G::kStage + s * G::kTileBytes;
-    ok = mbar_wait(full0 + 8 * s, (j >> 1) & 1);
-    ok = __syncthreads_and(ok);
-    if (!ok) break;
-    dequant_tile<D, GT>(stage, sb + G::kK, sb + G::kV, min((int64_t)kPTile, (int64_t)T - (int64_t)j * kPTile));
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();  // K^/V^ written; stage s consumed
-    tc_fence_after();
-    if (tid == 0) {
-      if (j + 2 < ntiles) issue_tile<D, GT>(p, b, h, j + 2, T, stage, full0 + 8 * s);
-      constexpr uint32_t kS = idesc_f16_f32(kPRows, kPTile);
+  if (warp < kSoftWarps) {
+    // ---------------------------------------------------------------- softmax
+    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lanes
+    float m_run = -INFINITY, l_run = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int buf = j % kSBufs;
+      if (!(ok = wwait(bars + 8 * (kBSFull + buf), (uint32_t)(j / kSBufs) & 1u, abort))) break;
+      tc_fence_after();
+      const uint32_t sp = t_row + (uint32_t)(buf * kPTile);
+      const int64_t p0 = (int64_t)j * kPTile;
+      const bool fast = p0 + kPTile - 1 <= pos_min;  // no position of the tile masked for any row
+      const int lim = row_ok ? (int)min((int64_t)kPTile, max((int64_t)0, pos_r - p0 + 1)) : 0;
+      // pass 1: the row's maximum over the tile (raw scores; cs > 0)
+      float mx = -INFINITY;
+      {
+        uint32_t v0[32], v1[32];
+        tmem_ld32_async(sp, v0);
+        tmem_ld32_async(sp + 32, v1);
+        tmem_wait_ld(v0);
+        tmem_wait_ld(v1);
+        mx = chunk_max(v1, fast, 32, lim, chunk_max(v0, fast, 0, lim, mx));
+        tmem_ld32_async(sp + 64, v0);
+        tmem_ld32_async(sp + 96, v1);
+        tmem_wait_ld(v0);
+        tmem_wait_ld(v1);
+        mx = chunk_max(v1, fast, 96, lim, chunk_max(v0, fast, 64, lim, mx));
+      }
+      const float mt = mx * cs;
+      // lazy reference: raised only when the tile passes it by the slack; O
+      // and l then shrink by 2^(old - new)
+      float al = 1.0f;
+      if (mt > m_run + kPSlack) {
+        if (m_run != -INFINITY) al = fast_exp2(m_run - mt);
+        m_run = mt;
+      }
+      if (__any_sync(0xFFFFFFFFu, al != 1.0f)) {  // TMEM accesses are warp-collective
+        if (!(ok = wwait(bars + 8 * (kBPvDone + (j - 1) % kSBufs), (uint32_t)((j - 1) / kSBufs) & 1u, abort)))
+          break;
+        tc_fence_after();
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks)
-        tc_mma_f16(tmem, smem_desc(sb + G::kQ + ks * 2 * (kPRows / 8) * 128, (kPRows / 8) * 128, 128),
-                   smem_desc(sb + G::kK + ks * 2 * (kPTile / 8) * 128, (kPTile / 8) * 128, 128), kS, ks > 0);
-      tc_commit(mma_bar);
-    }
-    ok = __syncthreads_and(mbar_wait(mma_bar, mma_phase & 1));
-    ++mma_phase;
-    tc_fence_after();
-    if (!ok) break;
-
-    // ---- softmax of row tid over this tile, in one pass against the running
-    // reference m_run; a row whose tile maximum passes it by the slack (and
-    // every row on its first tile) redoes the pass with the raised reference
-    const int64_t p0 = (int64_t)j * kPTile;
-    const bool all_in = row_ok && p0 + kPTile - 1 <= pos_r;  // no position of the tile masked
-    const bool none_in = !row_ok || p0 > pos_r;
-    float mt = -INFINITY, lt = 0.0f;
-    {
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(t_row + (uint32_t)(kOCol + c0), o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al);
+          tmem_st32_async(t_row + (uint32_t)(kOCol + c0), o);
+        }
+      }
+      l_run *= al;
+      // pass 2: P into the first 64 columns of the tile's S (two positions per
+      // column), each 64-column half after its scores have been read
       const float nref = m_run == -INFINITY ? 0.0f : -m_run;
+      float l0 = 0.0f, l1 = 0.0f;
 #pragma unroll
-      for (int c0 = 0; c0 < kPTile; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(t_row + (uint32_t)c0, v);
-        uint32_t f[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float xa = __uint_as_float(v[2 * i]) * cs, xb = __uint_as_float(v[2 * i + 1]) * cs;
-          if (!all_in) {
-            if (none_in || p0 + c0 + 2 * i > pos_r) xa = -INFINITY;
-            if (none_in || p0 + c0 + 2 * i + 1 > pos_r) xb = -INFINITY;
-          }
-          mt = fmaxf(mt, fmaxf(xa, xb));
-          const float pa = fast_exp2(xa + nref), pb = fast_exp2(xb + nref);
-          lt += pa + pb;
-          f[i] = pack_f16x2(pa, pb);
-        }
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8)
-          sts128(sb + G::kP + core_offset((uint32_t)tid, (uint32_t)(c0 + 8 * c8), kPRows),
-                 make_uint4(f[4 * c8], f[4 * c8 + 1], f[4 * c8 + 2], f[4 * c8 + 3]));
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t v0[32], v1[32], w[32];
+        tmem_ld32_async(sp + 64 * hf, v0);
+        tmem_ld32_async(sp + 64 * hf + 32, v1);
+        tmem_wait_ld(v0);
+        tmem_wait_ld(v1);
+        chunk_p(v0, w, fast, 64 * hf, lim, cs, nref, l0, l1);
+        chunk_p(v1, w + 16, fast, 64 * hf + 32, lim, cs, nref, l0, l1);
+        tmem_st32_async(sp + 32 * hf, w);
       }
+      tmem_wait_st();
+      l_run += l0 + l1;
+      tc_fence_before();
+      mbar_arrive(bars + 8 * (kBPFull + buf));
     }
-    const bool raise = row_ok && mt > m_run + kPSlack;
-    if (__any_sync(0xFFFFFFFFu, raise)) {
-      const float nref = -mt;
-#pragma unroll
-      for (int c0 = 0; c0 < kPTile; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(t_row + (uint32_t)c0, v);
-        if (raise) {
-          uint32_t f[16];
-          float l2 = 0.0f;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float xa = __uint_as_float(v[2 * i]) * cs, xb = __uint_as_float(v[2 * i + 1]) * cs;
-            if (!all_in) {
-              if (p0 + c0 + 2 * i > pos_r) xa = -INFINITY;
-              if (p0 + c0 + 2 * i + 1 > pos_r) xb = -INFINITY;
-            }
-            const float pa = fast_exp2(xa + nref), pb = fast_exp2(xb + nref);
-            l2 += pa + pb;
-            f[i] = pack_f16x2(pa, pb);
-          }
-          lt = c0 == 0 ? l2 : lt + l2;
-#pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8)
-            sts128(sb + G::kP + core_offset((uint32_t)tid, (uint32_t)(c0 + 8 * c8), kPRows),
-                   make_uint4(f[4 * c8], f[4 * c8 + 1], f[4 * c8 + 2], f[4 * c8 + 3]));
-        }
-      }
-    }
-    // rows that raised their reference: rescale l and their row of O (TMEM
-    // accesses are warp-collective; the other rows multiply by 1)
-    const float al = (raise && m_run != -INFINITY) ? fast_exp2(m_run - mt) : 1.0f;
-    if (__any_sync(0xFFFFFFFFu, al != 1.0f)) {
+    // O / l (times the NVFP4 value scale) once the last O += P V is done
+    if (ok) ok = wwait(bars + 8 * (kBPvDone + (ntiles - 1) % kSBufs), (uint32_t)((ntiles - 1) / kSBufs) & 1u, abort);
+    if (__all_sync(0xFFFFFFFFu, ok)) {
+      tc_fence_after();
+      const float vs = p.v_gscale ? __ldg(p.v_gscale + h) : 1.0f;
+      const float inv = l_run > 0.0f ? vs / l_run : 0.0f;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t o[32];
-        tmem_ld32(t_row + (uint32_t)(kPTile + c0), o);
+        tmem_ld32(t_row + (uint32_t)(kOCol + c0), o);
+        if (row_ok) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al);
-        tmem_st32(t_row + (uint32_t)(kPTile + c0), o);
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(orow + c0 + i) =
+                make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
+                            __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+        }
       }
     }
-    if (raise) {
-      l_run *= al;
-      m_run = mt;
+  } else if (warp < kSoftWarps + kDeqWarps) {
+    // ---------------------------------------------------------- dequantisation
+    const int dt = tid - 32 * kSoftWarps;
+    for (int j = 0; j < ntiles; ++j) {
+      const int s = j % kFp4Stages, slot = j % kRing;
+      const uint32_t stage = sb + G::kStage + s * G::kTileBytes;
+      const int valid = (int)min((int64_t)kPTile, (int64_t)T - (int64_t)j * kPTile);
+      if (!wwait(bars + 8 * (kBFp4Full + s), (uint32_t)(j / kFp4Stages) & 1u, abort)) break;
+      if (j >= kRing && !wwait(bars + 8 * (kBKEmpty + slot), (uint32_t)(j / kRing - 1) & 1u, abort)) break;
+      dequant_k<D, GT>(stage, sb + G::kK + slot * G::kOpBytes, valid, dt);
+      fence_async_smem();
+      mbar_arrive(bars + 8 * (kBKFull + slot));
+      if (j >= kRing && !wwait(bars + 8 * (kBVEmpty + slot), (uint32_t)(j / kRing - 1) & 1u, abort)) break;
+      dequant_v<D, GT>(stage, sb + G::kV + slot * G::kOpBytes, valid, dt);
+      mbar_arrive(bars + 8 * (kBFp4Empty + s));
+      fence_async_smem();
+      mbar_arrive(bars + 8 * (kBVFull + slot));
     }
-    l_run += lt;
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();  // P written; O rescales done
-    tc_fence_after();
-    if (tid == 0) {
-      constexpr uint32_t kO = idesc_f16_f32(kPRows, D);
-#pragma unroll
-      for (int ks = 0; ks < kPTile / 16; ++ks)
-        tc_mma_f16(tmem + kPTile, smem_desc(sb + G::kP + ks * 2 * (kPRows / 8) * 128, (kPRows / 8) * 128, 128),
-                   smem_desc(sb + G::kV + ks * 2 * (D / 8) * 128, (D / 8) * 128, 128), kO, j > 0 || ks > 0);
-      tc_commit(mma_bar);
-    }
-    ok = __syncthreads_and(mbar_wait(mma_bar, mma_phase & 1));
-    ++mma_phase;
-    tc_fence_after();
-  }
-  if (ok) {
-    const float vs = p.v_gscale ? __ldg(p.v_gscale + h) : 1.0f;
-    const float inv = l_run > 0.0f ? vs / l_run : 0.0f;
-#pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t o[32];
-      tmem_ld32(t_row + (uint32_t)(kPTile + c0), o);
-      if (row_ok) {
-#pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          *reinterpret_cast<float4*>(orow + c0 + i) =
-              make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
-                          __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+  } else if (warp == kLoadWarp) {
+    // ---------------------------------------------------------- bulk copies
+    if (lane == 0) {
+      int issued = 0;
+      for (int j = 0; j < ntiles; ++j) {
+        const int s = j % kFp4Stages;
+        if (j >= kFp4Stages && !pwait(bars + 8 * (kBFp4Empty + s), (uint32_t)(j / kFp4Stages - 1) & 1u, abort))
+          break;
+        issue_tile<D, GT>(p, b, h, j, T, sb + G::kStage + s * G::kTileBytes, bars + 8 * (kBFp4Full + s));
+        issued = j + 1;
+      }
+      if (*abort) {  // let copies still in flight land before the shared memory goes away
+        for (int j = max(0, issued - kFp4Stages); j < issued; ++j) {
+          const uint32_t bar = bars + 8 * (kBFp4Full + j % kFp4Stages);
+          const uint32_t par = (uint32_t)(j / kFp4Stages) & 1u;
+          const uint64_t t0 = global_ns();
+          while (!mbar_try_wait_hint(bar, par, kPollNs) && global_ns() - t0 < 20000000ull) {
+          }
+        }
       }
     }
-  } else {
-    if (tid == 0) {
-      set_flag(p.flag, KVQ_FLAG_TIMEOUT);
-      // let copies still in flight land before the CTA's shared memory goes away
-      for (int s = 0; s < 2; ++s) (void)mbar_try_wait_hint(full0 + 8 * s, 0u, 1000000u);
+  } else if (lane == 0) {
+    // ---------------------------------------------------------- tensor cores
+    constexpr uint32_t kIdS = idesc_f16_f32(kPRows, kPTile);
+    constexpr uint32_t kIdO = idesc_f16_f32(kPRows, D);
+    uint32_t last_bar = 0, last_par = 0;
+    for (int j = 0; j <= ntiles; ++j) {
+      if (j < ntiles) {  // S(j) = Q K^(j)^T into S buffer j % 3, once O += P V of tile j - 3 has freed it
+        const int slot = j % kRing, buf = j % kSBufs;
+        if (!pwait(bars + 8 * (kBKFull + slot), (uint32_t)(j / kRing) & 1u, abort)) break;
+        if (j >= kSBufs && !pwait(bars + 8 * (kBPvDone + buf), (uint32_t)(j / kSBufs - 1) & 1u, abort)) break;
+        tc_fence_after();
+        const uint32_t kaddr = sb + G::kK + slot * G::kOpBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          tc_mma_f16(tmem + (uint32_t)(buf * kPTile),
+                     smem_desc(sb + G::kQ + ks * 2 * (kPRows / 8) * 128, (kPRows / 8) * 128, 128),
+                     smem_desc(kaddr + ks * 2 * (kPTile / 8) * 128, (kPTile / 8) * 128, 128), kIdS, ks > 0);
+        tc_commit(bars + 8 * (kBSFull + buf));
+        tc_commit(bars + 8 * (kBKEmpty + slot));
+        last_bar = bars + 8 * (kBKEmpty + slot);
+        last_par = (uint32_t)(j / kRing) & 1u;
+      }
+      if (j >= 1) {  // O += P(j-1) V^(j-1), P from TMEM
+        const int jj = j - 1, slot = jj % kRing, buf = jj % kSBufs;
+        if (!pwait(bars + 8 * (kBPFull + buf), (uint32_t)(jj / kSBufs) & 1u, abort)) break;
+        if (!pwait(bars + 8 * (kBVFull + slot), (uint32_t)(jj / kRing) & 1u, abort)) break;
+        tc_fence_after();
+        const uint32_t vaddr = sb + G::kV + slot * G::kOpBytes;
+#pragma unroll
+        for (int ks = 0; ks < kPTile / 16; ++ks)
+          tc_mma_f16_ta(tmem + (uint32_t)kOCol, tmem + (uint32_t)(buf * kPTile + ks * 8),
+                        smem_desc(vaddr + ks * 2 * (D / 8) * 128, (D / 8) * 128, 128), kIdO, jj > 0 || ks > 0);
+        tc_commit(bars + 8 * (kBPvDone + buf));
+        tc_commit(bars + 8 * (kBVEmpty + slot));
+        last_bar = bars + 8 * (kBVEmpty + slot);
+        last_par = (uint32_t)(jj / kRing) & 1u;
+      }
+    }
+    if (*abort && last_bar != 0) {  // MMAs still running when the CTA gave up: let them finish
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait_hint(last_bar, last_par, kPollNs) && global_ns() - t0 < 20000000ull) {
+      }
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (tid == 0 && *abort) set_flag(p.flag, KVQ_FLAG_TIMEOUT);
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
