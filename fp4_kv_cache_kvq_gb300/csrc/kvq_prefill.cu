@@ -126,19 +126,24 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
-// (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1), one packed instruction
-__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
-                                      float c1) {
-  asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mov.b64 c, {%6, %7};\n"
-      " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}\n"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+// Packed pairs of fp32 (low word first) and their one-instruction arithmetic.
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};\n" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
 }
-__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1) {
-  asm("{\n .reg .b64 a, d;\n mov.b64 a, {%2, %3};\n mov.b64 d, {%0, %1};\n add.rn.f32x2 d, d, a;\n"
-      " mov.b64 {%0, %1}, d;\n}\n"
-      : "+f"(d0), "+f"(d1)
-      : "f"(a0), "f"(a1));
+__device__ __forceinline__ void f2unpack(uint64_t x, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;\n" : "=f"(lo), "=f"(hi) : "l"(x));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(r) : "l"(a), "l"(b));
+  return r;
 }
 
 // Issue the bulk copies of tile j (its groups that start before position T)
@@ -217,80 +222,81 @@ __device__ __forceinline__ void dequant_k(uint32_t stage, uint32_t kdst, int val
 }
 
 // V^ of one staged tile into its operand layout ([channel][position],
-// K-major over positions).  Item (4 channels c..c+3, 8 positions = 4
-// token-pair rows): a 4-byte code load per pair row (each byte pairs the
-// row's two positions), the pair's scales, one 16-byte store per channel.
+// K-major over positions).  Item (8 channels c..c+7, 8 positions = 4
+// token-pair rows): an 8-byte code load per pair row (each byte pairs the
+// row's two positions; the 8 channels share one 16-channel block scale), the
+// pair's scales, one 16-byte store per channel.
 template <int D, int GT>
 __device__ __forceinline__ void dequant_v(uint32_t stage, uint32_t vdst, int valid, int dt) {
   constexpr int NB = D / 16;
   constexpr int kGroupBytes = GT * 9 * D / 8;
-#pragma unroll 2
-  for (int it = dt; it < (D / 4) * (kPTile / 8); it += 32 * kDeqWarps) {
-    const int c = (it % (D / 4)) * 4;
-    const int kb = it / (D / 4);
-    const int n0 = kb * 8;
+#pragma unroll 1
+  for (int it = dt; it < (D / 8) * (kPTile / 8); it += 32 * kDeqWarps) {
+    const int c = (it % (D / 8)) * 8;
+    const int n0 = (it / (D / 8)) * 8;
+    const int i0 = (n0 % GT) >> 1;  // first pair row, a multiple of 4
     const uint32_t grp = stage + (uint32_t)((n0 / GT) * kGroupBytes);
-    uint32_t words[4], sc[4];
+    const uint32_t codes = grp + (uint32_t)(GT * (D / 2 + NB) + i0 * D);  // pair row i0
+    const uint32_t scales = grp + (uint32_t)(GT * (D + NB) + i0 * 2 * NB + 2 * (c >> 4));
+    // the 8 lanes of a store phase write channels 8t + k: rotating each
+    // thread's bytes by r = (c / 8) mod 8 spreads them over 8 bank groups
+    const uint32_t r = (uint32_t)(c >> 3) & 7u;
+    const uint32_t sh = 8u * (r & 3u);
+    uint32_t res[8][4];  // [rotated channel][pair]
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int n = n0 + 2 * q;  // even position of the pair
-      const int i = (n % GT) >> 1;
-      words[q] = 0u;
-      sc[q] = 0u;
+      uint32_t t[2][4];
+      uint32_t sc = 0u;
+      uint2 w = make_uint2(0u, 0u);
       if (n < valid) {
-        const int phys = (D == 64) ? 8 * ((c >> 3) ^ (((i >> 1) & 1) << 2)) + (c & 7)
-                                   : 16 * ((c >> 4) ^ ((i & 3) << 1)) + (c & 15);
-        words[q] = lds32(grp + (uint32_t)(GT * (D / 2 + NB) + i * D + phys));
-        uint32_t s2 = lds16(grp + (uint32_t)(GT * (D + NB) + i * 2 * NB + 2 * (c >> 4)));
+        // pair row i0 + q (i0 % 4 == 0): channel chunks permuted by the row index
+        const int phys = (D == 64) ? 8 * ((c >> 3) ^ (((q >> 1) & 1) << 2)) : 16 * ((c >> 4) ^ (q << 1)) + (c & 15);
+        w = lds64(codes + (uint32_t)(q * D + phys));
+        uint32_t s2 = lds16(scales + (uint32_t)(q * 2 * NB));
         if (n + 1 >= valid) s2 &= 0x00FFu;  // the pair's second position is past the end: scale 0
-        sc[q] = f16x2_from_e4m3x2(s2);
+        sc = f16x2_from_e4m3x2(s2);
       }
+      const uint32_t a = (r & 4u) ? w.y : w.x, bb = (r & 4u) ? w.x : w.y;
+      f16x2x4_from_e2m1x8(__funnelshift_r(a, bb, sh), t[0]);  // byte k -> channel c + (k + r) % 8
+      f16x2x4_from_e2m1x8(__funnelshift_r(bb, a, sh), t[1]);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) res[k][q] = hmul2_u32(t[k >> 2][k & 3], sc);
     }
-    // the 8 lanes of a store phase write channels 4t + cc: rotating each
-    // thread's byte order by (c / 8) mod 4 spreads them over 8 bank groups
-    const uint32_t rot = (uint32_t)(c >> 3) & 3u;
-    const uint32_t sel = (0x3210u + rot * 0x1111u) & 0x3333u;
-    uint32_t r[4][4];  // [rotated channel][pair]
+    const uint32_t row0 = vdst + core_offset((uint32_t)c, (uint32_t)n0, D);  // channel c; c % 8 == 0
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t t[4];
-      f16x2x4_from_e2m1x8(prmt(words[q], 0u, sel), t);  // t[cc]: channel c + (cc + rot) % 4, positions (n, n+1)
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) r[cc][q] = hmul2_u32(t[cc], sc[q]);
-    }
-#pragma unroll
-    for (int cc = 0; cc < 4; ++cc)
-      sts128(vdst + core_offset((uint32_t)c + ((cc + rot) & 3u), (uint32_t)n0, D),
-             make_uint4(r[cc][0], r[cc][1], r[cc][2], r[cc][3]));
+    for (int k = 0; k < 8; ++k)
+      sts128(row0 + (((uint32_t)k + r) & 7u) * 16u, make_uint4(res[k][0], res[k][1], res[k][2], res[k][3]));
   }
 }
 
-// Row max of 32 raw scores of a tile (positions >= lim masked when !fast).
-__device__ __forceinline__ float chunk_max(const uint32_t (&v)[32], bool fast, int c0, int lim, float m) {
+// Row max of 32 raw scores of a tile (positions >= lim masked when !fast),
+// into four independent running maxima.
+__device__ __forceinline__ void chunk_max(const uint32_t (&v)[32], bool fast, int c0, int lim, float (&m)[4]) {
   if (fast) {
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) m = fmax3(m, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+    for (int i = 0; i < 16; ++i) m[i & 3] = fmax3(m[i & 3], __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
   } else {
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-      if (c0 + i < lim) m = fmaxf(m, __uint_as_float(v[i]));
+      if (c0 + i < lim) m[i & 3] = fmaxf(m[i & 3], __uint_as_float(v[i]));
   }
-  return m;
 }
 
-// P = exp2(S * cs - m) for 32 scores, as 16 f16 pairs; adds the row sum.
-__device__ __forceinline__ void chunk_p(const uint32_t (&v)[32], uint32_t* w, bool fast, int c0, int lim, float cs,
-                                        float nref, float& l0, float& l1) {
+// P = 2^(S * cs - m) for 32 scores, as 16 f16 pairs; the row sum goes into
+// two packed running sums.
+__device__ __forceinline__ void chunk_p(const uint32_t (&v)[32], uint32_t* w, bool fast, int c0, int lim,
+                                        uint64_t cs2, uint64_t nref2, uint64_t (&l2)[2]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     float y0, y1;
-    ffma2(y0, y1, __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), cs, cs, nref, nref);
+    f2unpack(ffma2(f2pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), cs2, nref2), y0, y1);
     float e0 = fast_exp2(y0), e1 = fast_exp2(y1);
     if (!fast) {
       if (c0 + 2 * i >= lim) e0 = 0.0f;
       if (c0 + 2 * i + 1 >= lim) e1 = 0.0f;
     }
-    fadd2(l0, l1, e0, e1);
+    l2[i & 1] = fadd2(l2[i & 1], f2pack(e0, e1));
     w[i] = pack_f16x2(e0, e1);
   }
 }
@@ -352,37 +358,33 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
   // range), into the A-operand layout; the factor returns in the score scale
   float cs = 0.0f;
   if (warp < kSoftWarps) {
-    float v[D];
-    float amax = 0.0f;
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + (((int64_t)b * p.chunk + ti) * p.hq + hh) * D);
+    uint32_t amax_bits = 0u;  // |x| of the row's largest element (bf16 bits, upper half)
     if (row_ok) {
-      const uint16_t* src = p.q + (((int64_t)b * p.chunk + ti) * p.hq + hh) * D;
-#pragma unroll
+#pragma unroll 4
       for (int i = 0; i < D / 8; ++i) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4*>(src) + i);
+        const uint4 w = __ldg(src + i);
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          v[8 * i + 2 * k] = bf16_lo(ws[k]);
-          v[8 * i + 2 * k + 1] = bf16_hi(ws[k]);
-        }
+        for (int k = 0; k < 4; ++k)
+          amax_bits = max(amax_bits, max((ws[k] << 16) & 0x7FFF0000u, ws[k] & 0x7FFF0000u));
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < D; ++i) v[i] = 0.0f;
     }
-#pragma unroll
-    for (int i = 0; i < D; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const float amax = __uint_as_float(amax_bits);
     int k = 0;
     if (amax > 0.0f && amax <= 3.4e38f) {
-      const int e = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+      const int e = (int)((amax_bits >> 23) & 0xFF) - 127;
       k = min(100, max(-113, 14 - e));
     }
     const float up = __uint_as_float((uint32_t)(k + 127) << 23);
-#pragma unroll
+#pragma unroll 4
     for (int c8 = 0; c8 < D / 8; ++c8) {
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (row_ok) w = __ldg(src + c8);
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
       uint32_t f[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) f[j] = pack_f16x2(v[8 * c8 + 2 * j] * up, v[8 * c8 + 2 * j + 1] * up);
+      for (int j = 0; j < 4; ++j) f[j] = pack_f16x2(bf16_lo(ws[j]) * up, bf16_hi(ws[j]) * up);
       sts128(sb + G::kQ + core_offset((uint32_t)tid, (uint32_t)(c8 * 8), kPRows), make_uint4(f[0], f[1], f[2], f[3]));
     }
     const float sk = p.k_gscale ? __ldg(p.k_gscale + h) : 1.0f;
@@ -397,6 +399,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
   if (warp < kSoftWarps) {
     // ---------------------------------------------------------------- softmax
     const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lanes
+    const uint64_t cs2 = f2pack(cs, cs);
     float m_run = -INFINITY, l_run = 0.0f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
@@ -408,21 +411,23 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
       const bool fast = p0 + kPTile - 1 <= pos_min;  // no position of the tile masked for any row
       const int lim = row_ok ? (int)min((int64_t)kPTile, max((int64_t)0, pos_r - p0 + 1)) : 0;
       // pass 1: the row's maximum over the tile (raw scores; cs > 0)
-      float mx = -INFINITY;
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       {
         uint32_t v0[32], v1[32];
         tmem_ld32_async(sp, v0);
         tmem_ld32_async(sp + 32, v1);
         tmem_wait_ld(v0);
         tmem_wait_ld(v1);
-        mx = chunk_max(v1, fast, 32, lim, chunk_max(v0, fast, 0, lim, mx));
+        chunk_max(v0, fast, 0, lim, m4);
+        chunk_max(v1, fast, 32, lim, m4);
         tmem_ld32_async(sp + 64, v0);
         tmem_ld32_async(sp + 96, v1);
         tmem_wait_ld(v0);
         tmem_wait_ld(v1);
-        mx = chunk_max(v1, fast, 96, lim, chunk_max(v0, fast, 64, lim, mx));
+        chunk_max(v0, fast, 64, lim, m4);
+        chunk_max(v1, fast, 96, lim, m4);
       }
-      const float mt = mx * cs;
+      const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * cs;
       // lazy reference: raised only when the tile passes it by the slack; O
       // and l then shrink by 2^(old - new)
       float al = 1.0f;
@@ -445,22 +450,37 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
       }
       l_run *= al;
       // pass 2: P into the first 64 columns of the tile's S (two positions per
-      // column), each 64-column half after its scores have been read
+      // column); the 16 columns of P from scores [32k, 32k + 32) land on
+      // scores [16k, 16k + 16), already read
       const float nref = m_run == -INFINITY ? 0.0f : -m_run;
-      float l0 = 0.0f, l1 = 0.0f;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t v0[32], v1[32], w[32];
-        tmem_ld32_async(sp + 64 * hf, v0);
-        tmem_ld32_async(sp + 64 * hf + 32, v1);
+      const uint64_t nref2 = f2pack(nref, nref);
+      uint64_t l2[2] = {0ull, 0ull};
+      {
+        uint32_t v0[32], v1[32], w[16];
+        tmem_ld32_async(sp, v0);
         tmem_wait_ld(v0);
+        tmem_ld32_async(sp + 32, v1);
+        chunk_p(v0, w, fast, 0, lim, cs2, nref2, l2);
+        tmem_st16_async(sp, w);
         tmem_wait_ld(v1);
-        chunk_p(v0, w, fast, 64 * hf, lim, cs, nref, l0, l1);
-        chunk_p(v1, w + 16, fast, 64 * hf + 32, lim, cs, nref, l0, l1);
-        tmem_st32_async(sp + 32 * hf, w);
+        tmem_ld32_async(sp + 64, v0);
+        chunk_p(v1, w, fast, 32, lim, cs2, nref2, l2);
+        tmem_st16_async(sp + 16, w);
+        tmem_wait_ld(v0);
+        tmem_ld32_async(sp + 96, v1);
+        chunk_p(v0, w, fast, 64, lim, cs2, nref2, l2);
+        tmem_st16_async(sp + 32, w);
+        tmem_wait_ld(v1);
+        chunk_p(v1, w, fast, 96, lim, cs2, nref2, l2);
+        tmem_st16_async(sp + 48, w);
       }
       tmem_wait_st();
-      l_run += l0 + l1;
+      {
+        float a0, a1, b0, b1;
+        f2unpack(l2[0], a0, a1);
+        f2unpack(l2[1], b0, b1);
+        l_run += (a0 + a1) + (b0 + b1);
+      }
       tc_fence_before();
       mbar_arrive(bars + 8 * (kBPFull + buf));
     }
