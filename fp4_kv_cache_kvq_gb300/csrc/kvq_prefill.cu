@@ -42,17 +42,18 @@ namespace kvq {
 namespace {
 
 constexpr int kPTile = 128;     // cache positions per tile
-constexpr int kPRows = 128;     // query rows per CTA
-constexpr int kSoftWarps = 4;   // warps 0-3: softmax, thread = query row; also Q and the output
-constexpr int kDeqWarps = 4;    // warps 4-7: FP4 -> f16 dequantisation of K^ and V^
-constexpr int kLoadWarp = 8;    // lane 0: bulk copies of the FP4 tiles
-constexpr int kMmaWarp = 9;     // lane 0: tensor-core issue
+constexpr int kPRows = 128;     // rows of one query tile (the MMA's M)
+constexpr int kQTiles = 2;      // query tiles per CTA, sharing each dequantised K^/V^ tile
+constexpr int kCtaRows = kQTiles * kPRows;
+constexpr int kSoftWarps = 4 * kQTiles;  // warps 0-7: softmax, warpgroup X = query tile X, thread = row
+constexpr int kDeqWarps = 4;    // warps 8-11: FP4 -> f16 dequantisation of K^ and V^
+constexpr int kLoadWarp = kSoftWarps + kDeqWarps;  // lane 0: bulk copies of the FP4 tiles
+constexpr int kMmaWarp = kLoadWarp + 1;            // lane 0: tensor-core issue
 constexpr int kPThreads = 32 * (kMmaWarp + 1);
-constexpr int kSBufs = 3;       // S tiles in TMEM (128 columns each); P overwrites its S
-constexpr int kOCol = kSBufs * kPTile;  // O: TMEM columns [384, 384 + d)
+constexpr int kOCol = kQTiles * kPTile;  // TMEM: S_X (then P_X) at [128 X, +128), O_X at [256 + 128 X, +d)
 constexpr int kTmemCols = 512;
 constexpr int kFp4Stages = 3;   // FP4 tiles in flight
-constexpr int kRing = 2;        // K^ and V^ slots
+constexpr int kKSlots = 2;      // K^ slots (V^ has one)
 constexpr float kPSlack = 8.0f;
 constexpr uint32_t kPollNs = 20000;  // suspend hint of a barrier poll
 
@@ -60,14 +61,14 @@ constexpr uint32_t kPollNs = 20000;  // suspend hint of a barrier poll
 enum : int {
   kBFp4Full = 0,                        // [kFp4Stages] tile landed (bulk-copy bytes)
   kBFp4Empty = kBFp4Full + kFp4Stages,  // [kFp4Stages] dequantisers done with the tile (128 arrivals)
-  kBKFull = kBFp4Empty + kFp4Stages,    // [kRing] K^ slot written (128 arrivals)
-  kBKEmpty = kBKFull + kRing,           // [kRing] S = Q K^T done reading it (MMA commit)
-  kBVFull = kBKEmpty + kRing,           // [kRing] V^ slot written
-  kBVEmpty = kBVFull + kRing,           // [kRing] O += P V done reading it
-  kBSFull = kBVEmpty + kRing,           // [kSBufs] S in TMEM
-  kBPFull = kBSFull + kSBufs,           // [kSBufs] P in TMEM, O rescaled (128 arrivals)
-  kBPvDone = kBPFull + kSBufs,          // [kSBufs] O += P V done (P's TMEM free again)
-  kNumBars = kBPvDone + kSBufs
+  kBKFull = kBFp4Empty + kFp4Stages,    // [kKSlots] K^ slot written (128 arrivals)
+  kBKEmpty = kBKFull + kKSlots,         // [kKSlots] both S = Q K^T done reading it (MMA commit)
+  kBVFull = kBKEmpty + kKSlots,         // V^ written
+  kBVEmpty = kBVFull + 1,               // both O += P V done reading it
+  kBSFull = kBVEmpty + 1,               // [kQTiles] S_X in TMEM
+  kBPFull = kBSFull + kQTiles,          // [kQTiles] P_X in TMEM, O_X rescaled (128 arrivals)
+  kBPvDone = kBPFull + kQTiles,         // [kQTiles] O_X += P_X V done (S_X's TMEM free again)
+  kNumBars = kBPvDone + kQTiles
 };
 
 struct PrefillParams {
@@ -86,12 +87,12 @@ struct PrefillParams {
 
 template <int D>
 struct PGeo {
-  static constexpr int kTileBytes = kPTile * 9 * D / 8;  // FP4 bytes of 128 positions of one kv head
-  static constexpr int kOpBytes = kPTile * D * 2;        // Q, one K^ slot or one V^ slot (f16, core layout)
-  static constexpr int kQ = 0;                           // Q  [128 rows][D]
-  static constexpr int kK = kQ + kOpBytes;               // K^ [kRing][128 positions][D]
-  static constexpr int kV = kK + kRing * kOpBytes;       // V^ [kRing][D channels][128 positions]
-  static constexpr int kStage = kV + kRing * kOpBytes;   // FP4 tiles [kFp4Stages]
+  static constexpr int kTileBytes = kPTile * 9 * D / 8;   // FP4 bytes of 128 positions of one kv head
+  static constexpr int kOpBytes = kPTile * D * 2;         // one query tile, K^ slot or V^ (f16, core layout)
+  static constexpr int kQ = 0;                            // Q  [kQTiles][128 rows][D]
+  static constexpr int kK = kQ + kQTiles * kOpBytes;      // K^ [kKSlots][128 positions][D]
+  static constexpr int kV = kK + kKSlots * kOpBytes;      // V^ [D channels][128 positions]
+  static constexpr int kStage = kV + kOpBytes;            // FP4 tiles [kFp4Stages]
   static constexpr int kBars = kStage + kFp4Stages * kTileBytes;
   static constexpr int kUsed = kBars + 8 * kNumBars + 8 + 128;  // + TMEM slot, abort word, alignment slack
   // at least half an SM's shared memory, so that one CTA (holding all 512
@@ -311,16 +312,18 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
   uint32_t* tslot = reinterpret_cast<uint32_t*>(base + G::kBars + 8 * kNumBars);
   volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int qpb = kPRows / p.g;  // query tokens per CTA
+  const int qpb = kCtaRows / p.g;  // query tokens per CTA
   const int nqb = (p.chunk + qpb - 1) / qpb;
   const int qb = (int)(blockIdx.x % nqb);
   const int bh = (int)(blockIdx.x / nqb);
   const int h = bh % p.hkv, b = bh / p.hkv;
   const int32_t T = __ldg(p.lens + b);
-  // softmax threads: query token ti of the chunk, query head hh
+  // softmax threads: CTA row tid = query token ti of the chunk, query head hh;
+  // query tile X = tid / 128, row tid % 128 of it
   const int ti = qb * qpb + tid / p.g;
   const int hh = h * p.g + tid % p.g;
-  const bool row_ok = tid < kPRows && ti < p.chunk;
+  const int X = tid / kPRows;
+  const bool row_ok = tid < kCtaRows && ti < p.chunk;
   float* orow = p.out + (((int64_t)b * p.chunk + ti) * p.hq + hh) * D;
   if (T < p.chunk) {  // the chunk's own tokens must be in the cache
     if (tid == 0) set_flag(p.flag, KVQ_FLAG_BAD_LENGTH);
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
       for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(orow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
-  const int64_t pos_r = (int64_t)T - p.chunk + ti;     // last position this row attends
+  const int64_t pos_r = (int64_t)T - p.chunk + ti;          // last position this row attends
   const int64_t pos_min = (int64_t)T - p.chunk + qb * qpb;  // ... the CTA's first query token
   const int last_ti = min(p.chunk, (qb + 1) * qpb) - 1;
   const int ntiles = (int)(((int64_t)T - p.chunk + last_ti) / kPTile) + 1;
@@ -338,15 +341,15 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
       mbar_init(bars + 8 * (kBFp4Full + i), 1);
       mbar_init(bars + 8 * (kBFp4Empty + i), 32 * kDeqWarps);
     }
-    for (int i = 0; i < kRing; ++i) {
+    for (int i = 0; i < kKSlots; ++i) {
       mbar_init(bars + 8 * (kBKFull + i), 32 * kDeqWarps);
       mbar_init(bars + 8 * (kBKEmpty + i), 1);
-      mbar_init(bars + 8 * (kBVFull + i), 32 * kDeqWarps);
-      mbar_init(bars + 8 * (kBVEmpty + i), 1);
     }
-    for (int i = 0; i < kSBufs; ++i) {
+    mbar_init(bars + 8 * kBVFull, 32 * kDeqWarps);
+    mbar_init(bars + 8 * kBVEmpty, 1);
+    for (int i = 0; i < kQTiles; ++i) {
       mbar_init(bars + 8 * (kBSFull + i), 1);
-      mbar_init(bars + 8 * (kBPFull + i), 32 * kSoftWarps);
+      mbar_init(bars + 8 * (kBPFull + i), 32 * 4);
       mbar_init(bars + 8 * (kBPvDone + i), 1);
     }
     *abort = 0;
@@ -355,7 +358,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
   if (warp == 0) tmem_alloc(smem_addr(tslot), kTmemCols);
 
   // query row -> f16 with a power-of-two prescale (exact for bf16 values in
-  // range), into the A-operand layout; the factor returns in the score scale
+  // range), into the A-operand layout of its query tile; the factor returns in
+  // the score scale
   float cs = 0.0f;
   if (warp < kSoftWarps) {
     const uint4* src = reinterpret_cast<const uint4*>(p.q + (((int64_t)b * p.chunk + ti) * p.hq + hh) * D);
@@ -377,6 +381,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
       k = min(100, max(-113, 14 - e));
     }
     const float up = __uint_as_float((uint32_t)(k + 127) << 23);
+    const uint32_t qdst = sb + G::kQ + X * G::kOpBytes;
 #pragma unroll 4
     for (int c8 = 0; c8 < D / 8; ++c8) {
       uint4 w = make_uint4(0u, 0u, 0u, 0u);
@@ -385,7 +390,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
       uint32_t f[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) f[j] = pack_f16x2(bf16_lo(ws[j]) * up, bf16_hi(ws[j]) * up);
-      sts128(sb + G::kQ + core_offset((uint32_t)tid, (uint32_t)(c8 * 8), kPRows), make_uint4(f[0], f[1], f[2], f[3]));
+      sts128(qdst + core_offset((uint32_t)(tid % kPRows), (uint32_t)(c8 * 8), kPRows),
+             make_uint4(f[0], f[1], f[2], f[3]));
     }
     const float sk = p.k_gscale ? __ldg(p.k_gscale + h) : 1.0f;
     cs = p.qk_log2 * sk * __uint_as_float((uint32_t)(127 - k) << 23);
@@ -398,15 +404,18 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
 
   if (warp < kSoftWarps) {
     // ---------------------------------------------------------------- softmax
-    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's TMEM lanes
+    // this warp's 32 TMEM lanes (rows), in query tile X's S/P and O columns
+    const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t sp = t_lane + (uint32_t)(X * kPTile);
+    const uint32_t op = t_lane + (uint32_t)(kOCol + X * kPTile);
+    const uint32_t s_full = bars + 8 * (kBSFull + X), p_full = bars + 8 * (kBPFull + X);
+    const uint32_t pv_done = bars + 8 * (kBPvDone + X);
     const uint64_t cs2 = f2pack(cs, cs);
     float m_run = -INFINITY, l_run = 0.0f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
-      const int buf = j % kSBufs;
-      if (!(ok = wwait(bars + 8 * (kBSFull + buf), (uint32_t)(j / kSBufs) & 1u, abort))) break;
+      if (!(ok = wwait(s_full, (uint32_t)j & 1u, abort))) break;
       tc_fence_after();
-      const uint32_t sp = t_row + (uint32_t)(buf * kPTile);
       const int64_t p0 = (int64_t)j * kPTile;
       const bool fast = p0 + kPTile - 1 <= pos_min;  // no position of the tile masked for any row
       const int lim = row_ok ? (int)min((int64_t)kPTile, max((int64_t)0, pos_r - p0 + 1)) : 0;
@@ -436,20 +445,19 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
         m_run = mt;
       }
       if (__any_sync(0xFFFFFFFFu, al != 1.0f)) {  // TMEM accesses are warp-collective
-        if (!(ok = wwait(bars + 8 * (kBPvDone + (j - 1) % kSBufs), (uint32_t)((j - 1) / kSBufs) & 1u, abort)))
-          break;
+        if (!(ok = wwait(pv_done, (uint32_t)(j - 1) & 1u, abort))) break;
         tc_fence_after();
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t o[32];
-          tmem_ld32(t_row + (uint32_t)(kOCol + c0), o);
+          tmem_ld32(op + (uint32_t)c0, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al);
-          tmem_st32_async(t_row + (uint32_t)(kOCol + c0), o);
+          tmem_st32_async(op + (uint32_t)c0, o);
         }
       }
       l_run *= al;
-      // pass 2: P into the first 64 columns of the tile's S (two positions per
+      // pass 2: P into the first 64 columns of S_X (two positions per
       // column); the 16 columns of P from scores [32k, 32k + 32) land on
       // scores [16k, 16k + 16), already read
       const float nref = m_run == -INFINITY ? 0.0f : -m_run;
@@ -482,18 +490,18 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
         l_run += (a0 + a1) + (b0 + b1);
       }
       tc_fence_before();
-      mbar_arrive(bars + 8 * (kBPFull + buf));
+      mbar_arrive(p_full);
     }
-    // O / l (times the NVFP4 value scale) once the last O += P V is done
-    if (ok) ok = wwait(bars + 8 * (kBPvDone + (ntiles - 1) % kSBufs), (uint32_t)((ntiles - 1) / kSBufs) & 1u, abort);
-    if (__all_sync(0xFFFFFFFFu, ok)) {
+    // O / l (times the NVFP4 value scale) once the last O_X += P_X V is done
+    if (ok) ok = wwait(pv_done, (uint32_t)(ntiles - 1) & 1u, abort);
+    if (ok) {
       tc_fence_after();
       const float vs = p.v_gscale ? __ldg(p.v_gscale + h) : 1.0f;
       const float inv = l_run > 0.0f ? vs / l_run : 0.0f;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t o[32];
-        tmem_ld32(t_row + (uint32_t)(kOCol + c0), o);
+        tmem_ld32(op + (uint32_t)c0, o);
         if (row_ok) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4)
@@ -507,19 +515,19 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
     // ---------------------------------------------------------- dequantisation
     const int dt = tid - 32 * kSoftWarps;
     for (int j = 0; j < ntiles; ++j) {
-      const int s = j % kFp4Stages, slot = j % kRing;
+      const int s = j % kFp4Stages, slot = j % kKSlots;
       const uint32_t stage = sb + G::kStage + s * G::kTileBytes;
       const int valid = (int)min((int64_t)kPTile, (int64_t)T - (int64_t)j * kPTile);
       if (!wwait(bars + 8 * (kBFp4Full + s), (uint32_t)(j / kFp4Stages) & 1u, abort)) break;
-      if (j >= kRing && !wwait(bars + 8 * (kBKEmpty + slot), (uint32_t)(j / kRing - 1) & 1u, abort)) break;
+      if (j >= kKSlots && !wwait(bars + 8 * (kBKEmpty + slot), (uint32_t)(j / kKSlots - 1) & 1u, abort)) break;
       dequant_k<D, GT>(stage, sb + G::kK + slot * G::kOpBytes, valid, dt);
       fence_async_smem();
       mbar_arrive(bars + 8 * (kBKFull + slot));
-      if (j >= kRing && !wwait(bars + 8 * (kBVEmpty + slot), (uint32_t)(j / kRing - 1) & 1u, abort)) break;
-      dequant_v<D, GT>(stage, sb + G::kV + slot * G::kOpBytes, valid, dt);
+      if (j >= 1 && !wwait(bars + 8 * kBVEmpty, (uint32_t)(j - 1) & 1u, abort)) break;
+      dequant_v<D, GT>(stage, sb + G::kV, valid, dt);
       mbar_arrive(bars + 8 * (kBFp4Empty + s));
       fence_async_smem();
-      mbar_arrive(bars + 8 * (kBVFull + slot));
+      mbar_arrive(bars + 8 * kBVFull);
     }
   } else if (warp == kLoadWarp) {
     // ---------------------------------------------------------- bulk copies
@@ -544,41 +552,47 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
     }
   } else if (lane == 0) {
     // ---------------------------------------------------------- tensor cores
+    // per tile: S_A = Q_A K^T, S_B = Q_B K^T (each once O_X += P_X V of the
+    // previous tile has freed S_X), then O_A += P_A V^, O_B += P_B V^
     constexpr uint32_t kIdS = idesc_f16_f32(kPRows, kPTile);
     constexpr uint32_t kIdO = idesc_f16_f32(kPRows, D);
     uint32_t last_bar = 0, last_par = 0;
-    for (int j = 0; j <= ntiles; ++j) {
-      if (j < ntiles) {  // S(j) = Q K^(j)^T into S buffer j % 3, once O += P V of tile j - 3 has freed it
-        const int slot = j % kRing, buf = j % kSBufs;
-        if (!pwait(bars + 8 * (kBKFull + slot), (uint32_t)(j / kRing) & 1u, abort)) break;
-        if (j >= kSBufs && !pwait(bars + 8 * (kBPvDone + buf), (uint32_t)(j / kSBufs - 1) & 1u, abort)) break;
+    for (int j = 0; j < ntiles; ++j) {
+      const int slot = j % kKSlots;
+      if (!pwait(bars + 8 * (kBKFull + slot), (uint32_t)(j / kKSlots) & 1u, abort)) break;
+      const uint32_t kaddr = sb + G::kK + slot * G::kOpBytes;
+      bool ok = true;
+#pragma unroll
+      for (int x = 0; x < kQTiles; ++x) {
+        if (j >= 1 && !(ok = pwait(bars + 8 * (kBPvDone + x), (uint32_t)(j - 1) & 1u, abort))) break;
         tc_fence_after();
-        const uint32_t kaddr = sb + G::kK + slot * G::kOpBytes;
+        const uint32_t qaddr = sb + G::kQ + x * G::kOpBytes;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          tc_mma_f16(tmem + (uint32_t)(buf * kPTile),
-                     smem_desc(sb + G::kQ + ks * 2 * (kPRows / 8) * 128, (kPRows / 8) * 128, 128),
+          tc_mma_f16(tmem + (uint32_t)(x * kPTile),
+                     smem_desc(qaddr + ks * 2 * (kPRows / 8) * 128, (kPRows / 8) * 128, 128),
                      smem_desc(kaddr + ks * 2 * (kPTile / 8) * 128, (kPTile / 8) * 128, 128), kIdS, ks > 0);
-        tc_commit(bars + 8 * (kBSFull + buf));
-        tc_commit(bars + 8 * (kBKEmpty + slot));
-        last_bar = bars + 8 * (kBKEmpty + slot);
-        last_par = (uint32_t)(j / kRing) & 1u;
+        tc_commit(bars + 8 * (kBSFull + x));
+        last_bar = bars + 8 * (kBSFull + x);
+        last_par = (uint32_t)j & 1u;
       }
-      if (j >= 1) {  // O += P(j-1) V^(j-1), P from TMEM
-        const int jj = j - 1, slot = jj % kRing, buf = jj % kSBufs;
-        if (!pwait(bars + 8 * (kBPFull + buf), (uint32_t)(jj / kSBufs) & 1u, abort)) break;
-        if (!pwait(bars + 8 * (kBVFull + slot), (uint32_t)(jj / kRing) & 1u, abort)) break;
+      if (!ok) break;
+      tc_commit(bars + 8 * (kBKEmpty + slot));
+      if (!pwait(bars + 8 * kBVFull, (uint32_t)j & 1u, abort)) break;
+#pragma unroll
+      for (int x = 0; x < kQTiles; ++x) {
+        if (!(ok = pwait(bars + 8 * (kBPFull + x), (uint32_t)j & 1u, abort))) break;
         tc_fence_after();
-        const uint32_t vaddr = sb + G::kV + slot * G::kOpBytes;
 #pragma unroll
         for (int ks = 0; ks < kPTile / 16; ++ks)
-          tc_mma_f16_ta(tmem + (uint32_t)kOCol, tmem + (uint32_t)(buf * kPTile + ks * 8),
-                        smem_desc(vaddr + ks * 2 * (D / 8) * 128, (D / 8) * 128, 128), kIdO, jj > 0 || ks > 0);
-        tc_commit(bars + 8 * (kBPvDone + buf));
-        tc_commit(bars + 8 * (kBVEmpty + slot));
-        last_bar = bars + 8 * (kBVEmpty + slot);
-        last_par = (uint32_t)(jj / kRing) & 1u;
+          tc_mma_f16_ta(tmem + (uint32_t)(kOCol + x * kPTile), tmem + (uint32_t)(x * kPTile + ks * 8),
+                        smem_desc(sb + G::kV + ks * 2 * (D / 8) * 128, (D / 8) * 128, 128), kIdO, j > 0 || ks > 0);
+        tc_commit(bars + 8 * (kBPvDone + x));
+        last_bar = bars + 8 * (kBPvDone + x);
+        last_par = (uint32_t)j & 1u;
       }
+      if (!ok) break;
+      tc_commit(bars + 8 * kBVEmpty);
     }
     if (*abort && last_bar != 0) {  // MMAs still running when the CTA gave up: let them finish
       const uint64_t t0 = global_ns();
@@ -639,8 +653,8 @@ extern "C" kvq_status kvq_prefill_attn(const kvq_cache* cache, int32_t batch, in
   if (d_seq_lens == nullptr || q == nullptr || out == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
   if (!aligned_to(q, 16) || !aligned_to(out, 16)) return KVQ_ERR_INVALID_ARGUMENT;
   if (D != 64 && D != 128) return KVQ_ERR_UNSUPPORTED;
-  if (g > 8 || (kPRows % g) != 0) return KVQ_ERR_UNSUPPORTED;
-  const int64_t nqb = ((int64_t)chunk + kPRows / g - 1) / (kPRows / g);
+  if (g > 8 || (kCtaRows % g) != 0) return KVQ_ERR_UNSUPPORTED;
+  const int64_t nqb = ((int64_t)chunk + kCtaRows / g - 1) / (kCtaRows / g);
   const int64_t grid = nqb * batch * hkv;
   if (grid > 0x7FFFFFFF) return KVQ_ERR_UNSUPPORTED;
   PrefillParams pp;
