@@ -552,47 +552,56 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
     }
   } else if (lane == 0) {
     // ---------------------------------------------------------- tensor cores
-    // per tile: S_A = Q_A K^T, S_B = Q_B K^T (each once O_X += P_X V of the
-    // previous tile has freed S_X), then O_A += P_A V^, O_B += P_B V^
+    // order: S_A(0), S_B(0), then per tile j: O_A += P_A V^(j), S_A(j+1),
+    // O_B += P_B V^(j), S_B(j+1) -- each query tile's next scores follow its
+    // own O update (P_X lives in S_X's columns, so S_X(j+1) waits for that
+    // update to complete) and never wait for the other tile's softmax
     constexpr uint32_t kIdS = idesc_f16_f32(kPRows, kPTile);
     constexpr uint32_t kIdO = idesc_f16_f32(kPRows, D);
     uint32_t last_bar = 0, last_par = 0;
-    for (int j = 0; j < ntiles; ++j) {
-      const int slot = j % kKSlots;
-      if (!pwait(bars + 8 * (kBKFull + slot), (uint32_t)(j / kKSlots) & 1u, abort)) break;
-      const uint32_t kaddr = sb + G::kK + slot * G::kOpBytes;
-      bool ok = true;
+    auto issue_s = [&](int jj, int x) {
+      const uint64_t dq = smem_desc(sb + G::kQ + x * G::kOpBytes, (kPRows / 8) * 128, 128);
+      const uint64_t dk = smem_desc(sb + G::kK + (jj % kKSlots) * G::kOpBytes, (kPTile / 8) * 128, 128);
 #pragma unroll
-      for (int x = 0; x < kQTiles; ++x) {
-        if (j >= 1 && !(ok = pwait(bars + 8 * (kBPvDone + x), (uint32_t)(j - 1) & 1u, abort))) break;
-        tc_fence_after();
-        const uint32_t qaddr = sb + G::kQ + x * G::kOpBytes;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          tc_mma_f16(tmem + (uint32_t)(x * kPTile),
-                     smem_desc(qaddr + ks * 2 * (kPRows / 8) * 128, (kPRows / 8) * 128, 128),
-                     smem_desc(kaddr + ks * 2 * (kPTile / 8) * 128, (kPTile / 8) * 128, 128), kIdS, ks > 0);
-        tc_commit(bars + 8 * (kBSFull + x));
-        last_bar = bars + 8 * (kBSFull + x);
-        last_par = (uint32_t)j & 1u;
-      }
-      if (!ok) break;
-      tc_commit(bars + 8 * (kBKEmpty + slot));
-      if (!pwait(bars + 8 * kBVFull, (uint32_t)j & 1u, abort)) break;
+      for (int ks = 0; ks < D / 16; ++ks)
+        tc_mma_f16(tmem + (uint32_t)(x * kPTile), dq + (uint64_t)(ks * 2 * (kPRows / 8) * 8),
+                   dk + (uint64_t)(ks * 2 * (kPTile / 8) * 8), kIdS, ks > 0);
+      tc_commit(bars + 8 * (kBSFull + x));
+      last_bar = bars + 8 * (kBSFull + x);
+      last_par = (uint32_t)jj & 1u;
+    };
+    bool ok = pwait(bars + 8 * kBKFull, 0u, abort);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0, 0);
+      issue_s(0, 1);
+      tc_commit(bars + 8 * kBKEmpty);
+    }
+    for (int j = 0; j < ntiles && ok; ++j) {
+      if (!(ok = pwait(bars + 8 * kBVFull, (uint32_t)j & 1u, abort))) break;
 #pragma unroll
       for (int x = 0; x < kQTiles; ++x) {
         if (!(ok = pwait(bars + 8 * (kBPFull + x), (uint32_t)j & 1u, abort))) break;
         tc_fence_after();
+        const uint64_t dv = smem_desc(sb + G::kV, (D / 8) * 128, 128);
 #pragma unroll
         for (int ks = 0; ks < kPTile / 16; ++ks)
           tc_mma_f16_ta(tmem + (uint32_t)(kOCol + x * kPTile), tmem + (uint32_t)(x * kPTile + ks * 8),
-                        smem_desc(sb + G::kV + ks * 2 * (D / 8) * 128, (D / 8) * 128, 128), kIdO, j > 0 || ks > 0);
+                        dv + (uint64_t)(ks * 2 * (D / 8) * 8), kIdO, j > 0 || ks > 0);
         tc_commit(bars + 8 * (kBPvDone + x));
         last_bar = bars + 8 * (kBPvDone + x);
         last_par = (uint32_t)j & 1u;
+        if (x == kQTiles - 1) tc_commit(bars + 8 * kBVEmpty);
+        if (j + 1 < ntiles) {
+          const int jn = j + 1;
+          if (x == 0 && !(ok = pwait(bars + 8 * (kBKFull + jn % kKSlots), (uint32_t)(jn / kKSlots) & 1u, abort)))
+            break;
+          if (!(ok = pwait(bars + 8 * (kBPvDone + x), (uint32_t)j & 1u, abort))) break;
+          tc_fence_after();
+          issue_s(jn, x);
+          if (x == kQTiles - 1) tc_commit(bars + 8 * (kBKEmpty + jn % kKSlots));
+        }
       }
-      if (!ok) break;
-      tc_commit(bars + 8 * kBVEmpty);
     }
     if (*abort && last_bar != 0) {  // MMAs still running when the CTA gave up: let them finish
       const uint64_t t0 = global_ns();
