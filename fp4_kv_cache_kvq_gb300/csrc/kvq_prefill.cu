@@ -10,26 +10,29 @@
 // run on the tensor cores; the cache is dequantised once per tile into shared
 // memory and shared by the CTA's 128 query rows.
 //
-// CTA = the G query heads of one kv head times 128/G consecutive query tokens
-// of one sequence (128 query rows), ten warps in four roles that run as a
+// CTA = the G query heads of one kv head times 256/G consecutive query tokens
+// of one sequence: 256 query rows as two 128-row query tiles A and B that share
+// every dequantised cache tile.  Fourteen warps in four roles run as a
 // pipeline over the sequence's 128-position cache tiles:
-//   loader (1 thread)   bulk copies of the FP4 tiles, 3 in flight
-//   dequant (4 warps)   K^ [128 pos][d] and V^ [d][128 pos] into shared memory
-//                       in the tensor core's K-major core-matrix layout (f16,
-//                       E2M1 code times E4M3 scale; positions past the end 0),
-//                       2 slots each
-//   MMA (1 thread)      S(j) = Q K^(j)^T     tcgen05.mma M=128 N=128 K=d into
-//                                           one of 3 TMEM S buffers
-//                       O += P(j-1) V^(j-1) tcgen05.mma M=128 N=d K=128, P read
-//                                           from TMEM, O accumulated in TMEM
-//   softmax (4 warps)   thread r owns row r: the tile's row max from TMEM, the
-//                       lazy reference (raised only past +8 in the log2 domain;
-//                       O rescaled in TMEM then), causal mask on the diagonal
-//                       tiles only, P = 2^(S - m) as f16 pairs written back over
-//                       the first half of its S buffer
-// so the tensor cores compute S(j+1) and O += P(j-1) V while the softmax warps
-// work on tile j and the dequantisers on tile j+1.  mbarriers hand each buffer
-// from producer to consumer and back (MMA completions arrive via
+//   loader (1 thread)    bulk copies of the FP4 tiles, 3 in flight
+//   dequant (4 warps)    K^ [128 pos][d] (2 slots) and V^ [d][128 pos] (1 slot)
+//                        into shared memory in the tensor core's K-major
+//                        core-matrix layout (f16, E2M1 code times E4M3 scale;
+//                        positions past the end 0)
+//   MMA (1 thread)       S_X = Q_X K^T    tcgen05.mma M=128 N=128 K=d into TMEM
+//                        O_X += P_X V^    tcgen05.mma M=128 N=d K=128, P_X read
+//                                         from TMEM, O_X accumulated in TMEM
+//                        issued per tile as O_A, S_A(next), O_B, S_B(next), so
+//                        each query tile's next scores follow its own O update
+//   softmax (2 x 4 warps) thread r of warpgroup X owns row r of tile X: pass 1
+//                        the tile's row max from TMEM; the lazy reference is
+//                        raised only past +8 in the log2 domain (O_X, l rescaled
+//                        then); pass 2 P = 2^(S - m) as f16 pairs written back
+//                        over the first half of S_X; causal mask on the
+//                        diagonal tiles only
+// TMEM (512 columns): S_A, S_B, O_A, O_B, 128 columns each.  While one query
+// tile's softmax runs, the tensor cores work on the other tile.  mbarriers hand
+// each buffer from producer to consumer and back (MMA completions arrive via
 // tcgen05.commit).  Finally O / l (times the NVFP4 value scale) goes to global
 // memory.  Every wait is bounded; a timeout raises the CTA's abort word, every
 // role leaves its loop, copies and MMAs still in flight are waited for

@@ -243,8 +243,11 @@ kvq_status kvq_decode_attn_noalloc(const kvq_cache *global, const kvq_cache *swa
  * T_b - chunk + i and attends positions 0..T_b - chunk + i (causal), every
  * one dequantised from the cache.  ("Quantising the KV cache", section
  * "Code": the quantised K and V feed an unchanged attention.)  Runs on the
- * tensor cores: one CTA per 128 query rows (G query heads x 128/G tokens),
- * cache tiles of 128 positions dequantised once into shared memory.
+ * tensor cores: one CTA per 256 query rows (G query heads x 256/G tokens, as
+ * two 128-row tiles), cache tiles of 128 positions dequantised once into
+ * shared memory and shared by both.  Query values are used at f16 precision
+ * after an exact power-of-two rescale of each row; dequantised K and V are
+ * exact in f16; P is rounded to f16; accumulation is fp32.
  *   cache        FP4 or NVFP4 cache, head_dim 64 or 128.
  *   num_q_heads  Hq, a multiple of num_kv_heads with G = Hq/Hkv in {1,2,4,8}.
  *   d_seq_lens   device int32 [batch]: T_b >= chunk, the positions in the
