@@ -28,6 +28,11 @@ tests compare against:
   * ``decode_unit`` -- one (sequence, kv head) decode: FP4 for positions
     [0, T - W'), FP8 for the last W' = min(W, T) positions, one softmax over
     the union.
+  * ``swa_forward`` / ``exact_replay_start`` / ``bounded_replay_start`` -- a
+    toy multilayer sliding-window network and the two replays of its window
+    state ("Week 6 -- FP4 KV Caches and Bounded Replay", Core Concepts
+    "Bounded replay" and Lab: exact replay ~ L n_win tokens, bounded replay
+    the last n_win).
 
 Parity pins live in ``tests/test_oracle_*.py``.  Functions without a pin:
 none (see the tests' module docstrings).
@@ -114,6 +119,9 @@ def lib() -> ctypes.CDLL:
                 getattr(L, name).restype = ctypes.c_int64
                 getattr(L, name).argtypes = [_f32p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                              ctypes.c_int, _i8p, _u16p]
+            L.oq_swa_forward.restype = None
+            L.oq_swa_forward.argtypes = [_f64p, ctypes.c_int, ctypes.c_int, _f64p, ctypes.c_int64, ctypes.c_int,
+                                         _f64p, _f64p, _f64p, _f64p, _f64p, _f64p]
             L.oq_attend.restype = None
             L.oq_attend.argtypes = [_f64p, _f64p, _f64p, ctypes.c_int, ctypes.c_int64,
                                     ctypes.c_int, ctypes.c_double, _f64p, _f64p, _f64p, _f64p]
@@ -337,3 +345,42 @@ def decode_unit(q, k, v, scale: float, window: int = 0, swa_scales=None, nvfp4_s
     out, _, _ = attend(_f32(q), kh, vh, scale)
     vmax = float(np.abs(vh).max()) if T > 0 else 0.0
     return out, vmax
+
+
+# ---------------------------------------------------------------- replay
+def swa_forward(w, emb, n_win: int):
+    """Toy sliding-window network over the replayed positions (fp64).
+
+    w: (L, 4, d, d) -- Wq, Wk, Wv, Wo per layer; emb: (n, d), the inputs of
+    the n >= n_win replayed positions in order (position i of the replay
+    attends positions max(0, i - n_win + 1) .. i).  Returns (hidden (n, d),
+    states (L, 2, n_win, d)): the last layer's output and each layer's K and
+    V rows of the last n_win positions -- the window state a decoder keeps.
+    """
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    emb = np.ascontiguousarray(emb, dtype=np.float64)
+    L, four, d, d2 = w.shape
+    assert four == 4 and d == d2
+    n = emb.shape[0]
+    assert emb.shape == (n, d) and 1 <= n_win <= n
+    hidden = np.empty((n, d), np.float64)
+    states = np.empty((L, 2, n_win, d), np.float64)
+    x = np.empty((n, d), np.float64)
+    kb = np.empty((n, d), np.float64)
+    vb = np.empty((n, d), np.float64)
+    tmp = np.empty(3 * d + n_win, np.float64)
+    lib().oq_swa_forward(_p(w, _f64p), L, d, _p(emb, _f64p), n, int(n_win), _p(hidden, _f64p),
+                         _p(states, _f64p), _p(x, _f64p), _p(kb, _f64p), _p(vb, _f64p), _p(tmp, _f64p))
+    return hidden, states
+
+
+def exact_replay_start(T: int, layers: int, n_win: int) -> int:
+    """First position an exact replay of the window state after T positions
+    must start from: the top layer's window [T - n_win, T) reaches back
+    n_win - 1 positions per layer below it."""
+    return max(0, T - n_win - (layers - 1) * (n_win - 1))
+
+
+def bounded_replay_start(T: int, n_win: int) -> int:
+    """Bounded replay starts at the window: only the last n_win positions."""
+    return max(0, T - n_win)

@@ -531,3 +531,100 @@ void oq_attend(const double *q, const double *k, const double *v, int G, int64_t
             l_out[h] = l;
     }
 }
+
+/* ------------------------------------------------------------------ */
+/* Toy sliding-window network and its replay, fp64                     */
+/* ("Week 6 -- FP4 KV Caches and Bounded Replay", Overview, Core       */
+/* Concepts "Bounded replay", Lecture notes, Lab: exact replay costs   */
+/* ~ L n_win; bounded replay rebuilds the SWA state from only the last */
+/* n_win tokens)                                                       */
+/* ------------------------------------------------------------------ */
+
+/* The pages give no shapes; the toy is a reading: L layers, width d, one
+ * attention head per layer.  Layer l maps x to x' with, for each position i,
+ *   u_i  = x_i / sqrt(mean_c(x_i[c]^2) + 1e-6)         (RMS normalisation)
+ *   q_i  = Wq u_i,  k_i = Wk u_i,  v_i = Wv u_i
+ *   a_i  = sum_{s in win(i)} softmax_s(q_i . k_s / sqrt(d)) v_s
+ *   x'_i = x_i + Wo a_i
+ * with win(i) = positions max(0, i - n_win + 1) .. i of the replayed range.
+ * w holds L x 4 matrices (Wq, Wk, Wv, Wo), each d x d row-major: (W u)[r] =
+ * sum_c W[r*d + c] u[c].  emb: n x d, the inputs of the n replayed positions in
+ * order.  Outputs: hidden (n x d), the last layer's x; states (L x 2 x n_win x
+ * d), each layer's K then V rows of the last n_win positions (n >= n_win).
+ * Work: x, kb, vb (n x d each), tmp (3 d + n_win). */
+void oq_swa_forward(const double *w, int L, int d, const double *emb, int64_t n, int n_win, double *hidden,
+                    double *states, double *x, double *kb, double *vb, double *tmp)
+{
+    double *u = tmp, *q = tmp + d, *a = tmp + 2 * d, *sc = tmp + 3 * d;
+    const double scale = 1.0 / sqrt((double)d);
+    memcpy(x, emb, (size_t)(n * d) * sizeof(double));
+    for (int l = 0; l < L; l++) {
+        const double *Wq = w + (size_t)(4 * l + 0) * d * d, *Wk = w + (size_t)(4 * l + 1) * d * d;
+        const double *Wv = w + (size_t)(4 * l + 2) * d * d, *Wo = w + (size_t)(4 * l + 3) * d * d;
+        /* keys and values of every position, from the layer's input */
+        for (int64_t i = 0; i < n; i++) {
+            double ms = 0.0;
+            for (int c = 0; c < d; c++)
+                ms += x[i * d + c] * x[i * d + c];
+            const double r = 1.0 / sqrt(ms / d + 1e-6);
+            for (int c = 0; c < d; c++)
+                u[c] = x[i * d + c] * r;
+            for (int o = 0; o < d; o++) {
+                double sk = 0.0, sv = 0.0;
+                for (int c = 0; c < d; c++) {
+                    sk += Wk[o * d + c] * u[c];
+                    sv += Wv[o * d + c] * u[c];
+                }
+                kb[i * d + o] = sk;
+                vb[i * d + o] = sv;
+            }
+        }
+        /* attention over each position's window, then the residual update
+         * (x_i is read for q_i before it is overwritten; keys and values of
+         * all positions were taken above from the layer input) */
+        for (int64_t i = 0; i < n; i++) {
+            double ms = 0.0;
+            for (int c = 0; c < d; c++)
+                ms += x[i * d + c] * x[i * d + c];
+            const double r = 1.0 / sqrt(ms / d + 1e-6);
+            for (int c = 0; c < d; c++)
+                u[c] = x[i * d + c] * r;
+            for (int o = 0; o < d; o++) {
+                double s = 0.0;
+                for (int c = 0; c < d; c++)
+                    s += Wq[o * d + c] * u[c];
+                q[o] = s;
+            }
+            const int64_t s0 = i - n_win + 1 > 0 ? i - n_win + 1 : 0;
+            double mx = -INFINITY, den = 0.0;
+            for (int64_t s = s0; s <= i; s++) {
+                double dot = 0.0;
+                for (int c = 0; c < d; c++)
+                    dot += q[c] * kb[s * d + c];
+                sc[s - s0] = dot * scale;
+                if (sc[s - s0] > mx)
+                    mx = sc[s - s0];
+            }
+            for (int c = 0; c < d; c++)
+                a[c] = 0.0;
+            for (int64_t s = s0; s <= i; s++) {
+                const double p = exp(sc[s - s0] - mx);
+                den += p;
+                for (int c = 0; c < d; c++)
+                    a[c] += p * vb[s * d + c];
+            }
+            for (int o = 0; o < d; o++) {
+                double y = 0.0;
+                for (int c = 0; c < d; c++)
+                    y += Wo[o * d + c] * (a[c] / den);
+                x[i * d + o] += y;
+            }
+        }
+        for (int64_t j = 0; j < n_win; j++)
+            for (int c = 0; c < d; c++) {
+                states[(((size_t)l * 2 + 0) * n_win + j) * d + c] = kb[(n - n_win + j) * d + c];
+                states[(((size_t)l * 2 + 1) * n_win + j) * d + c] = vb[(n - n_win + j) * d + c];
+            }
+    }
+    memcpy(hidden, x, (size_t)(n * d) * sizeof(double));
+}
