@@ -574,7 +574,7 @@ def run_prefill_attn(args, dist: Dist):
         "config": {"workload": f"prefill_attn: {w.description}" + (", NVFP4 cache" if nv else ""),
                    "format": args.format, "batch": B, "context": T, "chunk": C, "kv_heads": w.num_kv_heads,
                    "q_heads": w.num_q_heads, "head_dim": w.head_dim, "page_size": w.page_size,
-                   "l2": "each kv head's cache (2.36 MB) is read by the 64 query-block CTAs of its chunk; no flush",
+                   "l2": "each kv head's cache (2.36 MB) is read by the 32 query-block CTAs of its chunk; no flush",
                    "parallelism": f"replicas x{dist.world}"},
         "roofline": {"bound": "tensor", "kernel": "prefill_fp4_kernel (tcgen05.mma f16, TMEM accumulators)",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
@@ -586,6 +586,147 @@ def run_prefill_attn(args, dist: Dist):
     }
     if clk is not None:
         res["clocks"] = clk
+    return res
+
+
+SWA_REPLAY_METRIC = ("bounded SWA replay of a toy 8-layer sliding-window network (d 128, window 512): "
+                     "replayed layer-positions/s, 1xGB300")
+
+
+def run_swa_replay(args, dist: Dist):
+    """A step is one bounded replay: the last n_win = 512 positions before
+    position T = 65536 through all 8 layers of the toy sliding-window network
+    (d 128), rebuilding every layer's window state.  value = layers x
+    positions replayed per second.  The exact replay (from the receptive-field
+    start, 4089 positions) is timed beside it, and the bounded replay's error
+    against it is reported: each layer's state, and the output at position T
+    computed from each state."""
+    from fp4_kv_cache_kvq_gb300 import build, kvq
+    device = torch.device("cuda", dist.local)
+    torch.cuda.set_device(device)
+    build.build()
+    R = workloads.REPLAY
+    L, d, nw, T = R["layers"], R["d"], R["n_win"], R["T"]
+    t_exact = max(0, T - nw - (L - 1) * (nw - 1))
+    t_bound = T - nw
+    w = workloads.replay_net(L, d, seed=args.seed).to(device)
+    emb = workloads.replay_inputs(t_exact, T + 1 - t_exact, d, seed=args.seed).to(device)  # through position T
+    e_x = emb[:T - t_exact].contiguous()
+    e_b = emb[t_bound - t_exact:T - t_exact].contiguous()
+    ws = torch.empty(kvq.load().kvq_swa_replay_workspace_bytes(L, T + 1 - t_exact, d), dtype=torch.uint8,
+                     device=device)
+    states = torch.empty((L, 2, nw, d), dtype=torch.float32, device=device)
+    # quality of the bounded state against the exact one
+    sx, _ = kvq.swa_replay(w, e_x, nw, want_hidden=False, workspace=ws)
+    sx = sx.clone()
+    sb, _ = kvq.swa_replay(w, e_b, nw, want_hidden=False, workspace=ws)
+    sb = sb.clone()
+    _, hx = kvq.swa_replay(w, emb, nw, workspace=ws)
+    hx = hx[-1].clone()
+    _, hb = kvq.swa_replay(w, emb[t_bound - t_exact:].contiguous(), nw, workspace=ws)
+    hb = hb[-1].clone()
+    torch.cuda.synchronize()
+    state_err = [float((sb[l] - sx[l]).abs().max() / sx[l].abs().max()) for l in range(L)]
+    next_err = float((hb - hx).norm() / hx.norm())
+    K, Wm = args.steps, args.warmup
+    # quality against compute: replays that start m positions before the
+    # window, from bounded (m = 0) up to exact (m = (L - 1)(n_win - 1))
+    curve = []
+    for m in sorted({0, nw // 4, nw // 2, nw, 2 * nw, 4 * nw, (L - 1) * (nw - 1)}):
+        if m > (L - 1) * (nw - 1):
+            continue
+        t0 = T - nw - m
+        sm, _ = kvq.swa_replay(w, emb[t0 - t_exact:T - t_exact].contiguous(), nw, want_hidden=False, workspace=ws)
+        top = float((sm[L - 1] - sx[L - 1]).abs().max() / sx[L - 1].abs().max())
+        _, hm = kvq.swa_replay(w, emb[t0 - t_exact:].contiguous(), nw, workspace=ws)
+        nxt = float((hm[-1] - hx).norm() / hx.norm())
+        e_m = emb[t0 - t_exact:T - t_exact].contiguous()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(10):
+            kvq.swa_replay(w, e_m, nw, want_hidden=False, workspace=ws, states=states)
+        b.record()
+        torch.cuda.synchronize()
+        curve.append({"replayed_positions": nw + m, "ms": a.elapsed_time(b) / 10,
+                      "top_state_rel_err": top, "next_output_rel_err": nxt})
+
+    def timed(e, n_steps):
+        for _ in range(Wm):
+            kvq.swa_replay(w, e, nw, want_hidden=False, workspace=ws, states=states)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n_steps):
+            kvq.swa_replay(w, e, nw, want_hidden=False, workspace=ws, states=states)
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3
+
+    ke = min(K, 50)
+    secs_exact = timed(e_x, ke)
+    clocks = ClockSampler(device.index)
+    dist.barrier()
+    secs = timed(e_b, K)
+    dist.barrier()
+    clk = clocks.stop()
+    value, max_s = combine_ranks(dist, L * nw * K, secs)
+    # algorithmic fp32 work of one bounded replay: 4 d x d projections per
+    # position and layer (2 d^2 flop each), 4 d flop per (position, window
+    # position) for the scores and the weighted sum
+    attended = sum(min(i + 1, nw) for i in range(nw))
+    flops = L * (nw * 4 * 2 * d * d + attended * 4 * d)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    max_mhz = (clk or {}).get("sm_max_mhz") or 2070.0
+    peak = sms * 128 * 2 * max_mhz * 1e6 / 1e12  # fp32 FMA lanes x 2 flop x clock
+    achieved = flops * K / secs / 1e12
+    # end to end: the window's inputs in from pinned host memory, the state back
+    eh = e_b.cpu().pin_memory()
+    sh = torch.empty(states.shape, dtype=torch.float32).pin_memory()
+    Ke = min(K, 20)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(Ke):
+        e_b.copy_(eh, non_blocking=True)
+        kvq.swa_replay(w, e_b, nw, want_hidden=False, workspace=ws, states=states)
+        sh.copy_(states, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    e2e, _ = combine_ranks(dist, L * nw * Ke, a.elapsed_time(b) / 1e3)
+    res = {
+        "metric": SWA_REPLAY_METRIC, "value": value, "unit": "layer-positions/s", "n_gpus": dist.world, "steps": K,
+        "warmup": Wm, "ms_per_step": max_s * 1e3 / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"swa_replay: toy network L{L} d{d}, window {nw}, state after {T} positions; "
+                               f"bounded replay {nw} positions, exact replay {T - t_exact}",
+                   "layers": L, "d": d, "n_win": nw, "T": T,
+                   "exact_replay_ms": secs_exact * 1e3 / ke,
+                   "bounded_replay_ms": secs * 1e3 / K,
+                   "compute_saved": (secs_exact / ke) / (secs / K),
+                   "bounded_state_rel_err_per_layer": state_err,
+                   "bounded_next_output_rel_err": next_err,
+                   "quality_vs_replay_length": curve,
+                   "l2": "all operands (under 10 MB) stay in L2; no flush (latency-bound toy)",
+                   "parallelism": f"replicas x{dist.world}"},
+        "roofline": {"bound": "alu", "kernel": "one kvq_swa_replay call (swa_proj_kernel + swa_attn_kernel per layer)",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"fp32 FMA: {sms} SMs x 128 lanes x 2 flop x {max_mhz:.0f} MHz (derived)",
+                     "traffic": None, "algorithmic_flops_per_launch": flops},
+        "e2e": {"value": e2e, "unit": "layer-positions/s", "h2d_bytes_per_step": e_b.numel() * 4,
+                "d2h_bytes_per_step": states.numel() * 4, "steps": Ke},
+        "gpu_launches": K * (1 + 2 * L),
+    }
+    if clk is not None:
+        res["clocks"] = clk
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        import oracle
+        wn, en = w.cpu().double().numpy(), e_b.cpu().double().numpy()
+        t = time.perf_counter()
+        oracle.swa_forward(wn, en, nw)
+        dt = time.perf_counter() - t
+        res["cpu_baseline"] = {"value": L * nw / dt, "unit": "layer-positions/s", "cores": 1, "kind": "oracle",
+                               "sample": f"one bounded replay ({nw} positions x {L} layers), fp64 C, one thread"}
     return res
 
 
@@ -657,10 +798,41 @@ def cpu_baseline(w, seed, st=None, budget_s=20.0, nvfp4=False):
                       f"dequantise + fp64 attention, {cores} threads, {secs:.1f} s"}
 
 
+def run_reference_replay(args):
+    """The oracle's bounded replay of the swa_replay workload, one per step
+    (about a second each in fp64 C), capped at 5 timed steps."""
+    import oracle
+    R = workloads.REPLAY
+    L, d, nw, T = R["layers"], R["d"], R["n_win"], R["T"]
+    wn = workloads.replay_net(L, d, seed=args.seed).double().numpy()
+    en = workloads.replay_inputs(T - nw, nw, d, seed=args.seed).double().numpy()
+    steps = min(args.steps, 5)
+    for _ in range(min(args.warmup, 3)):
+        oracle.swa_forward(wn, en, nw)
+    t = time.perf_counter()
+    for _ in range(steps):
+        oracle.swa_forward(wn, en, nw)
+    secs = time.perf_counter() - t
+    value = L * nw * steps / secs
+    unit = "layer-positions/s"
+    return {
+        "impl": "reference", "metric": SWA_REPLAY_METRIC, "value": value, "unit": unit, "n_gpus": 1,
+        "steps": steps, "warmup": min(args.warmup, 3), "ms_per_step": secs * 1e3 / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"swa_replay: toy network L{L} d{d}, window {nw}; bounded replay of {nw} positions",
+                   "parallelism": "one host thread"},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+                         "sample": f"one bounded replay ({nw} positions x {L} layers) per step, fp64 C"},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args, dist: Dist):
-    w = workloads.WORKLOADS[args.workload]
     if dist.rank != 0:
         return None
+    if args.workload == "swa_replay":
+        return run_reference_replay(args)
+    w = workloads.WORKLOADS[args.workload]
     cores = os.cpu_count() or 1
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     # size each step so the whole warm-up + timed run stays around a minute
@@ -704,7 +876,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
     ap.add_argument("--workload", default="long_context",
                     choices=["long_context", "gqa_outliers", "paged_ragged", "swa_append", "tiny", "prefill",
-                             "prefill_attn"])
+                             "prefill_attn", "swa_replay"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--format", choices=["fp4", "nvfp4"], default="fp4",
                     help="cache format: FP4 (E4M3 scale per 16) or NVFP4 (plus an fp32 scale per kv head)")
@@ -723,6 +895,8 @@ def main(argv=None):
             res = run_prefill(args, dist)
         elif args.workload == "prefill_attn":
             res = run_prefill_attn(args, dist)
+        elif args.workload == "swa_replay":
+            res = run_swa_replay(args, dist)
         else:
             res = run_gpu(args, dist)
         if dist.rank == 0 and res is not None:

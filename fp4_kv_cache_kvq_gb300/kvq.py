@@ -96,6 +96,11 @@ def load() -> ctypes.CDLL:
             L.kvq_fake_quant.argtypes = [ctypes.c_int32] * 6 + [_P] * 6
             L.kvq_attn_dense.restype = ctypes.c_int
             L.kvq_attn_dense.argtypes = [ctypes.c_int32] * 5 + [_P, _P, _P, ctypes.c_float, _P, _P, _P]
+            L.kvq_swa_replay_workspace_bytes.restype = ctypes.c_size_t
+            L.kvq_swa_replay_workspace_bytes.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int32]
+            L.kvq_swa_replay.restype = ctypes.c_int
+            L.kvq_swa_replay.argtypes = [_P, ctypes.c_int32, ctypes.c_int32, _P, ctypes.c_int64, ctypes.c_int32,
+                                         _P, _P, _P, ctypes.c_size_t, _P]
             L.kvq_fp4_pool_bytes.restype = ctypes.c_size_t
             L.kvq_fp4_pool_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
             _lib = L
@@ -267,6 +272,30 @@ def prefill_attn(cache: Fp4Cache, seq_lens: torch.Tensor, q: torch.Tensor, softm
                                  _ptr(out), _ptr(err), _stream(stream))
     _check(st, "kvq_prefill_attn")
     return out
+
+
+def swa_replay(w: torch.Tensor, emb: torch.Tensor, n_win: int, want_hidden: bool = True,
+               workspace: Optional[torch.Tensor] = None, states: Optional[torch.Tensor] = None, stream=None):
+    """kvq_swa_replay: the toy sliding-window network over the positions whose
+    inputs are emb (float32 [n][d]) with weights w (float32 [L][4][d][d]:
+    Wq, Wk, Wv, Wo).  Returns (states float32 [L][2][n_win][d] -- each
+    layer's K then V rows of the last n_win positions --, hidden float32
+    [n][d] or None)."""
+    _need(w, torch.float32, "w")
+    _need(emb, torch.float32, "emb")
+    L, four, d, _ = w.shape
+    n = emb.shape[0]
+    if states is None:
+        states = torch.empty((L, 2, n_win, d), dtype=torch.float32, device=emb.device)
+    _need(states, torch.float32, "states")
+    hidden = torch.empty((n, d), dtype=torch.float32, device=emb.device) if want_hidden else None
+    need = load().kvq_swa_replay_workspace_bytes(L, n, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=emb.device)
+    st = load().kvq_swa_replay(_ptr(w), L, d, _ptr(emb), n, int(n_win), _ptr(states), _ptr(hidden), _ptr(workspace),
+                               workspace.numel(), _stream(stream))
+    _check(st, "kvq_swa_replay")
+    return states, hidden
 
 
 def dequant(cache, seq_lens: Optional[torch.Tensor], max_len: int, dtype: torch.dtype = torch.float32,

@@ -22,6 +22,12 @@ Workloads (one layer each):
   prefill_attn   B4, Hkv8, Hq64 (G8), d128: the last 1024 of 16384 cached
                  positions are a chunk of new queries attending causally.
 
+Toy sliding-window network for the replay experiment (``replay_net`` /
+``replay_inputs``): L layers of four d x d matrices drawn N(0, 1/d) (weights of
+unit gain on RMS-normalised inputs), position inputs N(0, 1).  ``REPLAY`` is
+the benchmark's configuration: L = 8, d = 128, window 512, state after 65536
+positions.
+
 Draw order per sequence b: K then V (then the i.i.d. outlier mask), from a
 generator seeded with (seed, b), so any subset of sequences can be redrawn.
 Queries and per-step tokens use their own seeded generators.
@@ -152,3 +158,31 @@ def scaled(w: Workload, **changes) -> Workload:
     d = dict(w.__dict__)
     d.update(changes)
     return Workload(**d)
+
+
+# ------------------------------------------------------------ replay toy
+REPLAY = {"layers": 8, "d": 128, "n_win": 512, "T": 65536}
+
+
+def replay_net(layers: int, d: int, seed: int = 0, device="cpu") -> torch.Tensor:
+    """Weights of the toy network: float32 [layers][4][d][d] (Wq, Wk, Wv, Wo),
+    N(0, 1/d)."""
+    g = _gen(device, seed * _MIX + 31)
+    return torch.randn((layers, 4, d, d), generator=g, device=device) * (1.0 / d ** 0.5)
+
+
+def replay_inputs(first: int, n: int, d: int, seed: int = 0, device="cpu") -> torch.Tensor:
+    """Inputs of positions first .. first + n - 1 of one synthetic sequence:
+    float32 [n][d], N(0, 1); position p's row does not depend on the range
+    drawn (each row from its own seeded generator chunk of 1024 positions)."""
+    out = torch.empty((n, d), dtype=torch.float32, device=device)
+    p = first
+    while p < first + n:
+        blk = p // 1024
+        g = _gen(device, (seed * _MIX + 47) * 1_000_003 + blk)
+        rows = torch.randn((1024, d), generator=g, device=device)
+        lo = p - blk * 1024
+        take = min(1024 - lo, first + n - p)
+        out[p - first:p - first + take] = rows[lo:lo + take]
+        p += take
+    return out

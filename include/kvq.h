@@ -343,6 +343,39 @@ kvq_status kvq_attn_dense(int32_t batch, int32_t tokens, int32_t num_q_heads, in
                           int32_t head_dim, const void *q, const float *k, const float *v,
                           float softmax_scale, float *out, int32_t *top, kvq_stream stream);
 
+/*
+ * kvq_swa_replay_workspace_bytes / kvq_swa_replay -- replay of a toy
+ * multilayer sliding-window (SWA) network over a range of positions,
+ * rebuilding each layer's window state: the K and V rows of the last n_win
+ * positions.  ("Week 6 -- FP4 KV Caches and Bounded Replay", Core Concepts
+ * "Bounded replay" and Lab: an exact replay reaches back about L n_win
+ * positions -- precisely n_win + (L - 1)(n_win - 1) -- while a bounded replay
+ * starts only n_win back.)  The pages give the toy no shapes; it is: L layers
+ * of width d, one head each; per position i of the replayed range
+ *   u = x_i / sqrt(mean(x_i^2) + 1e-6),  q, k, v = Wq u, Wk u, Wv u
+ *   a_i = sum over s = max(0, i - n_win + 1) .. i of
+ *         softmax_s(q_i . k_s / sqrt(d)) v_s,   x_i += Wo a_i
+ * with every layer's k, v, q taken from that layer's input.
+ *   w          device float [layers][4][d][d], row-major Wq, Wk, Wv, Wo
+ *              ((W u)[r] = sum_c W[r][c] u[c]).
+ *   emb        device float [n][d]: the inputs of the n replayed positions.
+ *   states     device float [layers][2][n_win][d]: out, each layer's K rows
+ *              then V rows of positions n - n_win .. n - 1.
+ *   hidden     device float [n][d] or NULL: out, the last layer's x.
+ *   workspace  device, at least kvq_swa_replay_workspace_bytes(layers, n, d)
+ *              bytes, 16-byte aligned, owned by the caller.
+ * d is 64 or 128; 1 <= n_win <= min(n, 4096); layers >= 1.  fp32 arithmetic.
+ * A position's result depends only on the inputs of its window (in a fixed
+ * order), so a replay that starts at the exact start reproduces the state of
+ * a forward pass over the whole sequence bit for bit.
+ * Host errors: INVALID_ARGUMENT (pointers, sizes, alignment), WORKSPACE
+ * (too small).  No device flags.
+ */
+size_t kvq_swa_replay_workspace_bytes(int32_t layers, int64_t n, int32_t d);
+kvq_status kvq_swa_replay(const float *w, int32_t layers, int32_t d, const float *emb, int64_t n, int32_t n_win,
+                          float *states, float *hidden, void *workspace, size_t workspace_bytes,
+                          kvq_stream stream);
+
 /* Bytes of an FP4 page pool: num_pages * num_kv_heads * page_size *
  * 9 * head_dim / 8 (0 for invalid sizes). */
 size_t kvq_fp4_pool_bytes(int64_t num_pages, int32_t num_kv_heads, int32_t page_size, int32_t head_dim);

@@ -32,7 +32,7 @@ def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "kvq_append", "kvq_attn_dense", "kvq_decode_attn", "kvq_decode_attn_noalloc", "kvq_decode_workspace_bytes",
         "kvq_dequant", "kvq_fake_quant", "kvq_fp4_pool_bytes", "kvq_fp8_set_scales", "kvq_prefill_attn",
-        "kvq_status_string", "kvq_version"])
+        "kvq_status_string", "kvq_swa_replay", "kvq_swa_replay_workspace_bytes", "kvq_version"])
 
 
 def test_library_exports_every_declared_function(lib):
@@ -86,6 +86,21 @@ def test_prefill_refuses_bad_arguments_on_the_host(lib):
     assert lib.kvq_prefill_attn(ctypes.byref(s), 2, 3, 4, 16, 32, 0.1, 64, None, None) == 1    # Hq % Hkv
     assert lib.kvq_prefill_attn(ctypes.byref(s), 2, 32, 4, 16, 32, 0.1, 64, None, None) == 2   # G = 16
     assert lib.kvq_prefill_attn(ctypes.byref(s), 2, 16, 4, None, 32, 0.1, 64, None, None) == 1  # no lengths
+
+
+def test_replay_refuses_bad_arguments_on_the_host(lib):
+    # (pointers are fake: every one of these is refused before any launch)
+    w, e, st, ws = 256, 512, 1024, 2048
+    need = lib.kvq_swa_replay_workspace_bytes(2, 100, 128)
+    assert need == (4 * 100 * 128 + 4 * 2 * 128 * 128) * 4
+    assert lib.kvq_swa_replay_workspace_bytes(2, 100, 96) == 0
+    assert lib.kvq_swa_replay(w, 2, 96, e, 100, 16, st, None, ws, need, None) == 1    # d
+    assert lib.kvq_swa_replay(w, 0, 128, e, 100, 16, st, None, ws, need, None) == 1   # layers
+    assert lib.kvq_swa_replay(w, 2, 128, e, 100, 101, st, None, ws, need, None) == 1  # n_win > n
+    assert lib.kvq_swa_replay(w, 2, 128, e, 9000, 4097, st, None, ws, 1 << 30, None) == 1  # n_win > 4096
+    assert lib.kvq_swa_replay(w, 2, 128, e, 100, 16, None, None, ws, need, None) == 1  # no states
+    assert lib.kvq_swa_replay(w, 2, 128, e, 100, 16, st, None, ws + 4, need, None) == 1  # workspace alignment
+    assert lib.kvq_swa_replay(w, 2, 128, e, 100, 16, st, None, ws, need - 4, None) == 3  # too small
 
 
 def test_fp4_pool_bytes(lib):
