@@ -10,29 +10,26 @@
 // run on the tensor cores; the cache is dequantised once per tile into shared
 // memory and shared by the CTA's 128 query rows.
 //
-// CTA = the G query heads of one kv head times 256/G consecutive query tokens
-// of one sequence: 256 query rows as two 128-row query tiles A and B that share
-// every dequantised cache tile.  Fourteen warps in four roles run as a
+// CTA = the G query heads of one kv head times 128/G consecutive query tokens
+// of one sequence (128 query rows), ten warps in four roles that run as a
 // pipeline over the sequence's 128-position cache tiles:
-//   loader (1 thread)    bulk copies of the FP4 tiles, 3 in flight
-//   dequant (4 warps)    K^ [128 pos][d] (2 slots) and V^ [d][128 pos] (1 slot)
-//                        into shared memory in the tensor core's K-major
-//                        core-matrix layout (f16, E2M1 code times E4M3 scale;
-//                        positions past the end 0)
-//   MMA (1 thread)       S_X = Q_X K^T    tcgen05.mma M=128 N=128 K=d into TMEM
-//                        O_X += P_X V^    tcgen05.mma M=128 N=d K=128, P_X read
-//                                         from TMEM, O_X accumulated in TMEM
-//                        issued per tile as O_A, S_A(next), O_B, S_B(next), so
-//                        each query tile's next scores follow its own O update
-//   softmax (2 x 4 warps) thread r of warpgroup X owns row r of tile X: pass 1
-//                        the tile's row max from TMEM; the lazy reference is
-//                        raised only past +8 in the log2 domain (O_X, l rescaled
-//                        then); pass 2 P = 2^(S - m) as f16 pairs written back
-//                        over the first half of S_X; causal mask on the
-//                        diagonal tiles only
-// TMEM (512 columns): S_A, S_B, O_A, O_B, 128 columns each.  While one query
-// tile's softmax runs, the tensor cores work on the other tile.  mbarriers hand
-// each buffer from producer to consumer and back (MMA completions arrive via
+//   loader (1 thread)   bulk copies of the FP4 tiles, 3 in flight
+//   dequant (4 warps)   K^ [128 pos][d] and V^ [d][128 pos] into shared memory
+//                       in the tensor core's K-major core-matrix layout (f16,
+//                       E2M1 code times E4M3 scale; positions past the end 0),
+//                       2 slots each
+//   MMA (1 thread)      S(j) = Q K^(j)^T     tcgen05.mma M=128 N=128 K=d into
+//                                           one of 3 TMEM S buffers
+//                       O += P(j-1) V^(j-1) tcgen05.mma M=128 N=d K=128, P read
+//                                           from TMEM, O accumulated in TMEM
+//   softmax (4 warps)   thread r owns row r: the tile's row max from TMEM, the
+//                       lazy reference (raised only past +8 in the log2 domain;
+//                       O rescaled in TMEM then), causal mask on the diagonal
+//                       tiles only, P = 2^(S - m) as f16 pairs written back over
+//                       the first half of its S buffer
+// so the tensor cores compute S(j+1) and O += P(j-1) V while the softmax warps
+// work on tile j and the dequantisers on tile j+1.  mbarriers hand each buffer
+// from producer to consumer and back (MMA completions arrive via
 // tcgen05.commit).  Finally O / l (times the NVFP4 value scale) goes to global
 // memory.  Every wait is bounded; a timeout raises the CTA's abort word, every
 // role leaves its loop, copies and MMAs still in flight are waited for
@@ -274,10 +271,11 @@ __device__ __forceinline__ void dequant_v(uint32_t stage, uint32_t vdst, int val
   }
 }
 
-// Row max of 32 raw scores of a tile (positions >= lim masked when !fast),
+// Row max of 32 raw scores of a tile (positions >= lim masked unless FAST),
 // into four independent running maxima.
-__device__ __forceinline__ void chunk_max(const uint32_t (&v)[32], bool fast, int c0, int lim, float (&m)[4]) {
-  if (fast) {
+template <bool FAST>
+__device__ __forceinline__ void chunk_max(const uint32_t (&v)[32], int c0, int lim, float (&m)[4]) {
+  if (FAST) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) m[i & 3] = fmax3(m[i & 3], __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
   } else {
@@ -288,21 +286,65 @@ __device__ __forceinline__ void chunk_max(const uint32_t (&v)[32], bool fast, in
 }
 
 // P = 2^(S * cs - m) for 32 scores, as 16 f16 pairs; the row sum goes into
-// two packed running sums.
-__device__ __forceinline__ void chunk_p(const uint32_t (&v)[32], uint32_t* w, bool fast, int c0, int lim,
-                                        uint64_t cs2, uint64_t nref2, uint64_t (&l2)[2]) {
+// two packed running sums.  Positions >= lim are masked unless FAST.
+template <bool FAST>
+__device__ __forceinline__ void chunk_p(const uint32_t (&v)[32], uint32_t* w, int c0, int lim, uint64_t cs2,
+                                        uint64_t nref2, uint64_t (&l2)[2]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     float y0, y1;
     f2unpack(ffma2(f2pack(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), cs2, nref2), y0, y1);
     float e0 = fast_exp2(y0), e1 = fast_exp2(y1);
-    if (!fast) {
+    if (!FAST) {
       if (c0 + 2 * i >= lim) e0 = 0.0f;
       if (c0 + 2 * i + 1 >= lim) e1 = 0.0f;
     }
     l2[i & 1] = fadd2(l2[i & 1], f2pack(e0, e1));
     w[i] = pack_f16x2(e0, e1);
   }
+}
+
+// One tile's softmax passes for one row (thread): pass 1 the max, then the
+// lazy reference update (returns al), pass 2 P into the first 64 columns of
+// S_X.  Split out so that the unmasked and the masked tiles each get their own
+// straight-line code.
+template <bool FAST>
+__device__ __forceinline__ float softmax_pass1(uint32_t sp, int lim) {
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  uint32_t v0[32], v1[32];
+  tmem_ld32_async(sp, v0);
+  tmem_ld32_async(sp + 32, v1);
+  tmem_wait_ld(v0);
+  tmem_wait_ld(v1);
+  chunk_max<FAST>(v0, 0, lim, m4);
+  chunk_max<FAST>(v1, 32, lim, m4);
+  tmem_ld32_async(sp + 64, v0);
+  tmem_ld32_async(sp + 96, v1);
+  tmem_wait_ld(v0);
+  tmem_wait_ld(v1);
+  chunk_max<FAST>(v0, 64, lim, m4);
+  chunk_max<FAST>(v1, 96, lim, m4);
+  return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+}
+template <bool FAST>
+__device__ __forceinline__ void softmax_pass2(uint32_t sp, int lim, uint64_t cs2, uint64_t nref2, uint64_t (&l2)[2]) {
+  uint32_t v0[32], v1[32], w[16];
+  tmem_ld32_async(sp, v0);
+  tmem_wait_ld(v0);
+  tmem_ld32_async(sp + 32, v1);
+  chunk_p<FAST>(v0, w, 0, lim, cs2, nref2, l2);
+  tmem_st16_async(sp, w);
+  tmem_wait_ld(v1);
+  tmem_ld32_async(sp + 64, v0);
+  chunk_p<FAST>(v1, w, 32, lim, cs2, nref2, l2);
+  tmem_st16_async(sp + 16, w);
+  tmem_wait_ld(v0);
+  tmem_ld32_async(sp + 96, v1);
+  chunk_p<FAST>(v0, w, 64, lim, cs2, nref2, l2);
+  tmem_st16_async(sp + 32, w);
+  tmem_wait_ld(v1);
+  chunk_p<FAST>(v1, w, 96, lim, cs2, nref2, l2);
+  tmem_st16_async(sp + 48, w);
 }
 
 template <int D, int GT>
@@ -423,23 +465,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
       const bool fast = p0 + kPTile - 1 <= pos_min;  // no position of the tile masked for any row
       const int lim = row_ok ? (int)min((int64_t)kPTile, max((int64_t)0, pos_r - p0 + 1)) : 0;
       // pass 1: the row's maximum over the tile (raw scores; cs > 0)
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      {
-        uint32_t v0[32], v1[32];
-        tmem_ld32_async(sp, v0);
-        tmem_ld32_async(sp + 32, v1);
-        tmem_wait_ld(v0);
-        tmem_wait_ld(v1);
-        chunk_max(v0, fast, 0, lim, m4);
-        chunk_max(v1, fast, 32, lim, m4);
-        tmem_ld32_async(sp + 64, v0);
-        tmem_ld32_async(sp + 96, v1);
-        tmem_wait_ld(v0);
-        tmem_wait_ld(v1);
-        chunk_max(v0, fast, 64, lim, m4);
-        chunk_max(v1, fast, 96, lim, m4);
-      }
-      const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * cs;
+      const float mt = (fast ? softmax_pass1<true>(sp, lim) : softmax_pass1<false>(sp, lim)) * cs;
       // lazy reference: raised only when the tile passes it by the slack; O
       // and l then shrink by 2^(old - new)
       float al = 1.0f;
@@ -466,25 +492,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
       const float nref = m_run == -INFINITY ? 0.0f : -m_run;
       const uint64_t nref2 = f2pack(nref, nref);
       uint64_t l2[2] = {0ull, 0ull};
-      {
-        uint32_t v0[32], v1[32], w[16];
-        tmem_ld32_async(sp, v0);
-        tmem_wait_ld(v0);
-        tmem_ld32_async(sp + 32, v1);
-        chunk_p(v0, w, fast, 0, lim, cs2, nref2, l2);
-        tmem_st16_async(sp, w);
-        tmem_wait_ld(v1);
-        tmem_ld32_async(sp + 64, v0);
-        chunk_p(v1, w, fast, 32, lim, cs2, nref2, l2);
-        tmem_st16_async(sp + 16, w);
-        tmem_wait_ld(v0);
-        tmem_ld32_async(sp + 96, v1);
-        chunk_p(v0, w, fast, 64, lim, cs2, nref2, l2);
-        tmem_st16_async(sp + 32, w);
-        tmem_wait_ld(v1);
-        chunk_p(v1, w, fast, 96, lim, cs2, nref2, l2);
-        tmem_st16_async(sp + 48, w);
-      }
+      if (fast)
+        softmax_pass2<true>(sp, lim, cs2, nref2, l2);
+      else
+        softmax_pass2<false>(sp, lim, cs2, nref2, l2);
       tmem_wait_st();
       {
         float a0, a1, b0, b1;
