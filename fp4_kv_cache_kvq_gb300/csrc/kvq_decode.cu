@@ -331,7 +331,7 @@ __device__ __forceinline__ void begin_unit(const DecodeParams& p, ConsumerState<
 // One stage for one consumer warp: two 16-token slices, rows [32w, 32w+32).
 // The stage holds pool groups of GT = min(page_size, 128) tokens back to back;
 // a 16-token slice never straddles two groups.
-template <int D, int GT>
+template <int D, int GT, bool PARTIAL>
 __device__ __forceinline__ void consume_stage(ConsumerState<D>& st, uint32_t stage, int ntok,
                                               uint32_t empty_bar) {
   using R = Grp<D, GT>;
@@ -420,7 +420,9 @@ __device__ __forceinline__ void consume_stage(ConsumerState<D>& st, uint32_t sta
 #pragma unroll
     for (int i = 0; i < 4; ++i) S[sl][i] = acc[0][i] + acc[1][i];
   }
-  const bool partial = ntok < kChunk;  // only a unit's last chunk
+  // PARTIAL: the stage holds fewer than kChunk tokens (only a unit's last
+  // chunk); full stages get code without any of the masking below
+  constexpr bool partial = PARTIAL;
   if (partial) {
 #pragma unroll
     for (int sl = 0; sl < kSlices; ++sl) {
@@ -635,7 +637,10 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
     const int ntok = sm.ntok[s];
     if (ntok > 16 * kSlices * warp) {
-      consume_stage<D, GT>(st, stages_base + s * G::kStageBytes, ntok, smem_addr(&sm.empty[s]));
+      if (ntok < kChunk)
+        consume_stage<D, GT, true>(st, stages_base + s * G::kStageBytes, ntok, smem_addr(&sm.empty[s]));
+      else
+        consume_stage<D, GT, false>(st, stages_base + s * G::kStageBytes, ntok, smem_addr(&sm.empty[s]));
     } else {
       mbar_arrive(smem_addr(&sm.empty[s]));
     }
