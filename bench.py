@@ -586,7 +586,38 @@ def run_prefill_attn(args, dist: Dist):
     }
     if clk is not None:
         res["clocks"] = clk
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = prefill_oracle_sample(w, args.seed, q, budget_s=min(20.0, args.cpu_budget))
     return res
+
+
+def prefill_oracle_sample(w, seed: int, q, budget_s: float):
+    """The oracle's prefill of sampled query tokens: for one (sequence, kv
+    head) unit, the FP4 cache dequantised once (resident state), then fp64
+    attention of each sampled token's G query rows over its causal prefix,
+    tokens taken from the end of the chunk until the budget is spent.  Value
+    in query tokens/s of the whole head group (Hq rows per token)."""
+    import numpy as np
+
+    import oracle
+    T, C, G, d = w.context, w.chunk, w.group, w.head_dim
+    k, v = workloads.sequence_kv(w, 0, T, seed=seed, device="cpu")
+    kc, ks, _ = oracle.quantize_rows(k[:, 0].float().numpy())
+    vc, vs, _ = oracle.quantize_rows(v[:, 0].float().numpy())
+    kh, vh = oracle.dequantize_rows(kc, ks), oracle.dequantize_rows(vc, vs)
+    qh = q[0, :, :G].float().cpu().numpy()
+    scale = 1.0 / math.sqrt(d)
+    t = time.perf_counter()
+    rows = 0
+    for i in range(C - 1, -1, -1):
+        oracle.attend(qh[i], kh[:T - C + i + 1], vh[:T - C + i + 1], scale)
+        rows += G
+        if time.perf_counter() - t > budget_s:
+            break
+    dt = time.perf_counter() - t
+    return {"value": rows / w.num_q_heads / dt, "unit": "query tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows // G} tokens x G={G} query rows of one kv head over ~{T} positions "
+                      f"(fp64 C attention, one thread, {dt:.1f} s), scaled to Hq={w.num_q_heads} rows per token"}
 
 
 SWA_REPLAY_METRIC = ("bounded SWA replay of a toy 8-layer sliding-window network (d 128, window 512): "

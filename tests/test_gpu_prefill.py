@@ -158,3 +158,39 @@ def test_bad_length_flag():
     torch.cuda.synchronize()
     assert err.item() & kvq.FLAG_BAD_LENGTH
     assert not out[1].any() and torch.isfinite(out[0]).all()
+
+
+def test_full_size_sampled_rows():
+    """The benchmark's configuration (B4, Hkv8, Hq64, d128, a 1024-token chunk
+    over 16384 positions, page 64) in its launch configuration; sampled rows
+    (first, middle and last chunk tokens, several heads) against the oracle."""
+    w = workloads.WORKLOADS["prefill_attn"]
+    B, T, C, d = w.batch, w.context, w.chunk, w.head_dim
+    mp = -(-T // w.page_size)
+    cache = kvq.Fp4Cache(w.num_kv_heads, d, w.page_size, B * mp, mp)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k = torch.empty((B, T, w.num_kv_heads, d), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    for b in range(B):
+        k[b], v[b] = workloads.sequence_kv(w, b, T, seed=0, device="cuda")
+    kvq.append(cache, torch.zeros(B, dtype=torch.int32, device="cuda"), k, v, err=err)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4242)
+    q = torch.randn((B, C, w.num_q_heads, d), generator=g, device="cuda").to(torch.bfloat16)
+    lens = torch.full((B,), T, dtype=torch.int32, device="cuda")
+    out = kvq.prefill_attn(cache, lens, q, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    out, qh = out.cpu().numpy(), q.float().cpu().numpy()
+    G = w.group
+    scale = 1.0 / math.sqrt(d)
+    for b, h in ((0, 0), (3, 7)):
+        kc, ks, _ = oracle.quantize_rows(k[b, :, h].float().cpu().numpy())
+        vc, vs, _ = oracle.quantize_rows(v[b, :, h].float().cpu().numpy())
+        kh, vh = oracle.dequantize_rows(kc, ks), oracle.dequantize_rows(vc, vs)
+        vabs = np.maximum.accumulate(np.abs(vh).max(axis=1))
+        for i in (0, 511, C - 1):
+            n = T - C + i + 1
+            hh = h * G + (i % G)
+            ref, _, _ = oracle.attend(qh[b, i, hh:hh + 1], kh[:n], vh[:n], scale)
+            assert np.abs(out[b, i, hh] - ref[0]).max() <= TOL * vabs[n - 1], (b, h, i)

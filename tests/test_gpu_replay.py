@@ -88,3 +88,24 @@ def test_one_layer_bounded_replay_is_exact():
     rep, _ = kvq.swa_replay(w, e[T - n_win:].contiguous(), n_win, want_hidden=False)
     torch.cuda.synchronize()
     assert torch.equal(rep, full)
+
+
+def test_benchmark_configuration():
+    """The benchmark's toy (L8, d128, window 512, state after 65536
+    positions): the exact replay (4089 positions) equals a forward over all
+    65536 positions bit for bit, and the bounded replay matches the oracle."""
+    R = workloads.REPLAY
+    L, d, nw, T = R["layers"], R["d"], R["n_win"], R["T"]
+    w = workloads.replay_net(L, d, seed=0).cuda()
+    e = workloads.replay_inputs(0, T, d, seed=0).cuda()
+    full, _ = kvq.swa_replay(w, e, nw, want_hidden=False)
+    t0 = oracle.exact_replay_start(T, L, nw)
+    assert T - t0 == 4089
+    rep, _ = kvq.swa_replay(w, e[t0:].contiguous(), nw, want_hidden=False)
+    bnd, hid = kvq.swa_replay(w, e[T - nw:].contiguous(), nw)
+    torch.cuda.synchronize()
+    assert torch.equal(rep, full)
+    ref_h, ref_s = oracle.swa_forward(w.cpu().numpy(), e[T - nw:].cpu().numpy(), nw)
+    for l in range(L):
+        _close(bnd[l], ref_s[l], f"state {l}")
+    _close(hid, ref_h, "hidden")
