@@ -304,49 +304,6 @@ __device__ __forceinline__ void chunk_p(const uint32_t (&v)[32], uint32_t* w, in
   }
 }
 
-// One tile's softmax passes for one row (thread): pass 1 the max, then the
-// lazy reference update (returns al), pass 2 P into the first 64 columns of
-// S_X.  Split out so that the unmasked and the masked tiles each get their own
-// straight-line code.
-template <bool FAST>
-__device__ __forceinline__ float softmax_pass1(uint32_t sp, int lim) {
-  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-  uint32_t v0[32], v1[32];
-  tmem_ld32_async(sp, v0);
-  tmem_ld32_async(sp + 32, v1);
-  tmem_wait_ld(v0);
-  tmem_wait_ld(v1);
-  chunk_max<FAST>(v0, 0, lim, m4);
-  chunk_max<FAST>(v1, 32, lim, m4);
-  tmem_ld32_async(sp + 64, v0);
-  tmem_ld32_async(sp + 96, v1);
-  tmem_wait_ld(v0);
-  tmem_wait_ld(v1);
-  chunk_max<FAST>(v0, 64, lim, m4);
-  chunk_max<FAST>(v1, 96, lim, m4);
-  return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-}
-template <bool FAST>
-__device__ __forceinline__ void softmax_pass2(uint32_t sp, int lim, uint64_t cs2, uint64_t nref2, uint64_t (&l2)[2]) {
-  uint32_t v0[32], v1[32], w[16];
-  tmem_ld32_async(sp, v0);
-  tmem_wait_ld(v0);
-  tmem_ld32_async(sp + 32, v1);
-  chunk_p<FAST>(v0, w, 0, lim, cs2, nref2, l2);
-  tmem_st16_async(sp, w);
-  tmem_wait_ld(v1);
-  tmem_ld32_async(sp + 64, v0);
-  chunk_p<FAST>(v1, w, 32, lim, cs2, nref2, l2);
-  tmem_st16_async(sp + 16, w);
-  tmem_wait_ld(v0);
-  tmem_ld32_async(sp + 96, v1);
-  chunk_p<FAST>(v0, w, 64, lim, cs2, nref2, l2);
-  tmem_st16_async(sp + 32, w);
-  tmem_wait_ld(v1);
-  chunk_p<FAST>(v1, w, 96, lim, cs2, nref2, l2);
-  tmem_st16_async(sp + 48, w);
-}
-
 template <int D, int GT>
 __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const PrefillParams p) {
   using G = PGeo<D>;
@@ -464,38 +421,83 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
       const int64_t p0 = (int64_t)j * kPTile;
       const bool fast = p0 + kPTile - 1 <= pos_min;  // no position of the tile masked for any row
       const int lim = row_ok ? (int)min((int64_t)kPTile, max((int64_t)0, pos_r - p0 + 1)) : 0;
-      // pass 1: the row's maximum over the tile (raw scores; cs > 0)
-      const float mt = (fast ? softmax_pass1<true>(sp, lim) : softmax_pass1<false>(sp, lim)) * cs;
-      // lazy reference: raised only when the tile passes it by the slack; O
-      // and l then shrink by 2^(old - new)
-      float al = 1.0f;
-      if (mt > m_run + kPSlack) {
-        if (m_run != -INFINITY) al = fast_exp2(m_run - mt);
-        m_run = mt;
-      }
-      if (__any_sync(0xFFFFFFFFu, al != 1.0f)) {  // TMEM accesses are warp-collective
-        if (!(ok = wwait(pv_done, (uint32_t)(j - 1) & 1u, abort))) break;
-        tc_fence_after();
+      // the tile in two halves of 64 scores, each read from TMEM once: its
+      // max (raw scores; cs > 0) against the lazy reference, then its P over
+      // scores already held in registers (half h -> columns [32h, 32h + 32)).
+      // A raise of the reference shrinks what was accumulated against the old
+      // one: l, O and, for the second half, the first half's P.
+      uint64_t l2[2] = {0ull, 0ull};
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
-          tmem_ld32(op + (uint32_t)c0, o);
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t va[32], vb[32];
+        tmem_ld32_async(sp + (uint32_t)(64 * hf), va);
+        tmem_ld32_async(sp + (uint32_t)(64 * hf + 32), vb);
+        tmem_wait_ld(va);
+        tmem_wait_ld(vb);
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (fast) {
+          chunk_max<true>(va, 64 * hf, lim, m4);
+          chunk_max<true>(vb, 64 * hf + 32, lim, m4);
+        } else {
+          chunk_max<false>(va, 64 * hf, lim, m4);
+          chunk_max<false>(vb, 64 * hf + 32, lim, m4);
+        }
+        const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * cs;
+        float al = 1.0f;
+        if (mt > m_run + kPSlack) {
+          if (m_run != -INFINITY) al = fast_exp2(m_run - mt);
+          m_run = mt;
+        }
+        if (__any_sync(0xFFFFFFFFu, al != 1.0f)) {  // TMEM accesses are warp-collective
+          if (hf == 1) {  // the first half's P, columns [0, 32)
+            const uint32_t al2 = pack_f16x2(al, al);
+            tmem_wait_st();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al);
-          tmem_st32_async(op + (uint32_t)c0, o);
+            for (int k = 0; k < 2; ++k) {
+              uint32_t pw[16];
+              tmem_ld16(sp + (uint32_t)(16 * k), pw);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) pw[i] = hmul2_u32(pw[i], al2);
+              tmem_st16_async(sp + (uint32_t)(16 * k), pw);
+            }
+          }
+          {
+            float a0, a1, b0, b1;
+            f2unpack(l2[0], a0, a1);
+            f2unpack(l2[1], b0, b1);
+            l2[0] = f2pack(a0 * al, a1 * al);
+            l2[1] = f2pack(b0 * al, b1 * al);
+          }
+          if (j > 0) {  // O: once O_X += P_X V of the previous tile is done
+            if (!(ok = wwait(pv_done, (uint32_t)(j - 1) & 1u, abort))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 16) {
+              uint32_t o[16];
+              tmem_ld16(op + (uint32_t)c0, o);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * al);
+              tmem_st16_async(op + (uint32_t)c0, o);
+            }
+          }
+        }
+        l_run *= al;
+        const float nref = m_run == -INFINITY ? 0.0f : -m_run;
+        const uint64_t nref2 = f2pack(nref, nref);
+        uint32_t w[16];
+        if (fast) {
+          chunk_p<true>(va, w, 64 * hf, lim, cs2, nref2, l2);
+          tmem_st16_async(sp + (uint32_t)(32 * hf), w);
+          chunk_p<true>(vb, w, 64 * hf + 32, lim, cs2, nref2, l2);
+          tmem_st16_async(sp + (uint32_t)(32 * hf + 16), w);
+        } else {
+          chunk_p<false>(va, w, 64 * hf, lim, cs2, nref2, l2);
+          tmem_st16_async(sp + (uint32_t)(32 * hf), w);
+          chunk_p<false>(vb, w, 64 * hf + 32, lim, cs2, nref2, l2);
+          tmem_st16_async(sp + (uint32_t)(32 * hf + 16), w);
         }
       }
-      l_run *= al;
-      // pass 2: P into the first 64 columns of S_X (two positions per
-      // column); the 16 columns of P from scores [32k, 32k + 32) land on
-      // scores [16k, 16k + 16), already read
-      const float nref = m_run == -INFINITY ? 0.0f : -m_run;
-      const uint64_t nref2 = f2pack(nref, nref);
-      uint64_t l2[2] = {0ull, 0ull};
-      if (fast)
-        softmax_pass2<true>(sp, lim, cs2, nref2, l2);
-      else
-        softmax_pass2<false>(sp, lim, cs2, nref2, l2);
+      if (!ok) break;
       tmem_wait_st();
       {
         float a0, a1, b0, b1;
