@@ -158,6 +158,37 @@ __device__ __noinline__ uint4 quantize_plain(const uint16_t* src, float S) {
   return make_uint4(q.x, q.y, sb, ok ? 0u : 1u);
 }
 
+// NVFP4 block: the FP4 quantiser on y = x / S (IEEE fp32 division by the kv
+// head's second-level scale S), the scale byte from the IEEE amax(y) / 6 as
+// in quantize_plain, and the codes from the corrected reciprocal quotient
+// block_quotient(y, s, RN(1/s)).  For an E4M3 scale s that quotient equals
+// the IEEE fp32 y / s for every finite fp32 y: checked exhaustively over all
+// 2^23 significands of y against the eight E4M3 significands, and every step
+// scales exactly with the exponents while the values stay normal; below that
+// the quotient lies far under the first E2M1 midpoint and both give the
+// signed zero.  Blocks with a value that is not finite after the division
+// take quantize_plain.
+__device__ __forceinline__ uint4 quantize_nv(const uint16_t* src, float S) {
+  Block16 blk = load_bf16x16(src);
+  bool ok = blk.finite;
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    blk.x[i] = __fdiv_rn(blk.x[i], S);
+    ok &= isfinite(blk.x[i]);
+    amax = fmaxf(amax, fabsf(blk.x[i]));
+  }
+  if (!ok) return quantize_plain(src, S);
+  uint32_t sb = e4m3x2_from_f32(__fdiv_rn(amax, 6.0f), 0.0f) & 0xFFu;
+  if (sb == 0u) sb = 0x01u;  // E4M3 minimum subnormal 2^-9
+  const float s = e4m3_to_f32(sb), r = __frcp_rn(s);
+  float q[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) q[i] = block_quotient(blk.x[i], s, r);
+  return make_uint4(e2m1x8_from_f32(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]),
+                    e2m1x8_from_f32(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]), sb, 0u);
+}
+
 // n / d for n < 2^31 without a hardware divide: (umulhi(n, mul) + n) >> shift
 // (Granlund and Montgomery, "Division by invariant integers using
 // multiplication", 1994, the round-up variant with a 33-bit multiplier).
@@ -246,7 +277,7 @@ __global__ void __launch_bounds__(256, kAppendMinCtas) append_fp4_kernel(const k
       const float S = __ldg(static_cast<const float*>(c.k_scale) + h);
 #pragma unroll
       for (int jb = 0; jb < BK; ++jb) {
-        const uint4 r4 = quantize_plain(src + 16 * jb, S);
+        const uint4 r4 = quantize_nv(src + 16 * jb, S);
         if (r4.w) set_flag(flag, KVQ_FLAG_NONFINITE);
         codes[2 * jb] = r4.x;
         codes[2 * jb + 1] = r4.y;
@@ -331,7 +362,8 @@ __global__ void __launch_bounds__(256, kAppendMinCtas) append_fp4_kernel(const k
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         if (!(hf ? mine1 : mine0)) continue;
-        const uint4 q = quantize_plain(v + ((row + (pos + hf - sp)) * hkv + h) * D + 16 * j, S);
+        const uint16_t* vsrc = v + ((row + (pos + hf - sp)) * hkv + h) * D + 16 * j;
+        const uint4 q = NV ? quantize_nv(vsrc, S) : quantize_plain(vsrc, S);
         if (q.w) set_flag(flag, KVQ_FLAG_NONFINITE);
         lo |= spread_nibbles(q.x) << (4 * hf);
         hi |= spread_nibbles(q.y) << (4 * hf);
