@@ -263,6 +263,42 @@ class Setup:
             ev[1].record()
         return self.kv_tokens[s] * self.layers
 
+    def capture_graphs(self):
+        """One CUDA graph per step of the cycle for the appends and one for the
+        decode calls (the same launches as step(), replayed without host
+        launch gaps); the decode-only events go between the two replays."""
+        self.graphs = []
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for i in range(CYCLE):
+                s = i % CYCLE
+                ga, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+                with torch.cuda.graph(ga, stream=side):
+                    for cache, swa in zip(self.caches, self.swas):
+                        self.kvq.append(cache, self.pos[s], self.k_new[s], self.v_new[s], err=self.err)
+                        if swa is not None:
+                            self.kvq.append(swa, self.pos[s], self.k_new[s], self.v_new[s], err=self.err)
+                with torch.cuda.graph(gd, stream=side):
+                    for cache, swa, out in zip(self.caches, self.swas, self.outs):
+                        self.kvq.decode_attn(cache, self.lens[s], self.q[i % NQ], self.scale, swa=swa, out=out,
+                                             workspace=self.ws, err=self.err)
+                self.graphs.append((ga, gd))
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+
+    def step_graph(self, i: int, ev=None):
+        """step(i) replayed from the captured graphs (i % CYCLE == the cycle
+        slot, and CYCLE is a multiple of NQ, so slot and query set match)."""
+        ga, gd = self.graphs[i % CYCLE]
+        ga.replay()
+        if ev is not None:
+            ev[0].record()
+        gd.replay()
+        if ev is not None:
+            ev[1].record()
+        return self.kv_tokens[i % CYCLE] * self.layers
+
     def decode_algorithmic_bytes(self, i: int) -> int:
         """Algorithmic bytes of one layer's decode call at step i."""
         w = self.w
@@ -292,6 +328,11 @@ def run_gpu(args, dist: Dist):
     torch.cuda.synchronize()
     if st.err.item() != 0:
         raise RuntimeError(f"device error flag {st.err.item()} during warm-up")
+    if args.graphs:
+        st.capture_graphs()
+        for i in range(Wm):
+            st.step_graph(Wm + i)
+        torch.cuda.synchronize()
 
     # ---- device-resident timing.  A cache smaller than twice L2 would stay
     # in L2 from step to step: then every step is timed on its own, after a
@@ -314,7 +355,7 @@ def run_gpu(args, dist: Dist):
             if flushed:
                 flush.fill_(i & 0xFF)
             steps[i][0].record()
-            tokens += st.step(Wm + i, ev=evs[i])
+            tokens += st.step_graph(Wm + i, ev=evs[i]) if args.graphs else st.step(Wm + i, ev=evs[i])
             steps[i][1].record()
         t1.record()
         torch.cuda.synchronize()
@@ -382,6 +423,8 @@ def run_gpu(args, dist: Dist):
                    "l2": (f"cache smaller than 2 x L2: {2 * l2_bytes} B written before every step, steps timed "
                           f"one by one (warm-L2 rate without the flush: {warm_value:.4g} {UNIT})") if small
                    else f"inputs larger than L2 (FP4 cache {st.cache.nbytes} B vs {l2_bytes} B L2), no flush",
+                   "launch": "CUDA graphs (one per step of the cycle: appends, then decode)" if args.graphs
+                   else "eager launches",
                    "parallelism": f"replicas x{dist.world}"},
         "value_l2_warm": warm_value,
         "hbm_gbs_step": step_bytes * K / elapsed_s / 1e9,
@@ -915,6 +958,8 @@ def main(argv=None):
                     help="layers per step, each with its own cache (long_context at 4 layers: 4.84 GB)")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graphs", action=argparse.BooleanOptionalAction, default=False,
+                    help="replay each step's appends and decode from CUDA graphs (decode workloads)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

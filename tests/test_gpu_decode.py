@@ -154,3 +154,37 @@ def test_workspace_too_small_is_refused():
     with pytest.raises(kvq.KvqError) as e:
         kvq.decode_attn(built.cache, built.lens_dev, workloads.queries(w, device="cuda"), workspace=ws)
     assert e.value.status == 3
+
+
+def test_decode_replays_from_a_cuda_graph():
+    """kvq_decode_attn enqueues only kernels on the caller's stream (no
+    allocation, no synchronisation), so it can be captured in a CUDA graph; a
+    replay gives the eager result bit for bit, and a replay after the captured
+    query is changed in place computes with the new values."""
+    w = workloads.scaled(BASE, batch=3, num_kv_heads=2, num_q_heads=8)
+    lens = [700, 129, 64]
+    built = build_fp4(w, lens, seed=11)
+    q = workloads.queries(w, seed=11, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(kvq.decode_workspace_bytes(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim), 16),
+                     dtype=torch.uint8, device="cuda")
+    eager = kvq.decode_attn(built.cache, built.lens_dev, q, workspace=ws, err=err).clone()
+    out = torch.empty_like(eager)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            kvq.decode_attn(built.cache, built.lens_dev, q, out=out, workspace=ws, err=err)
+    torch.cuda.current_stream().wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    q2 = workloads.queries(w, seed=12, device="cuda")
+    q.copy_(q2)
+    eager2 = kvq.decode_attn(built.cache, built.lens_dev, q2, workspace=ws, err=err).clone()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager2) and not torch.equal(eager2, eager)
+    assert err.item() == 0
