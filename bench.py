@@ -242,7 +242,7 @@ class Setup:
         self.ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
         torch.cuda.synchronize()
 
-    def step(self, i: int, q=None, k=None, v=None, ev=None):
+    def step(self, i: int, q=None, k=None, v=None, ev=None, outs=None):
         """One decode step: append the new token to every layer's caches,
         then decode attention for every layer (the same token and query per
         layer).  Returns the KV-tokens attended (all layers)."""
@@ -257,7 +257,7 @@ class Setup:
         if ev is not None:
             ev[0].record()
         qq = self.q[i % NQ] if q is None else q
-        for cache, swa, out in zip(self.caches, self.swas, self.outs):
+        for cache, swa, out in zip(self.caches, self.swas, self.outs if outs is None else outs):
             kvq.decode_attn(cache, self.lens[s], qq, self.scale, swa=swa, out=out, workspace=self.ws, err=self.err)
         if ev is not None:
             ev[1].record()
@@ -342,8 +342,13 @@ def run_gpu(args, dist: Dist):
     small = st.cache.nbytes < 2 * l2_bytes
     flush = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=device) if small else None
 
+    def run_step(i, ev=None):
+        return st.step_graph(i, ev=ev) if args.graphs else st.step(i, ev=ev)
+
     def timed(flushed: bool):
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        """K steps.  Back to back (events only at the two ends: a timing event
+        between two kernels keeps the second from starting while the first
+        drains), or, after an L2 flush, each step on its own events."""
         steps = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         clocks = ClockSampler(device.index)
@@ -354,9 +359,10 @@ def run_gpu(args, dist: Dist):
         for i in range(K):
             if flushed:
                 flush.fill_(i & 0xFF)
-            steps[i][0].record()
-            tokens += st.step_graph(Wm + i, ev=evs[i]) if args.graphs else st.step(Wm + i, ev=evs[i])
-            steps[i][1].record()
+                steps[i][0].record()
+            tokens += run_step(Wm + i)
+            if flushed:
+                steps[i][1].record()
         t1.record()
         torch.cuda.synchronize()
         dist.barrier()
@@ -365,13 +371,26 @@ def run_gpu(args, dist: Dist):
             elapsed = sum(a.elapsed_time(b) for a, b in steps) / 1e3
         else:
             elapsed = t0.elapsed_time(t1) / 1e3
-        return tokens, elapsed, [a.elapsed_time(b) for a, b in evs], clk
+        return tokens, elapsed, clk
+
+    def decode_call_ms(flushed: bool):
+        """The decode calls' own duration (events around the decode part of
+        each step), for the roofline: the same steps, timed again."""
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        torch.cuda.synchronize()
+        for i in range(K):
+            if flushed:
+                flush.fill_(i & 0xFF)
+            run_step(Wm + i, ev=evs[i])
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
 
     warm_value = None
     if small:
-        wt, we, _, _ = timed(False)
+        wt, we, _ = timed(False)
         warm_value, _ = combine_ranks(dist, wt, we)
-    tokens, elapsed_s, decode_ms, clk = timed(small)
+    tokens, elapsed_s, clk = timed(small)
+    decode_ms = decode_call_ms(small)
     if st.err.item() != 0:
         raise RuntimeError(f"device error flag {st.err.item()} during the timed steps")
     value, max_s = combine_ranks(dist, tokens, elapsed_s)
@@ -383,32 +402,64 @@ def run_gpu(args, dist: Dist):
     append_bytes = w.batch * (2 * w.num_kv_heads * w.head_dim * 2 + fp4_bytes_per_token(w))
     step_bytes = L * (dec_bytes + append_bytes)
 
-    # ---- end to end through the public API with pinned host buffers
+    # ---- end to end through the public API with pinned host buffers.  Every
+    # step copies its query and new token in from pinned host memory and its
+    # output back; the copies run on a second stream, double-buffered, so that
+    # step i + 1's inputs upload and step i - 1's output downloads while step i
+    # computes (events order each buffer's reuse).
     Ke = min(K, max(50, K // 4))
     q_host = [q.cpu().pin_memory() for q in st.q]
     k_host = [k.cpu().pin_memory() for k in st.k_new]
     v_host = [v.cpu().pin_memory() for v in st.v_new]
-    outs_host = [torch.empty(st.out.shape, dtype=torch.float32).pin_memory() for _ in range(L)]
-    q_dev, k_dev, v_dev = torch.empty_like(st.q[0]), torch.empty_like(st.k_new[0]), torch.empty_like(st.v_new[0])
+    outs_host = [[torch.empty(st.out.shape, dtype=torch.float32).pin_memory() for _ in range(L)] for _ in range(2)]
+    bufs = [(torch.empty_like(st.q[0]), torch.empty_like(st.k_new[0]), torch.empty_like(st.v_new[0]),
+             [torch.empty_like(st.out) for _ in range(L)]) for _ in range(2)]
+    q_dev, k_dev, v_dev = bufs[0][0], bufs[0][1], bufs[0][2]
+    compute = torch.cuda.current_stream()
+    copier = torch.cuda.Stream()
+    loaded = [torch.cuda.Event() for _ in range(2)]    # inputs of a buffer set uploaded
+    consumed = [torch.cuda.Event() for _ in range(2)]  # step done with a buffer set's inputs and outputs
+    fetched = [torch.cuda.Event() for _ in range(2)]   # a buffer set's outputs downloaded
     torch.cuda.synchronize()
     dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
+    copier.wait_stream(compute)
+
+    def upload(i):
+        qd, kd, vd, _ = bufs[i % 2]
+        with torch.cuda.stream(copier):
+            if i >= 2:
+                copier.wait_event(consumed[i % 2])
+            s_ = (Wm + i) % CYCLE
+            qd.copy_(q_host[(Wm + i) % NQ], non_blocking=True)
+            kd.copy_(k_host[s_], non_blocking=True)
+            vd.copy_(v_host[s_], non_blocking=True)
+            loaded[i % 2].record(copier)
+
     e2e_tokens = 0
+    upload(0)
     for i in range(Ke):
-        s = (Wm + i) % CYCLE
-        q_dev.copy_(q_host[(Wm + i) % NQ], non_blocking=True)
-        k_dev.copy_(k_host[s], non_blocking=True)
-        v_dev.copy_(v_host[s], non_blocking=True)
-        e2e_tokens += st.step(Wm + i, q=q_dev, k=k_dev, v=v_dev)
-        for oh, od in zip(outs_host, st.outs):
-            oh.copy_(od, non_blocking=True)
+        if i + 1 < Ke:
+            upload(i + 1)
+        qd, kd, vd, od = bufs[i % 2]
+        compute.wait_event(loaded[i % 2])
+        if i >= 2:
+            compute.wait_event(fetched[i % 2])  # its outputs of step i - 2 are on the host
+        e2e_tokens += st.step(Wm + i, q=qd, k=kd, v=vd, outs=od)
+        consumed[i % 2].record(compute)
+        with torch.cuda.stream(copier):
+            copier.wait_event(consumed[i % 2])
+            for oh, o in zip(outs_host[i % 2], od):
+                oh.copy_(o, non_blocking=True)
+            fetched[i % 2].record(copier)
+    compute.wait_stream(copier)
     e1.record()
     torch.cuda.synchronize()
     dist.barrier()
     e2e_value, _ = combine_ranks(dist, e2e_tokens, e0.elapsed_time(e1) / 1e3)
     h2d = q_dev.numel() * 2 + k_dev.numel() * 2 + v_dev.numel() * 2
-    d2h = sum(oh.numel() for oh in outs_host) * 4
+    d2h = sum(oh.numel() for oh in outs_host[0]) * 4
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": K, "warmup": Wm,
