@@ -404,9 +404,10 @@ def run_gpu(args, dist: Dist):
 
     # ---- end to end through the public API with pinned host buffers.  Every
     # step copies its query and new token in from pinned host memory and its
-    # output back; the copies run on a second stream, double-buffered, so that
-    # step i + 1's inputs upload and step i - 1's output downloads while step i
-    # computes (events order each buffer's reuse).
+    # output back.  For caches larger than L2 the copies run on a second
+    # stream, double-buffered, so that step i + 1's inputs upload and step
+    # i - 1's output downloads while step i computes (events order each
+    # buffer's reuse).
     Ke = min(K, max(50, K // 4))
     q_host = [q.cpu().pin_memory() for q in st.q]
     k_host = [k.cpu().pin_memory() for k in st.k_new]
@@ -438,21 +439,35 @@ def run_gpu(args, dist: Dist):
             loaded[i % 2].record(copier)
 
     e2e_tokens = 0
-    upload(0)
-    for i in range(Ke):
-        if i + 1 < Ke:
-            upload(i + 1)
-        qd, kd, vd, od = bufs[i % 2]
-        compute.wait_event(loaded[i % 2])
-        if i >= 2:
-            compute.wait_event(fetched[i % 2])  # its outputs of step i - 2 are on the host
-        e2e_tokens += st.step(Wm + i, q=qd, k=kd, v=vd, outs=od)
-        consumed[i % 2].record(compute)
-        with torch.cuda.stream(copier):
-            copier.wait_event(consumed[i % 2])
-            for oh, o in zip(outs_host[i % 2], od):
+    if small:
+        # steps of a few tens of microseconds: the host's event calls would
+        # cost more than the copies they hide, so the copies go in line on the
+        # compute stream
+        qd, kd, vd, od = bufs[0]
+        for i in range(Ke):
+            s_ = (Wm + i) % CYCLE
+            qd.copy_(q_host[(Wm + i) % NQ], non_blocking=True)
+            kd.copy_(k_host[s_], non_blocking=True)
+            vd.copy_(v_host[s_], non_blocking=True)
+            e2e_tokens += st.step(Wm + i, q=qd, k=kd, v=vd, outs=od)
+            for oh, o in zip(outs_host[0], od):
                 oh.copy_(o, non_blocking=True)
-            fetched[i % 2].record(copier)
+    else:
+        upload(0)
+        for i in range(Ke):
+            if i + 1 < Ke:
+                upload(i + 1)
+            qd, kd, vd, od = bufs[i % 2]
+            compute.wait_event(loaded[i % 2])
+            if i >= 2:
+                compute.wait_event(fetched[i % 2])  # its outputs of step i - 2 are on the host
+            e2e_tokens += st.step(Wm + i, q=qd, k=kd, v=vd, outs=od)
+            consumed[i % 2].record(compute)
+            with torch.cuda.stream(copier):
+                copier.wait_event(consumed[i % 2])
+                for oh, o in zip(outs_host[i % 2], od):
+                    oh.copy_(o, non_blocking=True)
+                fetched[i % 2].record(copier)
     compute.wait_stream(copier)
     e1.record()
     torch.cuda.synchronize()
