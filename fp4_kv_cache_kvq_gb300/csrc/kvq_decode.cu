@@ -668,15 +668,16 @@ struct MergeParams {
 };
 
 // Merge without a window: one CTA per unit, thread (row r, 4 channels) takes
-// float4 partials.  Loads of the unit's partials are independent of one
-// another (four partials in flight per step), so a unit costs a few L2 round
-// trips whatever its split count.
+// float4 partials.  The unit's record and length load together, then one
+// online pass over the partials whose loads are all independent: two L2
+// round trips whatever the split count.
 template <int D>
 __global__ void __launch_bounds__(kNG * D / 4) merge_splits_kernel(const MergeParams p) {
   const int u = blockIdx.x;
   const int b = u / p.hkv, h = u % p.hkv;
   const int r = threadIdx.x / (D / 4), c4 = threadIdx.x % (D / 4);
   if (r >= p.g) return;
+  const int2 rec = __ldg(p.unit_rec + u);  // loaded beside the length (unused when T == 0)
   int32_t T = __ldg(p.lens + b);
   if (T < 0) {
     if (threadIdx.x == 0 && h == 0) set_flag(p.flag, KVQ_FLAG_BAD_LENGTH);
@@ -688,25 +689,27 @@ __global__ void __launch_bounds__(kNG * D / 4) merge_splits_kernel(const MergePa
     *dst = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
-  const int2 rec = __ldg(p.unit_rec + u);
+  // one pass over the unit's partials with every load independent: the
+  // running maximum rescales what has been summed so far (online
+  // log-sum-exp merge)
   float mx = -INFINITY;
-#pragma unroll 4
-  for (int k = 0; k < rec.y; ++k) mx = fmaxf(mx, __ldcg(p.part_ml + ((int64_t)(rec.x + k) * p.g + r) * 2));
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   float l = 0.0f;
-  if (mx != -INFINITY) {
 #pragma unroll 4
-    for (int k = 0; k < rec.y; ++k) {
-      const int64_t sl = (int64_t)(rec.x + k) * p.g + r;
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + sl);
-      const float4 ov = __ldcg(reinterpret_cast<const float4*>(p.part_o + sl * D) + c4);
-      const float f = ml.x == -INFINITY ? 0.0f : fast_exp2(ml.x - mx);
-      o.x = fmaf(f, ov.x, o.x);
-      o.y = fmaf(f, ov.y, o.y);
-      o.z = fmaf(f, ov.z, o.z);
-      o.w = fmaf(f, ov.w, o.w);
-      l = fmaf(f, ml.y, l);
-    }
+  for (int k = 0; k < rec.y; ++k) {
+    const int64_t sl = (int64_t)(rec.x + k) * p.g + r;
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + sl);
+    const float4 ov = __ldcg(reinterpret_cast<const float4*>(p.part_o + sl * D) + c4);
+    if (ml.x == -INFINITY) continue;  // a split with no position of this unit
+    const float mn = fmaxf(mx, ml.x);
+    const float a = mx == -INFINITY ? 0.0f : fast_exp2(mx - mn);
+    const float f = fast_exp2(ml.x - mn);
+    o.x = fmaf(f, ov.x, o.x * a);
+    o.y = fmaf(f, ov.y, o.y * a);
+    o.z = fmaf(f, ov.z, o.z * a);
+    o.w = fmaf(f, ov.w, o.w * a);
+    l = fmaf(f, ml.y, l * a);
+    mx = mn;
   }
   const float inv = l > 0.0f ? 1.0f / l : 0.0f;
   *dst = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
