@@ -48,6 +48,8 @@ DECODE_SRC = os.path.join(ROOT, "fp4_kv_cache_kvq_gb300", "csrc", "kvq_decode.cu
 PROFILE = os.path.join(ROOT, "profiles", "decode_fp4_long_context.md")
 APPEND_SRC = os.path.join(ROOT, "fp4_kv_cache_kvq_gb300", "csrc", "kvq_append.cu")
 APPEND_PROFILE = os.path.join(ROOT, "profiles", "append_fp4_prefill.md")
+PREFILL_SRC = os.path.join(ROOT, "fp4_kv_cache_kvq_gb300", "csrc", "kvq_prefill.cu")
+PREFILL_PROFILE = os.path.join(ROOT, "profiles", "prefill_fp4_prefill_attn.md")
 
 
 # ----------------------------------------------------------------- distributed plumbing
@@ -687,7 +689,9 @@ def run_prefill_attn(args, dist: Dist):
                    "parallelism": f"replicas x{dist.world}"},
         "roofline": {"bound": "tensor", "kernel": "prefill_fp4_kernel (tcgen05.mma f16, TMEM accumulators)",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_source": peak_src, "traffic": None, "algorithmic_flops_per_launch": flops,
+                     "peak_source": peak_src,
+                     "traffic": profiled_traffic(PREFILL_PROFILE, PREFILL_SRC) if not nv else None,
+                     "algorithmic_flops_per_launch": flops,
                      "avg_launch_ms": secs * 1e3 / K},
         "e2e": {"value": e2e, "unit": "query tokens/s", "h2d_bytes_per_step": q.numel() * 2,
                 "d2h_bytes_per_step": out.numel() * 4, "steps": Ke},
