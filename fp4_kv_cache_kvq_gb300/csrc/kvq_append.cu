@@ -158,35 +158,65 @@ __device__ __noinline__ uint4 quantize_plain(const uint16_t* src, float S) {
   return make_uint4(q.x, q.y, sb, ok ? 0u : 1u);
 }
 
-// NVFP4 block: the FP4 quantiser on y = x / S (IEEE fp32 division by the kv
-// head's second-level scale S), the scale byte from the IEEE amax(y) / 6 as
-// in quantize_plain, and the codes from the corrected reciprocal quotient
-// block_quotient(y, s, RN(1/s)).  For an E4M3 scale s that quotient equals
-// the IEEE fp32 y / s for every finite fp32 y: checked exhaustively over all
-// 2^23 significands of y against the eight E4M3 significands, and every step
-// scales exactly with the exponents while the values stay normal; below that
-// the quotient lies far under the first E2M1 midpoint and both give the
-// signed zero.  Blocks with a value that is not finite after the division
-// take quantize_plain.
-__device__ __forceinline__ uint4 quantize_nv(const uint16_t* src, float S) {
-  Block16 blk = load_bf16x16(src);
-  bool ok = blk.finite;
-  float amax = 0.0f;
+// NVFP4 block: the FP4 quantiser on y = x / S, S the kv head's fp32
+// second-level scale, with the codes and scale byte of the IEEE fp32
+// divisions and no division on the way:
+//   y = block_quotient(x, S, RN(1/S)) is the IEEE fp32 x / S for every bf16
+//     x and every fp32 S: checked exhaustively over the 2^7 significands of
+//     x against all 2^23 significands of S; the steps scale exactly with
+//     both exponents while the values stay normal, and a quotient that falls
+//     below the normal range keeps its sign and lies far under the first
+//     E2M1 midpoint of any block scale (s >= 2^-9), so its code is the
+//     signed zero either way;
+//   max |y| = RN(max |x| / S) (rounding is monotone), taken once per block;
+//   amax(y) / 6 and y / s by block_quotient as well: 6 and every E4M3 scale
+//     have E4M3 significands, for which that quotient equals the IEEE one
+//     for every fp32 dividend (exhaustive over the 2^23 significands).
+// nv_fast_scale says whether S and RN(1/S) are normal; a block whose largest
+// quotient is not finite (Inf/NaN input or overflow of x / S) returns false
+// and takes quantize_plain, which flags it.
+__device__ __forceinline__ bool nv_fast_scale(float S) { return S >= 0x1p-126f && S <= 0x1p126f; }
+
+__device__ __forceinline__ bool nv_quotients(const Raw16& b, float S, float R, float (&y)[16], uint32_t& sb) {
+  if (!b.finite) return false;
+  const float ya = block_quotient(b.amax, S, R);
+  if (!(ya <= 3.40282347e38f)) return false;
+  sb = block_scale_byte(ya);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    blk.x[i] = __fdiv_rn(blk.x[i], S);
-    ok &= isfinite(blk.x[i]);
-    amax = fmaxf(amax, fabsf(blk.x[i]));
+  for (int i = 0; i < 8; ++i) {
+    y[2 * i] = block_quotient(bf16_lo(b.w[i]), S, R);
+    y[2 * i + 1] = block_quotient(bf16_hi(b.w[i]), S, R);
   }
-  if (!ok) return quantize_plain(src, S);
-  uint32_t sb = e4m3x2_from_f32(__fdiv_rn(amax, 6.0f), 0.0f) & 0xFFu;
-  if (sb == 0u) sb = 0x01u;  // E4M3 minimum subnormal 2^-9
-  const float s = e4m3_to_f32(sb), r = __frcp_rn(s);
-  float q[16];
+  return true;
+}
+
+// 8 code bytes of 16 quotients (channel 2i in the low nibble of byte i).
+__device__ __forceinline__ uint2 k_codes_f32(const float (&y)[16], float s, float r) {
+  uint32_t out[2];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) q[i] = block_quotient(blk.x[i], s, r);
-  return make_uint4(e2m1x8_from_f32(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]),
-                    e2m1x8_from_f32(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]), sb, 0u);
+  for (int half = 0; half < 2; ++half) {
+    const float* a = y + 8 * half;
+    out[half] = e2m1x8_from_f32(block_quotient(a[0], s, r), block_quotient(a[1], s, r), block_quotient(a[2], s, r),
+                                block_quotient(a[3], s, r), block_quotient(a[4], s, r), block_quotient(a[5], s, r),
+                                block_quotient(a[6], s, r), block_quotient(a[7], s, r));
+  }
+  return make_uint2(out[0], out[1]);
+}
+
+// Token-pair V codes of two tokens' quotients: byte c holds channel c of
+// token 0 (low nibble) and token 1 (high nibble).
+__device__ __forceinline__ uint4 v_pair_codes_f32(const float (&y0)[16], float s0, float r0, const float (&y1)[16],
+                                                  float s1, float r1) {
+  uint32_t out[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int c = 4 * q;
+    out[q] = e2m1x8_from_f32(block_quotient(y0[c], s0, r0), block_quotient(y1[c], s1, r1),
+                             block_quotient(y0[c + 1], s0, r0), block_quotient(y1[c + 1], s1, r1),
+                             block_quotient(y0[c + 2], s0, r0), block_quotient(y1[c + 2], s1, r1),
+                             block_quotient(y0[c + 3], s0, r0), block_quotient(y1[c + 3], s1, r1));
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
 // n / d for n < 2^31 without a hardware divide: (umulhi(n, mul) + n) >> shift
@@ -217,7 +247,8 @@ constexpr int kAppendMinCtas = 4;
 // take consecutive spans of the input; the row, page and address arithmetic
 // is done once per item, not once per block.  Indices are 32-bit;
 // the host splits the batch so that every launch's item count fits.
-// NV: an NVFP4 cache (codes of x / S_h, the IEEE path for every block).
+// NV: an NVFP4 cache (codes of x / S_h from nv_quotients; blocks it refuses
+// take the IEEE-division quantiser).
 template <int D, bool NV>
 __global__ void __launch_bounds__(256, kAppendMinCtas) append_fp4_kernel(const kvq_cache c, int32_t b_begin, uint32_t k_items,
                                                          uint32_t v_items, uint32_t k_ctas, DivU32 div_hkv,
@@ -275,13 +306,27 @@ __global__ void __launch_bounds__(256, kAppendMinCtas) append_fp4_kernel(const k
     uint32_t scales = 0;
     if constexpr (NV) {
       const float S = __ldg(static_cast<const float*>(c.k_scale) + h);
+      const bool fast = nv_fast_scale(S);
+      const float R = __frcp_rn(S);
 #pragma unroll
       for (int jb = 0; jb < BK; ++jb) {
-        const uint4 r4 = quantize_nv(src + 16 * jb, S);
-        if (r4.w) set_flag(flag, KVQ_FLAG_NONFINITE);
-        codes[2 * jb] = r4.x;
-        codes[2 * jb + 1] = r4.y;
-        scales |= r4.z << (8 * jb);
+        Raw16 kb;
+        load_raw16(src + 16 * jb, kb);
+        float y[16];
+        uint32_t sb;
+        uint2 q;
+        if (fast && nv_quotients(kb, S, R, y, sb)) {
+          const float s = e4m3_to_f32(sb);
+          q = k_codes_f32(y, s, __frcp_rn(s));
+        } else {
+          const uint4 r4 = quantize_plain(src + 16 * jb, S);
+          if (r4.w) set_flag(flag, KVQ_FLAG_NONFINITE);
+          q = make_uint2(r4.x, r4.y);
+          sb = r4.z;
+        }
+        codes[2 * jb] = q.x;
+        codes[2 * jb + 1] = q.y;
+        scales |= sb << (8 * jb);
       }
     } else {
       Raw16 kb[BK];
@@ -330,7 +375,7 @@ __global__ void __launch_bounds__(256, kAppendMinCtas) append_fp4_kernel(const k
     const uint16_t* src = v + ((row + (pos + hf - sp)) * hkv + h) * D + 16 * j0;
 #pragma unroll
     for (int jb = 0; jb < BV; ++jb) {
-      if (m && !NV) {
+      if (m) {
         load_raw16(src + 16 * jb, vb[hf][jb]);
       } else {
 #pragma unroll
@@ -351,19 +396,24 @@ __global__ void __launch_bounds__(256, kAppendMinCtas) append_fp4_kernel(const k
     uint4* dst = reinterpret_cast<uint4*>(grp + vblk);
     uint4 codes;
     uint32_t sb0 = 0, sb1 = 0;
+    const float S = NV ? __ldg(static_cast<const float*>(c.v_scale) + h) : 1.0f;
+    float y0[16], y1[16];
     if (!NV && vb[0][jb].finite && vb[1][jb].finite) {
       sb0 = block_scale_byte(vb[0][jb].amax);
       sb1 = block_scale_byte(vb[1][jb].amax);
       const float s0 = e4m3_to_f32(sb0), s1 = e4m3_to_f32(sb1);
       codes = v_pair_codes_finite(vb[0][jb].w, s0, __frcp_rn(s0), vb[1][jb].w, s1, __frcp_rn(s1));
+    } else if (NV && nv_fast_scale(S) && nv_quotients(vb[0][jb], S, __frcp_rn(S), y0, sb0) &&
+               nv_quotients(vb[1][jb], S, __frcp_rn(S), y1, sb1)) {
+      const float s0 = e4m3_to_f32(sb0), s1 = e4m3_to_f32(sb1);
+      codes = v_pair_codes_f32(y0, s0, __frcp_rn(s0), y1, s1, __frcp_rn(s1));
     } else {
-      const float S = NV ? __ldg(static_cast<const float*>(c.v_scale) + h) : 1.0f;
       uint64_t lo = 0, hi = 0;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         if (!(hf ? mine1 : mine0)) continue;
         const uint16_t* vsrc = v + ((row + (pos + hf - sp)) * hkv + h) * D + 16 * j;
-        const uint4 q = NV ? quantize_nv(vsrc, S) : quantize_plain(vsrc, S);
+        const uint4 q = quantize_plain(vsrc, S);
         if (q.w) set_flag(flag, KVQ_FLAG_NONFINITE);
         lo |= spread_nibbles(q.x) << (4 * hf);
         hi |= spread_nibbles(q.y) << (4 * hf);

@@ -1,33 +1,54 @@
-// Exhaustive check behind the NVFP4 append's division-free quotient: for every
-// fp32 y in [1, 2) and every E4M3 significand s in {1, 1.125, ..., 1.875},
-// q' = fma(-fma(q, s, -y), r, q) with r = RN(1/s) and q = RN(y * r) equals the
-// IEEE fp32 quotient RN(y / s).  All steps scale exactly with the exponents of y
-// and s while the values stay normal, so this covers every y and every E4M3
-// scale (subnormal E4M3 scales have significands in the same set).  Exit status
-// 0 when every case matches.
+// Exhaustive checks behind the append's division-free quotients.  Both take
+// q = RN(y * r) with r = RN(1/s), then q' = fma(-fma(q, s, -y), r, q), and
+// require q' == RN(y / s), the IEEE fp32 quotient:
+//   1. every fp32 y in [1, 2) against every E4M3 significand s in
+//      {1, 1.125, ..., 1.875} (the block scale, and the divisor 6 of amax/6);
+//   2. every bf16 y in [1, 2) (the 2^7 significands of the input) against
+//      every fp32 s in [1, 2) (the NVFP4 second-level scale).
+// All steps scale exactly with the exponents of y and s while the values stay
+// normal, so these cover every normal dividend and divisor of each kind.
+// Exit status 0 when every case matches.
 #include <math.h>
 #include <stdint.h>
 #include <stdio.h>
 #include <string.h>
 static float f_of(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
 static uint32_t u_of(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+static volatile float g_one = 1.0f;  // keeps the compiler from folding the probe below
+
+static long check(float y, float s, float r, long* bad, const char* what) {
+  const float q = y * r;
+  const float q2 = fmaf(-fmaf(q, s, -y), r, q);
+  const float ref = y / s;
+  if (u_of(q2) != u_of(ref)) {
+    if (*bad < 5) printf("%s mismatch s=%a y=%a q2=%a ref=%a\n", what, s, y, q2, ref);
+    ++*bad;
+  }
+  return 1;
+}
+
 int main(void) {
+  // fmaf must round once: (1 + 2^-23)^2 - (1 + 2^-22) is 2^-46 exactly,
+  // and 0 when the product is rounded first
+  const float e = g_one + 0x1p-23f;
+  if (fmaf(e, e, -(g_one + 0x1p-22f)) != 0x1p-46f) {
+    printf("fmaf is not fused on this host\n");
+    return 2;
+  }
   long bad = 0, total = 0;
   for (int m = 0; m < 8; ++m) {
     const float s = 1.0f + m / 8.0f;
     const float r = 1.0f / s;
-    for (uint32_t k = 0; k < (1u << 23); ++k) {
-      const float y = f_of(0x3F800000u | k);
-      const float q = y * r;
-      const float q2 = fmaf(-fmaf(q, s, -y), r, q);
-      const float ref = y / s;
-      ++total;
-      if (u_of(q2) != u_of(ref)) {
-        if (bad < 5) printf("mismatch s=%g y=%a q2=%a ref=%a\n", s, y, q2, ref);
-        ++bad;
-      }
-    }
+    for (uint32_t k = 0; k < (1u << 23); ++k) total += check(f_of(0x3F800000u | k), s, r, &bad, "e4m3");
   }
-  printf("checked %ld, mismatches %ld\n", total, bad);
+  printf("e4m3 divisors: checked %ld, mismatches %ld\n", total, bad);
+  const long bad1 = bad;
+  total = 0;
+  for (uint32_t k = 0; k < (1u << 23); ++k) {
+    const float s = f_of(0x3F800000u | k);
+    const float r = 1.0f / s;
+    for (uint32_t j = 0; j < 128; ++j) total += check(f_of(0x3F800000u | (j << 16)), s, r, &bad, "fp32");
+  }
+  printf("fp32 divisors, bf16 dividends: checked %ld, mismatches %ld\n", total, bad - bad1);
   return bad != 0;
 }

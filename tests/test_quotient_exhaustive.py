@@ -1,9 +1,13 @@
-"""The append's division-free quotient for NVFP4 blocks (the value already
-divided by the kv head's fp32 scale, then by the block's E4M3 scale) relies on
-y * RN(1/s) plus one fused residual correction being exactly the IEEE fp32
-y / s.  This runs the exhaustive host check of that identity (all 2^23
-significands of y against the eight E4M3 significands) in IEEE fp32 with
-fused multiply-adds, as the GPU computes it."""
+"""The append's division-free quotients rely on y * RN(1/s) plus one fused
+residual correction being exactly the IEEE fp32 y / s for the divisors and
+dividends it meets:
+  * an E4M3 block scale (and the divisor 6 of amax/6) with any fp32 dividend,
+    the NVFP4 value already divided by the kv head's scale included;
+  * the NVFP4 kv head's fp32 second-level scale with a bf16 input value.
+This runs the exhaustive host check of both identities (all 2^23 fp32
+significands against the eight E4M3 significands; all 2^7 bf16 significands
+against all 2^23 fp32 significands) in IEEE fp32 with fused multiply-adds, as
+the GPU computes them."""
 import os
 import subprocess
 import tempfile
@@ -11,11 +15,12 @@ import tempfile
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-def test_reciprocal_quotient_is_the_ieee_quotient_for_e4m3_divisors():
+def test_reciprocal_quotient_is_the_ieee_quotient():
     with tempfile.TemporaryDirectory() as d:
         exe = os.path.join(d, "quotient_check")
         subprocess.run(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-o", exe,
                         os.path.join(HERE, "native", "quotient_check.c"), "-lm"], check=True)
-        r = subprocess.run([exe], capture_output=True, text=True)
+        r = subprocess.run([exe], capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout
-    assert "mismatches 0" in r.stdout
+    assert "e4m3 divisors: checked 67108864, mismatches 0" in r.stdout
+    assert "fp32 divisors, bf16 dividends: checked 1073741824, mismatches 0" in r.stdout
