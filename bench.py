@@ -148,16 +148,16 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic(profile=PROFILE, src=DECODE_SRC):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
+def profiled_traffic(profile=PROFILE, src=DECODE_SRC, key="traffic_bytes_per_launch"):
+    """DRAM bytes per launch (the summary's line `key`) from a committed ncu
+    summary, if it was taken on the current kernel source (else None)."""
     try:
         text = open(profile).read()
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
         fields = dict(line.split(":", 1) for line in text.splitlines() if line.startswith(("traffic_", "source_")))
         if fields.get("source_sha256", "").strip() != sha:
             return None
-        return int(float(fields["traffic_bytes_per_launch"].strip()))
+        return int(float(fields[key].strip()))
     except Exception:
         return None
 
@@ -589,7 +589,8 @@ def run_prefill(args, dist: Dist):
                    "parallelism": f"replicas x{dist.world}"},
         "roofline": {"bound": "hbm", "kernel": "append_fp4_kernel", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
-                     "traffic": profiled_traffic(APPEND_PROFILE, APPEND_SRC),
+                     "traffic": profiled_traffic(APPEND_PROFILE, APPEND_SRC,
+                                                 "traffic_bytes_per_launch_nvfp4" if nv else "traffic_bytes_per_launch"),
                      "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": secs * 1e3 / K},
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": 2 * k.numel() * 2, "d2h_bytes_per_step": 4,
                 "steps": Ke},
