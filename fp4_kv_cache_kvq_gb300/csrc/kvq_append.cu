@@ -162,20 +162,23 @@ __device__ __noinline__ uint4 quantize_plain(const uint16_t* src, float S) {
 // second-level scale, with the codes and scale byte of the IEEE fp32
 // divisions and no division on the way:
 //   y = block_quotient(x, S, RN(1/S)) is the IEEE fp32 x / S for every bf16
-//     x and every fp32 S: checked exhaustively over the 2^7 significands of
-//     x against all 2^23 significands of S; the steps scale exactly with
-//     both exponents while the values stay normal, and a quotient that falls
-//     below the normal range keeps its sign and lies far under the first
-//     E2M1 midpoint of any block scale (s >= 2^-9), so its code is the
-//     signed zero either way;
+//     x and every fp32 S while the residual x - q*S is exact: checked
+//     exhaustively over the 2^7 significands of x against all 2^23
+//     significands of S, the steps scaling exactly with both exponents.  The
+//     residual is a multiple of about 2^-47 |x|, exact down to |x| = 2^-102;
+//     with S >= 2^-90 a smaller x gives |x / S| < 2^-12, far under the first
+//     E2M1 midpoint of any block scale (s >= 2^-9), where only the sign
+//     reaches the code, and the sign is always kept.  S < 2^-90 (where tiny
+//     x would give wrong codes) and S > 2^126 (a subnormal 1/S) take the
+//     IEEE path;
 //   max |y| = RN(max |x| / S) (rounding is monotone), taken once per block;
 //   amax(y) / 6 and y / s by block_quotient as well: 6 and every E4M3 scale
 //     have E4M3 significands, for which that quotient equals the IEEE one
 //     for every fp32 dividend (exhaustive over the 2^23 significands).
-// nv_fast_scale says whether S and RN(1/S) are normal; a block whose largest
+// nv_fast_scale says whether S is in [2^-90, 2^126]; a block whose largest
 // quotient is not finite (Inf/NaN input or overflow of x / S) returns false
 // and takes quantize_plain, which flags it.
-__device__ __forceinline__ bool nv_fast_scale(float S) { return S >= 0x1p-126f && S <= 0x1p126f; }
+__device__ __forceinline__ bool nv_fast_scale(float S) { return S >= 0x1p-90f && S <= 0x1p126f; }
 
 __device__ __forceinline__ bool nv_quotients(const Raw16& b, float S, float R, float (&y)[16], uint32_t& sb) {
   if (!b.finite) return false;

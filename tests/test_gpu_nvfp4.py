@@ -117,3 +117,96 @@ def test_nvfp4_needs_its_scales():
     st = kvq.load().kvq_append(ctypes.byref(s), 1, 1, start.data_ptr(), k.data_ptr(), k.data_ptr(), None,
                                torch.cuda.current_stream().cuda_stream)
     assert st == 1  # KVQ_ERR_INVALID_ARGUMENT, nothing enqueued
+
+
+# One second-level scale per kv head across the fp32 range, with the decimal
+# span of x / S its blocks take: the division-free path's ends 2^-90 (tiny
+# x included: x below 2^-102 gives |x / S| < 2^-12) and 2^126, just outside
+# them 2^-91 and 1e38 (IEEE path), a subnormal S, S = 1e-37 with x / S
+# overflowing for the larger blocks (flagged, saturated codes), and two
+# ordinary scales.
+RANGE_SCALES = [(2.0 ** -90, -14, 12), (2.0 ** -91, -14, 12), (1e-37, -10, 41), (1e-38, -10, 10),
+                (3.7e-20, -12, 12), (0.3, -30, 30), (2.0 ** 126, -12, 1), (1e38, -12, 1)]
+
+
+def _range_blocks(scales, n, d, g):
+    """bf16-valued [n][Hkv][d]: per 16-value block, N(0,1) times 10^u with
+    u uniform in log10(S_h) + [lo, hi] (kept inside the bf16 range)."""
+    out = np.empty((n, len(scales), d), np.float32)
+    for h, (S, lo, hi) in enumerate(scales):
+        u = torch.empty(n, d // 16).uniform_(lo, hi, generator=g) + math.log10(S)
+        u = u.clamp(-45.0, 37.5).repeat_interleave(16, dim=-1)
+        x = torch.randn(n, d, generator=g, dtype=torch.float64) * 10.0 ** u.double()
+        out[:, h] = x.float().to(torch.bfloat16).float().numpy()
+    return out
+
+
+def _append_with_scales(k: np.ndarray, v: np.ndarray, Sk, Sv):
+    """Append bf16-valued arrays [n][Hkv][d] as one sequence under the given
+    per-head second-level scales; return the cache and the error flag."""
+    n, hkv, d = k.shape
+    P = 64
+    pages = -(-n // P)
+    cache = kvq.Fp4Cache(hkv, d, P, pages, pages, nvfp4=True)
+    cache.k_gscale.copy_(torch.tensor(Sk, dtype=torch.float32))
+    cache.v_gscale.copy_(torch.tensor(Sv, dtype=torch.float32))
+    kt = torch.from_numpy(k).to(torch.bfloat16)
+    vt = torch.from_numpy(v).to(torch.bfloat16)
+    assert torch.equal(kt.float(), torch.from_numpy(k)) and torch.equal(vt.float(), torch.from_numpy(v))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq.append(cache, torch.zeros(1, dtype=torch.int32, device="cuda"), kt[None].cuda(), vt[None].cuda(), err=err)
+    torch.cuda.synchronize()
+    return cache, int(err.item())
+
+
+def _check_against_oracle(cache, k, v, Sk, Sv):
+    n, hkv, _ = k.shape
+    bad = 0
+    for h in range(hkv):
+        kc, ks, vc, vs = gather_unit_bytes(cache, None, 0, h, n)
+        okc, oks, kbad = oracle.nvfp4_quantize_rows(k[:, h], float(np.float32(Sk[h])))
+        ovc, ovs, vbad = oracle.nvfp4_quantize_rows(v[:, h], float(np.float32(Sv[h])))
+        assert np.array_equal(ks, oks) and np.array_equal(kc, okc), ("K", h, Sk[h])
+        assert np.array_equal(vs, ovs) and np.array_equal(vc, ovc), ("V", h, Sv[h])
+        bad += kbad + vbad
+    return bad
+
+
+def test_second_level_scales_across_the_fp32_range():
+    """Blocks around each scale of RANGE_SCALES (V takes them in reverse
+    order): codes and scale bytes equal the oracle's IEEE divisions bit for
+    bit, and the non-finite flag is raised exactly when some x / S
+    overflows.  Every branch of the append's NVFP4 path runs here; the rare
+    inputs where a one-ulp error in x / S would move a code across an E2M1
+    midpoint are pinned by the host check in test_quotient_exhaustive.py."""
+    hkv, d, n = len(RANGE_SCALES), 128, 96
+    g = torch.Generator().manual_seed(21)
+    k = _range_blocks(RANGE_SCALES, n, d, g)
+    v = _range_blocks(RANGE_SCALES[::-1], n, d, g)
+    Sk = [S for S, _, _ in RANGE_SCALES]
+    Sv = Sk[::-1]
+    cache, flag = _append_with_scales(k, v, Sk, Sv)
+    bad = _check_against_oracle(cache, k, v, Sk, Sv)
+    assert bad > 0  # the 1e-37 head overflows
+    assert flag == kvq.FLAG_NONFINITE
+
+
+def test_ties_and_special_blocks_under_a_second_level_scale():
+    """Every E2M1 tie, saturation, signed zeros and tiny values, scaled by an
+    exact power of two so that x / S lands on them exactly, through the
+    division-free path."""
+    rows = [np.zeros(16), np.full(16, -0.0), np.full(16, 2.0 ** -12),
+            np.array([6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -1.25, -1.75, -2.5, -3.5, -5.0, -6.0]),
+            np.array([3000.0] + [1.0] * 15), np.array([2688.0, -2688.0] + [0.0] * 14),
+            np.array([9 * 2.0 ** -9] + [0.0] * 15), np.array([1e-30] * 8 + [-1e-30] * 8)]
+    S = 0.25
+    blk = np.array(rows, np.float64) * S
+    blk = torch.tensor(blk, dtype=torch.float32).to(torch.bfloat16).float().numpy()
+    n = blk.shape[0]
+    k = np.zeros((n, 2, 128), np.float32)
+    k[:, :, :16] = blk[:, None, :]
+    k[:, :, 64:80] = -blk[:, None, :]
+    v = k[::-1].copy()
+    cache, flag = _append_with_scales(k, v, [S, 3.0 * S], [S, S])
+    assert _check_against_oracle(cache, k, v, [S, 3.0 * S], [S, S]) == 0
+    assert flag == 0
