@@ -210,3 +210,40 @@ def test_ties_and_special_blocks_under_a_second_level_scale():
     cache, flag = _append_with_scales(k, v, [S, 3.0 * S], [S, S])
     assert _check_against_oracle(cache, k, v, [S, 3.0 * S], [S, S]) == 0
     assert flag == 0
+
+
+@pytest.mark.parametrize("d,mag,T", [(128, 1.0, 300), (64, 3e3, 300), (128, 3e3, 50)])
+def test_decode_with_fp8_window(d, mag, T):
+    """An NVFP4 global cache with the FP8 sliding window (W = 64): positions
+    before the window from the NVFP4 cache with both second-level scales,
+    the last min(W, T) from the FP8 ring, one softmax; T = 50 reads the
+    window alone."""
+    W = 64
+    w = workloads.scaled(BASE, batch=2, num_kv_heads=2, num_q_heads=8, head_dim=d,
+                         k_outlier_channels=(3, 17, 40) if d == 64 else (3, 17, 64, 101))
+    cache, K, V = _build(w, T, mag, seed=7 + d)
+    B, hkv, G = w.batch, w.num_kv_heads, w.group
+    swa = kvq.Fp8WindowCache(B, hkv, d, W)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    w0 = min(W, T)
+    kw, vw = K[:, T - w0:].contiguous(), V[:, T - w0:].contiguous()
+    kvq.fp8_set_scales(swa, kw, vw, err=err)
+    kvq.append(swa, torch.full((B,), T - w0, dtype=torch.int32, device="cuda"), kw, vw, err=err)
+    lens = torch.full((B,), T, dtype=torch.int32, device="cuda")
+    q = workloads.queries(w, seed=d, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    out = kvq.decode_attn(cache, lens, q, scale, swa=swa, err=err).cpu().numpy()
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    Kh, Vh = K.float().cpu().numpy(), V.float().cpu().numpy()
+    kwh, vwh = kw.float().cpu().numpy(), vw.float().cpu().numpy()
+    Sk, Sv = cache.k_gscale.cpu().numpy(), cache.v_gscale.cpu().numpy()
+    qh = q.float().cpu().numpy()
+    for h in range(hkv):
+        sk = oracle.fp8_head_scale(kwh[:, :, h])
+        sv = oracle.fp8_head_scale(vwh[:, :, h])
+        assert swa.k_scales[h].item() == sk and swa.v_scales[h].item() == sv
+        for b in range(B):
+            ref, vmax = oracle.decode_unit(qh[b, h * G:(h + 1) * G], Kh[b, :, h], Vh[b, :, h], scale, window=W,
+                                           swa_scales=(sk, sv), nvfp4_scales=(float(Sk[h]), float(Sv[h])))
+            assert np.abs(out[b, h * G:(h + 1) * G] - ref).max() <= TOL * vmax
