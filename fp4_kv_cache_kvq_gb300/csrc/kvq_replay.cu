@@ -13,16 +13,23 @@
 // with each layer's q, k, v taken from that layer's input.
 //
 // Work is data-parallel over positions.  Per layer:
-//   swa_proj_kernel  8 positions per CTA, thread = output channel: RMS
-//                    normalisation (fixed-order reductions), q, k, v with the
-//                    transposed weights read coalesced; the last n_win
-//                    positions' k, v also go to the caller's state array
-//   swa_attn_kernel  one CTA per position: window scores by warp dot
-//                    products, softmax with fixed-order block reductions, the
-//                    weighted sum of V, Wo, the residual update in place
+//   swa_proj_kernel  8 positions and one of q, k, v per CTA, thread = output
+//                    channel: RMS normalisation (fixed-order reductions),
+//                    the projection with the transposed weight read
+//                    coalesced; the last n_win positions' k, v also go to
+//                    the caller's state array
+//   swa_attn_kernel  8 positions per CTA, one warp each for the scores and
+//                    the softmax: the window rows of all 8 are staged 64 at a
+//                    time in shared memory (the next tile loaded into
+//                    registers meanwhile) and each lane takes two rows' dot
+//                    products; the probabilities are laid out by row so that
+//                    each V value loaded serves 4 positions; then Wo and the
+//                    residual update in place
 // A position's arithmetic depends only on its window's contents, in an order
-// fixed by the offset within the window, so a replay from the exact start
-// reproduces the whole sequence's state bit for bit.
+// fixed by the offset within the window (rows outside a position's window
+// enter its V sum with probability zero, which leaves the sum unchanged), so
+// a replay from the exact start reproduces the whole sequence's state bit for
+// bit.
 #include "kvq_common.cuh"
 #include "kvq_host.cuh"
 
@@ -30,7 +37,18 @@ namespace kvq {
 namespace {
 
 constexpr int kProjPos = 8;     // positions per projection CTA
-constexpr int kMaxWin = 4096;   // window positions held in shared memory
+constexpr int kMaxWin = 4096;   // largest window
+constexpr int kAttnPos = 8;     // positions per attention CTA (a warp each)
+constexpr int kAttnThreads = 32 * kAttnPos;
+constexpr int kKTile = 64;      // window rows staged per tile (two per lane in the scores)
+constexpr int kRowPad = 4;      // floats of padding per staged row
+
+// Shared-memory floats of one attention CTA: query rows [P][D], a staged
+// tile [kKTile][D + kRowPad], probabilities by row [n_win + P][P], the
+// attention outputs by channel [D][P], the softmax sums [P].
+__host__ __device__ constexpr int attn_smem_floats(int d, int n_win) {
+  return kAttnPos * d + kKTile * (d + kRowPad) + (n_win + kAttnPos) * kAttnPos + d * kAttnPos + kAttnPos;
+}
 
 // wt[m][c][r] = w[m][r][c] for each d x d matrix m.
 __global__ void transpose_kernel(const float* __restrict__ w, float* __restrict__ wt, int d) {
@@ -80,8 +98,9 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   return s;
 }
 
-// q, k, v of kProjPos positions from the layer input x; wt = this layer's
-// transposed Wq, Wk, Wv ([3][D][D], wt[m][c][o] = W_m[o][c]).
+// One of q, k, v (blockIdx.y = 0, 1, 2) for kProjPos positions from the
+// layer input x; wt = this layer's transposed Wq, Wk, Wv ([3][D][D],
+// wt[m][c][o] = W_m[o][c]).
 template <int D>
 __global__ void __launch_bounds__(D) swa_proj_kernel(const float* __restrict__ x, const float* __restrict__ wt,
                                                       float* __restrict__ qb, float* __restrict__ kb,
@@ -90,6 +109,7 @@ __global__ void __launch_bounds__(D) swa_proj_kernel(const float* __restrict__ x
   __shared__ float u[kProjPos][D];
   __shared__ float part[kProjPos][D / 32];
   const int o = threadIdx.x, lane = o & 31, wp = o >> 5;
+  const int m = blockIdx.y;
   const int64_t i0 = (int64_t)blockIdx.x * kProjPos;
   float xv[kProjPos];
 #pragma unroll
@@ -108,95 +128,174 @@ __global__ void __launch_bounds__(D) swa_proj_kernel(const float* __restrict__ x
     u[p][o] = xv[p] * (1.0f / sqrtf(ms / (float)D + 1e-6f));
   }
   __syncthreads();
-  float q[kProjPos], k[kProjPos], v[kProjPos];
+  float acc[kProjPos];
 #pragma unroll
-  for (int p = 0; p < kProjPos; ++p) q[p] = k[p] = v[p] = 0.0f;
-#pragma unroll 4
+  for (int p = 0; p < kProjPos; ++p) acc[p] = 0.0f;
+  const float* wm = wt + (size_t)m * D * D + o;
+#pragma unroll 16
   for (int c = 0; c < D; ++c) {
-    const float wq = __ldg(wt + (size_t)(0 * D + c) * D + o);
-    const float wk = __ldg(wt + (size_t)(1 * D + c) * D + o);
-    const float wv = __ldg(wt + (size_t)(2 * D + c) * D + o);
+    const float wc = __ldg(wm + (size_t)c * D);
 #pragma unroll
-    for (int p = 0; p < kProjPos; ++p) {
-      const float uc = u[p][c];
-      q[p] = fmaf(wq, uc, q[p]);
-      k[p] = fmaf(wk, uc, k[p]);
-      v[p] = fmaf(wv, uc, v[p]);
-    }
+    for (int p = 0; p < kProjPos; ++p) acc[p] = fmaf(wc, u[p][c], acc[p]);
   }
+  float* out = m == 0 ? qb : (m == 1 ? kb : vb);
+  float* st = m == 1 ? st_k : (m == 2 ? st_v : nullptr);
 #pragma unroll
   for (int p = 0; p < kProjPos; ++p) {
     const int64_t i = i0 + p;
     if (i >= n) break;
-    qb[i * D + o] = q[p];
-    kb[i * D + o] = k[p];
-    vb[i * D + o] = v[p];
+    out[i * D + o] = acc[p];
     const int64_t j = i - (n - n_win);  // row of the window state
-    if (j >= 0) {
-      st_k[j * D + o] = k[p];
-      st_v[j * D + o] = v[p];
-    }
+    if (st != nullptr && j >= 0) st[j * D + o] = acc[p];
   }
 }
 
-// Position i = blockIdx.x: softmax attention over its window, then
-// x_i += Wo a_i (wot[c][o] = Wo[o][c]).
+// A tile of kKTile rows (from row R, rows past hi read as zeros) of a [n][D]
+// array: NQ float4s per thread, thread t taking float4s t, t + 256, ...
 template <int D>
-__global__ void __launch_bounds__(D) swa_attn_kernel(float* __restrict__ x, const float* __restrict__ qb,
-                                                      const float* __restrict__ kb, const float* __restrict__ vb,
-                                                      const float* __restrict__ wot, int n_win, float scale) {
-  constexpr int NW = D / 32;
-  __shared__ float qs[D];
-  __shared__ float as[D];
-  __shared__ float sc[kMaxWin];
-  __shared__ float red[NW];
-  const int64_t i = blockIdx.x;
-  const int o = threadIdx.x, lane = o & 31, wp = o >> 5;
-  const int64_t s0 = i - n_win + 1 > 0 ? i - n_win + 1 : 0;
-  const int len = (int)(i - s0 + 1);
-  qs[o] = qb[i * D + o];
-  __syncthreads();
-  // scores: window offset r goes to warp r % NW, lanes split the channels
-#pragma unroll 4
-  for (int r = wp; r < len; r += NW) {
-    const float* kr = kb + (s0 + r) * D;
-    float acc = 0.0f;
+__device__ __forceinline__ void load_tile_regs(const float* __restrict__ src, int64_t R, int64_t hi,
+                                               float4 (&reg)[kKTile * D / 4 / kAttnThreads]) {
+  constexpr int NQ = kKTile * D / 4 / kAttnThreads;
 #pragma unroll
-    for (int m = 0; m < D / 32; ++m) acc = fmaf(qs[lane + 32 * m], __ldg(kr + lane + 32 * m), acc);
-    acc = warp_sum(acc);
-    if (lane == 0) sc[r] = acc * scale;
+  for (int q = 0; q < NQ; ++q) {
+    const int e = threadIdx.x + q * kAttnThreads;
+    const int rr = e / (D / 4), c4 = e % (D / 4);
+    reg[q] = R + rr <= hi ? __ldg(reinterpret_cast<const float4*>(src + (R + rr) * D) + c4)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+template <int D>
+__device__ __forceinline__ void store_tile_regs(float* tile, const float4 (&reg)[kKTile * D / 4 / kAttnThreads]) {
+  constexpr int NQ = kKTile * D / 4 / kAttnThreads;
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    const int e = threadIdx.x + q * kAttnThreads;
+    const int rr = e / (D / 4), c4 = e % (D / 4);
+    *reinterpret_cast<float4*>(tile + rr * (D + kRowPad) + 4 * c4) = reg[q];
+  }
+}
+
+// Positions i0 .. i0 + kAttnPos - 1 (i0 = blockIdx.x * kAttnPos): softmax
+// attention over each one's window, then x_i += Wo a_i (wot[c][o] =
+// Wo[o][c]).  The CTA walks the union of the windows, rows lo .. hi.
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads) swa_attn_kernel(float* __restrict__ x, const float* __restrict__ qb,
+                                                                 const float* __restrict__ kb,
+                                                                 const float* __restrict__ vb,
+                                                                 const float* __restrict__ wot, int64_t n, int n_win,
+                                                                 float scale) {
+  constexpr int P = kAttnPos;
+  constexpr int RS = D + kRowPad;  // staged row stride: float4 rows without bank conflicts
+  constexpr int PG = P * D / kAttnThreads;  // positions per thread in PV and Wo (4 at D 128, 2 at 64)
+  constexpr int NQ = kKTile * D / 4 / kAttnThreads;  // float4s of a staged tile per thread
+  static_assert(NQ * kAttnThreads * 4 == kKTile * D, "tile split");
+  extern __shared__ float4 smem4[];
+  float* qs = reinterpret_cast<float*>(smem4);  // [P][D]
+  float* tile = qs + P * D;                     // [kKTile][RS]
+  float* pr = tile + kKTile * RS;               // [n_win + P][P]: probability of row lo + r for position p
+  float* as = pr + (n_win + P) * P;             // [D][P]
+  float* sums = as + D * P;                     // [P]
+  const int tid = threadIdx.x, lane = tid & 31, p = tid >> 5;
+  const int64_t i0 = (int64_t)blockIdx.x * P;
+  const int64_t i = i0 + p;  // this warp's position
+  const bool live = i < n;
+  const int64_t s0 = live ? (i - n_win + 1 > 0 ? i - n_win + 1 : 0) : 0;  // its window: rows s0 .. i
+  const int64_t lo = i0 - n_win + 1 > 0 ? i0 - n_win + 1 : 0;
+  const int64_t hi = (i0 + P < n ? i0 + P : n) - 1;
+  const int rows = (int)(hi - lo + 1);
+  for (int e = tid; e < P * D; e += kAttnThreads) {
+    const int64_t ii = i0 + e / D;
+    qs[e] = ii < n ? qb[ii * D + e % D] : 0.0f;
+  }
+  for (int e = tid; e < rows * P; e += kAttnThreads) pr[e] = 0.0f;
+  // ---- scores: lane = rows lane, lane + 32 of the staged tile, four channel chains.  The
+  // next tile's rows are loaded into registers while this one is used.
+  float4 reg[NQ];
+  load_tile_regs<D>(kb, lo, hi, reg);
+  for (int64_t R = lo; R <= hi; R += kKTile) {
+    __syncthreads();  // the previous tile is consumed (first pass: qs and pr are set)
+    store_tile_regs<D>(tile, reg);
+    __syncthreads();
+    if (R + kKTile <= hi) load_tile_regs<D>(kb, R + kKTile, hi, reg);
+#pragma unroll
+    for (int h2 = 0; h2 < kKTile / 32; ++h2) {
+      const int rr = lane + 32 * h2;
+      const int64_t s = R + rr;
+      if (live && s >= s0 && s <= i) {
+        const float4* qr = reinterpret_cast<const float4*>(qs + p * D);
+        const float4* kr = reinterpret_cast<const float4*>(tile + rr * RS);
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 8
+        for (int c4 = 0; c4 < D / 4; ++c4) {
+          const float4 a = qr[c4], b = kr[c4];
+          a0 = fmaf(a.x, b.x, a0);
+          a1 = fmaf(a.y, b.y, a1);
+          a2 = fmaf(a.z, b.z, a2);
+          a3 = fmaf(a.w, b.w, a3);
+        }
+        pr[(s - lo) * P + p] = ((a0 + a1) + (a2 + a3)) * scale;
+      }
+    }
+  }
+  load_tile_regs<D>(vb, lo, hi, reg);  // the first V tile, in flight during the softmax
+  __syncwarp();
+  // ---- softmax of this warp's position: lane l takes window offsets l, l + 32, ...
+  if (live) {
+    const int len = (int)(i - s0 + 1);
+    float* col = pr + (s0 - lo) * P + p;  // offset r at col[r * P]
+    float mx = -INFINITY;
+    for (int r = lane; r < len; r += 32) mx = fmaxf(mx, col[r * P]);
+    mx = warp_max(mx);
+    float sum = 0.0f;
+    for (int r = lane; r < len; r += 32) {
+      const float e = expf(col[r * P] - mx);
+      col[r * P] = e;
+      sum += e;
+    }
+    sum = warp_sum(sum);
+    if (lane == 0) sums[p] = sum;
+  } else if (lane == 0) {
+    sums[p] = 1.0f;
   }
   __syncthreads();
-  float mx = -INFINITY;
-  for (int r = o; r < len; r += D) mx = fmaxf(mx, sc[r]);
-  mx = block_max<D>(mx, red);
-  float sum = 0.0f;
-  for (int r = o; r < len; r += D) {
-    const float p = expf(sc[r] - mx);
-    sc[r] = p;
-    sum += p;
-  }
-  sum = block_sum<D>(sum, red);  // its barriers also publish the p values
-  // weighted sum of V: four independent chains (window offset mod 4), joined
-  // in a fixed order
-  // (16 rows' loads issued before their multiply-adds)
-  float a4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  const float* vcol = vb + s0 * D + o;
-  int r = 0;
-  for (; r + 16 <= len; r += 16) {
-    float vv[16];
+  // ---- weighted sum of V: thread = (channel, group of PG positions), rows
+  // in order, V staged a tile at a time like K
+  const int c = tid % D, g = tid / D;
+  float acc[PG];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) vv[k] = __ldg(vcol + (int64_t)(r + k) * D);
+  for (int k = 0; k < PG; ++k) acc[k] = 0.0f;
+  for (int64_t R = lo; R <= hi; R += kKTile) {
+    __syncthreads();  // the previous tile is consumed (first pass: the softmax is done)
+    store_tile_regs<D>(tile, reg);
+    __syncthreads();
+    if (R + kKTile <= hi) load_tile_regs<D>(vb, R + kKTile, hi, reg);
+    const int nr = hi - R + 1 < kKTile ? (int)(hi - R + 1) : kKTile;
+    const float* pcol = pr + (R - lo) * P + g * PG;
+#pragma unroll 8
+    for (int r = 0; r < nr; ++r) {
+      const float vv = tile[r * RS + c];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) a4[k & 3] = fmaf(sc[r + k], vv[k], a4[k & 3]);
+      for (int j = 0; j < PG; ++j) acc[j] = fmaf(pcol[r * P + j], vv, acc[j]);
+    }
   }
-  for (; r < len; ++r) a4[r & 3] = fmaf(sc[r], __ldg(vcol + (int64_t)r * D), a4[r & 3]);
-  as[o] = ((a4[0] + a4[1]) + (a4[2] + a4[3])) / sum;
+#pragma unroll
+  for (int j = 0; j < PG; ++j) as[c * P + g * PG + j] = acc[j] / sums[g * PG + j];
   __syncthreads();
-  float y = 0.0f;
-#pragma unroll 4
-  for (int c = 0; c < D; ++c) y = fmaf(__ldg(wot + (size_t)c * D + o), as[c], y);
-  x[i * D + o] += y;
+  // ---- x_i += Wo a_i: thread = (output channel, the same positions)
+  float y[PG];
+#pragma unroll
+  for (int j = 0; j < PG; ++j) y[j] = 0.0f;
+#pragma unroll 16
+  for (int cc = 0; cc < D; ++cc) {
+    const float wv = __ldg(wot + (size_t)cc * D + c);
+#pragma unroll
+    for (int j = 0; j < PG; ++j) y[j] = fmaf(wv, as[cc * P + g * PG + j], y[j]);
+  }
+#pragma unroll
+  for (int j = 0; j < PG; ++j) {
+    const int64_t ii = i0 + g * PG + j;
+    if (ii < n) x[ii * D + c] += y[j];
+  }
 }
 
 template <int D>
@@ -210,14 +309,26 @@ kvq_status run_replay(const float* w, int layers, const float* emb, int64_t n, i
   transpose_kernel<<<dim3(D / 32, D / 32, 4 * layers), dim3(32, 8), 0, st>>>(w, wt, D);
   if (cudaMemcpyAsync(xb, emb, (size_t)n * D * sizeof(float), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
     return KVQ_ERR_CUDA;
+  static DeviceOnce attr_set;  // the attention kernel's shared-memory opt-in, once per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (attr_set.pending(dev)) {
+    if (cudaFuncSetAttribute(swa_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             attn_smem_floats(D, kMaxWin) * (int)sizeof(float)) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+    attr_set.mark(dev);
+  }
   const float scale = 1.0f / sqrtf((float)D);
-  const unsigned proj_grid = (unsigned)((n + kProjPos - 1) / kProjPos);
+  const dim3 proj_grid((unsigned)((n + kProjPos - 1) / kProjPos), 3);
+  const unsigned attn_grid = (unsigned)((n + kAttnPos - 1) / kAttnPos);
+  const int attn_smem = attn_smem_floats(D, n_win) * (int)sizeof(float);
   for (int l = 0; l < layers; ++l) {
     const float* wl = wt + (size_t)4 * l * D * D;
     float* st_k = states + (size_t)(2 * l) * n_win * D;
     float* st_v = states + (size_t)(2 * l + 1) * n_win * D;
     swa_proj_kernel<D><<<proj_grid, D, 0, st>>>(xb, wl, qb, kb, vb, st_k, st_v, n, n_win);
-    swa_attn_kernel<D><<<(unsigned)n, D, 0, st>>>(xb, qb, kb, vb, wl + (size_t)3 * D * D, n_win, scale);
+    swa_attn_kernel<D><<<attn_grid, kAttnThreads, attn_smem, st>>>(xb, qb, kb, vb, wl + (size_t)3 * D * D, n,
+                                                                   n_win, scale);
   }
   if (hidden != nullptr &&
       cudaMemcpyAsync(hidden, xb, (size_t)n * D * sizeof(float), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
