@@ -14,17 +14,18 @@
 //
 // Work is data-parallel over positions.  Per layer:
 //   swa_proj_kernel  8 positions and one of q, k, v per CTA, thread = output
-//                    channel: RMS normalisation (fixed-order reductions),
-//                    the projection with the transposed weight read
-//                    coalesced; the last n_win positions' k, v also go to
-//                    the caller's state array
+//                    channel: the transposed weight copied to shared memory
+//                    (cp.async) during the RMS normalisation (fixed-order
+//                    reductions), then the projection; the last n_win
+//                    positions' k, v also go to the caller's state array
 //   swa_attn_kernel  8 positions per CTA, one warp each for the scores and
-//                    the softmax: the window rows of all 8 are staged 64 at a
+//                    the softmax: the window rows of all 8 are staged 32 at a
 //                    time in shared memory (the next tile loaded into
-//                    registers meanwhile) and each lane takes two rows' dot
-//                    products; the probabilities are laid out by row so that
-//                    each V value loaded serves 4 positions; then Wo and the
-//                    residual update in place
+//                    registers meanwhile) and each lane takes a row's dot
+//                    product; the probabilities are laid out by row so that
+//                    each V value loaded serves 4 positions; then Wo (copied
+//                    to shared memory from the start) and the residual
+//                    update in place
 // A position's arithmetic depends only on its window's contents, in an order
 // fixed by the offset within the window (rows outside a position's window
 // enter its V sum with probability zero, which leaves the sum unchanged), so
@@ -40,14 +41,29 @@ constexpr int kProjPos = 8;     // positions per projection CTA
 constexpr int kMaxWin = 4096;   // largest window
 constexpr int kAttnPos = 8;     // positions per attention CTA (a warp each)
 constexpr int kAttnThreads = 32 * kAttnPos;
-constexpr int kKTile = 64;      // window rows staged per tile (two per lane in the scores)
+constexpr int kKTile = 32;      // window rows staged per tile (a lane each in the scores)
 constexpr int kRowPad = 4;      // floats of padding per staged row
 
 // Shared-memory floats of one attention CTA: query rows [P][D], a staged
 // tile [kKTile][D + kRowPad], probabilities by row [n_win + P][P], the
-// attention outputs by channel [D][P], the softmax sums [P].
+// attention outputs by channel [D][P], the softmax sums [P], then the
+// layer's transposed Wo [D][D] (every region a multiple of 4 floats).
 __host__ __device__ constexpr int attn_smem_floats(int d, int n_win) {
-  return kAttnPos * d + kKTile * (d + kRowPad) + (n_win + kAttnPos) * kAttnPos + d * kAttnPos + kAttnPos;
+  return kAttnPos * d + kKTile * (d + kRowPad) + (n_win + kAttnPos) * kAttnPos + d * kAttnPos + kAttnPos + d * d;
+}
+
+// 16-byte asynchronous copy global -> shared; a thread's copies are complete
+// after cp_async_wait_all, and visible to the CTA after a barrier.
+__device__ __forceinline__ void cp_async16(float* smem, const float* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+// Copy a [D][D] float matrix into shared memory, 16 bytes per copy, spread
+// over `nthreads` threads.
+template <int D>
+__device__ __forceinline__ void stage_matrix(float* dst, const float* __restrict__ src, int nthreads) {
+  for (int e = threadIdx.x; e < D * D / 4; e += nthreads) cp_async16(dst + 4 * e, src + 4 * e);
 }
 
 // wt[m][c][r] = w[m][r][c] for each d x d matrix m.
@@ -108,8 +124,11 @@ __global__ void __launch_bounds__(D) swa_proj_kernel(const float* __restrict__ x
                                                       float* __restrict__ st_v, int64_t n, int n_win) {
   __shared__ float u[kProjPos][D];
   __shared__ float part[kProjPos][D / 32];
+  extern __shared__ float4 proj_smem4[];
+  float* wsm = reinterpret_cast<float*>(proj_smem4);  // [D][D]: wsm[c * D + o] = W_m[o][c]
   const int o = threadIdx.x, lane = o & 31, wp = o >> 5;
   const int m = blockIdx.y;
+  stage_matrix<D>(wsm, wt + (size_t)m * D * D, D);  // in flight during the normalisation
   const int64_t i0 = (int64_t)blockIdx.x * kProjPos;
   float xv[kProjPos];
 #pragma unroll
@@ -127,14 +146,14 @@ __global__ void __launch_bounds__(D) swa_proj_kernel(const float* __restrict__ x
     for (int w = 1; w < D / 32; ++w) ms += part[p][w];
     u[p][o] = xv[p] * (1.0f / sqrtf(ms / (float)D + 1e-6f));
   }
+  cp_async_wait_all();  // this thread's part of W_m
   __syncthreads();
   float acc[kProjPos];
 #pragma unroll
   for (int p = 0; p < kProjPos; ++p) acc[p] = 0.0f;
-  const float* wm = wt + (size_t)m * D * D + o;
-#pragma unroll 16
+#pragma unroll 8
   for (int c = 0; c < D; ++c) {
-    const float wc = __ldg(wm + (size_t)c * D);
+    const float wc = wsm[c * D + o];
 #pragma unroll
     for (int p = 0; p < kProjPos; ++p) acc[p] = fmaf(wc, u[p][c], acc[p]);
   }
@@ -195,6 +214,8 @@ __global__ void __launch_bounds__(kAttnThreads) swa_attn_kernel(float* __restric
   float* pr = tile + kKTile * RS;               // [n_win + P][P]: probability of row lo + r for position p
   float* as = pr + (n_win + P) * P;             // [D][P]
   float* sums = as + D * P;                     // [P]
+  float* wos = sums + P;                        // [D][D]: wos[c * D + o] = Wo[o][c]
+  stage_matrix<D>(wos, wot, kAttnThreads);      // in flight until the Wo phase
   const int tid = threadIdx.x, lane = tid & 31, p = tid >> 5;
   const int64_t i0 = (int64_t)blockIdx.x * P;
   const int64_t i = i0 + p;  // this warp's position
@@ -208,7 +229,7 @@ __global__ void __launch_bounds__(kAttnThreads) swa_attn_kernel(float* __restric
     qs[e] = ii < n ? qb[ii * D + e % D] : 0.0f;
   }
   for (int e = tid; e < rows * P; e += kAttnThreads) pr[e] = 0.0f;
-  // ---- scores: lane = rows lane, lane + 32 of the staged tile, four channel chains.  The
+  // ---- scores: lane = row of the staged tile, four channel chains.  The
   // next tile's rows are loaded into registers while this one is used.
   float4 reg[NQ];
   load_tile_regs<D>(kb, lo, hi, reg);
@@ -217,24 +238,20 @@ __global__ void __launch_bounds__(kAttnThreads) swa_attn_kernel(float* __restric
     store_tile_regs<D>(tile, reg);
     __syncthreads();
     if (R + kKTile <= hi) load_tile_regs<D>(kb, R + kKTile, hi, reg);
-#pragma unroll
-    for (int h2 = 0; h2 < kKTile / 32; ++h2) {
-      const int rr = lane + 32 * h2;
-      const int64_t s = R + rr;
-      if (live && s >= s0 && s <= i) {
-        const float4* qr = reinterpret_cast<const float4*>(qs + p * D);
-        const float4* kr = reinterpret_cast<const float4*>(tile + rr * RS);
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    const int64_t s = R + lane;
+    if (live && s >= s0 && s <= i) {
+      const float4* qr = reinterpret_cast<const float4*>(qs + p * D);
+      const float4* kr = reinterpret_cast<const float4*>(tile + lane * RS);
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll 8
-        for (int c4 = 0; c4 < D / 4; ++c4) {
-          const float4 a = qr[c4], b = kr[c4];
-          a0 = fmaf(a.x, b.x, a0);
-          a1 = fmaf(a.y, b.y, a1);
-          a2 = fmaf(a.z, b.z, a2);
-          a3 = fmaf(a.w, b.w, a3);
-        }
-        pr[(s - lo) * P + p] = ((a0 + a1) + (a2 + a3)) * scale;
+      for (int c4 = 0; c4 < D / 4; ++c4) {
+        const float4 a = qr[c4], b = kr[c4];
+        a0 = fmaf(a.x, b.x, a0);
+        a1 = fmaf(a.y, b.y, a1);
+        a2 = fmaf(a.z, b.z, a2);
+        a3 = fmaf(a.w, b.w, a3);
       }
+      pr[(s - lo) * P + p] = ((a0 + a1) + (a2 + a3)) * scale;
     }
   }
   load_tile_regs<D>(vb, lo, hi, reg);  // the first V tile, in flight during the softmax
@@ -280,14 +297,15 @@ __global__ void __launch_bounds__(kAttnThreads) swa_attn_kernel(float* __restric
   }
 #pragma unroll
   for (int j = 0; j < PG; ++j) as[c * P + g * PG + j] = acc[j] / sums[g * PG + j];
+  cp_async_wait_all();  // this thread's part of Wo
   __syncthreads();
   // ---- x_i += Wo a_i: thread = (output channel, the same positions)
   float y[PG];
 #pragma unroll
   for (int j = 0; j < PG; ++j) y[j] = 0.0f;
-#pragma unroll 16
+#pragma unroll 8
   for (int cc = 0; cc < D; ++cc) {
-    const float wv = __ldg(wot + (size_t)cc * D + c);
+    const float wv = wos[cc * D + c];
 #pragma unroll
     for (int j = 0; j < PG; ++j) y[j] = fmaf(wv, as[cc * P + g * PG + j], y[j]);
   }
@@ -309,12 +327,14 @@ kvq_status run_replay(const float* w, int layers, const float* emb, int64_t n, i
   transpose_kernel<<<dim3(D / 32, D / 32, 4 * layers), dim3(32, 8), 0, st>>>(w, wt, D);
   if (cudaMemcpyAsync(xb, emb, (size_t)n * D * sizeof(float), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
     return KVQ_ERR_CUDA;
-  static DeviceOnce attr_set;  // the attention kernel's shared-memory opt-in, once per device
+  static DeviceOnce attr_set;  // the kernels' shared-memory opt-ins, once per device
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
   if (attr_set.pending(dev)) {
     if (cudaFuncSetAttribute(swa_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             attn_smem_floats(D, kMaxWin) * (int)sizeof(float)) != cudaSuccess)
+                             attn_smem_floats(D, kMaxWin) * (int)sizeof(float)) != cudaSuccess ||
+        cudaFuncSetAttribute(swa_proj_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             D * D * (int)sizeof(float)) != cudaSuccess)
       return KVQ_ERR_CUDA;
     attr_set.mark(dev);
   }
@@ -326,7 +346,7 @@ kvq_status run_replay(const float* w, int layers, const float* emb, int64_t n, i
     const float* wl = wt + (size_t)4 * l * D * D;
     float* st_k = states + (size_t)(2 * l) * n_win * D;
     float* st_v = states + (size_t)(2 * l + 1) * n_win * D;
-    swa_proj_kernel<D><<<proj_grid, D, 0, st>>>(xb, wl, qb, kb, vb, st_k, st_v, n, n_win);
+    swa_proj_kernel<D><<<proj_grid, D, D * D * sizeof(float), st>>>(xb, wl, qb, kb, vb, st_k, st_v, n, n_win);
     swa_attn_kernel<D><<<attn_grid, kAttnThreads, attn_smem, st>>>(xb, qb, kb, vb, wl + (size_t)3 * D * D, n,
                                                                    n_win, scale);
   }
