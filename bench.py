@@ -520,6 +520,69 @@ def run_gpu(args, dist: Dist):
 PREFILL_METRIC = "append (quantise-on-append) tokens/s and HBM GB/s into the FP4 cache, 1xGB300"
 
 
+class AppendOracleSample:
+    """The oracle's quantise-on-append of prefill tokens: the K and V of
+    sequence 0's first `n_tok` tokens, every kv head, through the CPU block
+    quantiser (NVFP4: with each head's second-level scale set from the
+    sample beforehand, outside the timing), 256 tokens of one head per task
+    on the host's threads (the oracle's C calls release the interpreter
+    lock).  One token = one position of one sequence across all kv heads,
+    K and V."""
+
+    CHUNK = 256
+
+    def __init__(self, w, seed: int, n_tok: int, nvfp4: bool, cores: int):
+        import numpy as np
+
+        import oracle
+        self.oracle, self.nvfp4, self.cores = oracle, nvfp4, cores
+        self.n_tok = max(self.CHUNK, n_tok // self.CHUNK * self.CHUNK)
+        k, v = workloads.sequence_kv(w, 0, self.n_tok, seed=seed, device="cpu")
+        # [Hkv][n][d], contiguous per head
+        self.k = np.ascontiguousarray(k.float().numpy().transpose(1, 0, 2))
+        self.v = np.ascontiguousarray(v.float().numpy().transpose(1, 0, 2))
+        self.hkv = self.k.shape[0]
+        self.Sk = [oracle.nvfp4_global_scale(self.k[h]) for h in range(self.hkv)] if nvfp4 else None
+        self.Sv = [oracle.nvfp4_global_scale(self.v[h]) for h in range(self.hkv)] if nvfp4 else None
+
+    def _task(self, h: int, t0: int):
+        o, c = self.oracle, self.CHUNK
+        if self.nvfp4:
+            o.nvfp4_quantize_rows(self.k[h, t0:t0 + c], self.Sk[h])
+            o.nvfp4_quantize_rows(self.v[h, t0:t0 + c], self.Sv[h])
+        else:
+            o.quantize_rows(self.k[h, t0:t0 + c])
+            o.quantize_rows(self.v[h, t0:t0 + c])
+
+    def run(self, pool):
+        """Quantise the whole sample once: (tokens, seconds)."""
+        t = time.perf_counter()
+        futs = [pool.submit(self._task, h, t0) for t0 in range(0, self.n_tok, self.CHUNK) for h in range(self.hkv)]
+        for f in futs:
+            f.result()
+        return self.n_tok, time.perf_counter() - t
+
+    def describe(self, rounds: int, secs: float) -> str:
+        return (f"{self.n_tok} tokens x {self.hkv} kv heads (K and V) of one prefill sequence through the CPU "
+                f"{'NVFP4' if self.nvfp4 else 'FP4'} quantiser, {rounds} pass(es), {self.cores} threads, {secs:.1f} s")
+
+
+def append_oracle_sample(w, seed: int, budget_s: float, nvfp4: bool = False):
+    """cpu_baseline of the append workload: AppendOracleSample passes until
+    about budget_s of host time is spent."""
+    cores = os.cpu_count() or 1
+    sample = AppendOracleSample(w, seed, 4096, nvfp4, cores)
+    toks, secs, rounds = 0, 0.0, 0
+    with cf.ThreadPoolExecutor(max_workers=cores) as pool:
+        while secs < budget_s:
+            n, dt = sample.run(pool)
+            toks += n
+            secs += dt
+            rounds += 1
+    return {"value": toks / secs, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": sample.describe(rounds, secs)}
+
+
 def run_prefill(args, dist: Dist):
     """A step appends a whole prefill (B16 x 16384 tokens, Hkv8, d128, bf16 K
     and V) into the FP4 cache; value = appended tokens/s (one token = one
@@ -598,6 +661,8 @@ def run_prefill(args, dist: Dist):
     }
     if clk is not None:
         res["clocks"] = clk
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = append_oracle_sample(w, args.seed, budget_s=min(20.0, args.cpu_budget), nvfp4=nv)
     return res
 
 
@@ -972,11 +1037,100 @@ def run_reference_replay(args):
     }
 
 
+def _reference_line(args, metric: str, unit: str, value: float, secs: float, dtype: str, config: dict,
+                    cores: int, sample: str):
+    return {
+        "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+        "config": config,
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_reference_prefill(args):
+    """The oracle's quantise-on-append of the prefill workload: each step one
+    pass of an AppendOracleSample sized so that the whole run takes about a
+    minute of host time."""
+    w = workloads.WORKLOADS["prefill"]
+    nv = args.format == "nvfp4"
+    cores = os.cpu_count() or 1
+    with cf.ThreadPoolExecutor(max_workers=cores) as pool:
+        probe = AppendOracleSample(w, args.seed, 4096, nv, cores)
+        n, dt = probe.run(pool)
+        budget_per_step = 60.0 / max(1, args.steps + args.warmup)
+        n_tok = int(min(w.context, max(AppendOracleSample.CHUNK, budget_per_step * n / dt)))
+        sample = AppendOracleSample(w, args.seed, n_tok, nv, cores)
+        for _ in range(args.warmup):
+            sample.run(pool)
+        toks, secs = 0, 0.0
+        for _ in range(args.steps):
+            n, dt = sample.run(pool)
+            toks += n
+            secs += dt
+    config = {"workload": f"prefill: {w.description}" + (", NVFP4 cache" if nv else ""), "format": args.format,
+              "batch": w.batch, "tokens": w.context, "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+              "page_size": w.page_size, "parallelism": "host threads"}
+    return _reference_line(args, PREFILL_METRIC, "tokens/s", toks / secs, secs, "f32", config, cores,
+                           sample.describe(args.steps, secs) + " per step")
+
+
+def run_reference_prefill_attn(args):
+    """The oracle's chunked prefill of the prefill_attn workload: fp64
+    attention of the chunk's query tokens (from its end) over the dequantised
+    FP4 cache of one (sequence, kv head) unit, each step a bounded sample
+    sized so that the whole run takes about a minute; value in query tokens/s
+    of the whole head group (Hq rows per token)."""
+    import oracle
+    w = workloads.WORKLOADS["prefill_attn"]
+    T, C, G, d = w.context, w.chunk, w.group, w.head_dim
+    k, v = workloads.sequence_kv(w, 0, T, seed=args.seed, device="cpu")
+    kc, ks, _ = oracle.quantize_rows(k[:, 0].float().numpy())
+    vc, vs, _ = oracle.quantize_rows(v[:, 0].float().numpy())
+    kh, vh = oracle.dequantize_rows(kc, ks), oracle.dequantize_rows(vc, vs)
+    g = torch.Generator()
+    g.manual_seed(args.seed * 1_000_003 + 4242)
+    qh = torch.randn((C, G, d), generator=g).to(torch.bfloat16).float().numpy()
+    scale = 1.0 / math.sqrt(d)
+    budget_per_step = 60.0 / max(1, args.steps + args.warmup)
+
+    def step():
+        t = time.perf_counter()
+        rows = 0
+        for i in range(C - 1, -1, -1):
+            oracle.attend(qh[i], kh[:T - C + i + 1], vh[:T - C + i + 1], scale)
+            rows += G
+            if time.perf_counter() - t > budget_per_step:
+                break
+        return rows, time.perf_counter() - t
+
+    for _ in range(args.warmup):
+        step()
+    rows, secs = 0, 0.0
+    for _ in range(args.steps):
+        r, dt = step()
+        rows += r
+        secs += dt
+    value = rows / w.num_q_heads / secs
+    config = {"workload": f"prefill_attn: {w.description}", "format": "fp4", "batch": w.batch, "context": T,
+              "chunk": C, "kv_heads": w.num_kv_heads, "q_heads": w.num_q_heads, "head_dim": d,
+              "page_size": w.page_size, "parallelism": "one host thread"}
+    return _reference_line(args, PREFILL_ATTN_METRIC, "query tokens/s", value, secs, "f64", config, 1,
+                           f"{rows // G} tokens x G={G} query rows of one kv head over ~{T} positions in all "
+                           f"(fp64 C attention, one thread, about {budget_per_step:.2f} s per step), scaled to "
+                           f"Hq={w.num_q_heads} rows per token")
+
+
 def run_reference(args, dist: Dist):
     if dist.rank != 0:
         return None
     if args.workload == "swa_replay":
         return run_reference_replay(args)
+    if args.workload == "prefill":
+        return run_reference_prefill(args)
+    if args.workload == "prefill_attn":
+        return run_reference_prefill_attn(args)
     w = workloads.WORKLOADS[args.workload]
     cores = os.cpu_count() or 1
     dev = "cuda" if torch.cuda.is_available() else "cpu"
