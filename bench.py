@@ -1037,6 +1037,12 @@ def run_reference_replay(args):
     }
 
 
+def reference_budget_s(args) -> float:
+    """Host seconds the whole reference run (warm-up and timed steps) is sized
+    for: three times --cpu-budget, a minute by default."""
+    return 3.0 * args.cpu_budget
+
+
 def _reference_line(args, metric: str, unit: str, value: float, secs: float, dtype: str, config: dict,
                     cores: int, sample: str):
     return {
@@ -1051,15 +1057,15 @@ def _reference_line(args, metric: str, unit: str, value: float, secs: float, dty
 
 def run_reference_prefill(args):
     """The oracle's quantise-on-append of the prefill workload: each step one
-    pass of an AppendOracleSample sized so that the whole run takes about a
-    minute of host time."""
+    pass of an AppendOracleSample sized so that the whole run takes about
+    reference_budget_s of host time."""
     w = workloads.WORKLOADS["prefill"]
     nv = args.format == "nvfp4"
     cores = os.cpu_count() or 1
     with cf.ThreadPoolExecutor(max_workers=cores) as pool:
         probe = AppendOracleSample(w, args.seed, 4096, nv, cores)
         n, dt = probe.run(pool)
-        budget_per_step = 60.0 / max(1, args.steps + args.warmup)
+        budget_per_step = reference_budget_s(args) / max(1, args.steps + args.warmup)
         n_tok = int(min(w.context, max(AppendOracleSample.CHUNK, budget_per_step * n / dt)))
         sample = AppendOracleSample(w, args.seed, n_tok, nv, cores)
         for _ in range(args.warmup):
@@ -1080,8 +1086,8 @@ def run_reference_prefill_attn(args):
     """The oracle's chunked prefill of the prefill_attn workload: fp64
     attention of the chunk's query tokens (from its end) over the dequantised
     FP4 cache of one (sequence, kv head) unit, each step a bounded sample
-    sized so that the whole run takes about a minute; value in query tokens/s
-    of the whole head group (Hq rows per token)."""
+    sized so that the whole run takes about reference_budget_s; value in query
+    tokens/s of the whole head group (Hq rows per token)."""
     import oracle
     w = workloads.WORKLOADS["prefill_attn"]
     T, C, G, d = w.context, w.chunk, w.group, w.head_dim
@@ -1093,7 +1099,7 @@ def run_reference_prefill_attn(args):
     g.manual_seed(args.seed * 1_000_003 + 4242)
     qh = torch.randn((C, G, d), generator=g).to(torch.bfloat16).float().numpy()
     scale = 1.0 / math.sqrt(d)
-    budget_per_step = 60.0 / max(1, args.steps + args.warmup)
+    budget_per_step = reference_budget_s(args) / max(1, args.steps + args.warmup)
 
     def step():
         t = time.perf_counter()
@@ -1134,13 +1140,13 @@ def run_reference(args, dist: Dist):
     w = workloads.WORKLOADS[args.workload]
     cores = os.cpu_count() or 1
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    # size each step so the whole warm-up + timed run stays around a minute
+    # size each step so the whole warm-up + timed run stays around reference_budget_s
     nv = args.format == "nvfp4"
     probe = OracleSample(w, args.seed, 1, max_tokens=4096, device=dev, nvfp4=nv)
     with cf.ThreadPoolExecutor(max_workers=cores) as pool:
         _, t_probe = probe.run(pool)
         per_token_s = t_probe / 4096
-        budget_per_step = 60.0 / max(1, args.steps + args.warmup)
+        budget_per_step = reference_budget_s(args) / max(1, args.steps + args.warmup)
         max_tokens = int(min(w.context or 131072, max(64, budget_per_step * cores / per_token_s)))
         sample = OracleSample(w, args.seed, cores, max_tokens=max_tokens, device=dev, nvfp4=nv)
         for _ in range(args.warmup):
@@ -1181,7 +1187,9 @@ def main(argv=None):
                     help="cache format: FP4 (E4M3 scale per 16) or NVFP4 (plus an fp32 scale per kv head)")
     ap.add_argument("--layers", type=int, default=1,
                     help="layers per step, each with its own cache (long_context at 4 layers: 4.84 GB)")
-    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--cpu-budget", type=float, default=20.0,
+                    help="host seconds for the CPU-oracle baseline; the reference arm's whole run is sized "
+                         "for three times this")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graphs", action=argparse.BooleanOptionalAction, default=False,
                     help="replay each step's appends and decode from CUDA graphs (decode workloads)")

@@ -56,3 +56,19 @@ def test_reference_arm_on_tiny_workload(capsys):
     res = json.loads(line)
     assert res["impl"] == "reference" and res["value"] > 0 and res["unit"] == bench.UNIT
     assert res["e2e"]["h2d_bytes_per_step"] == 0 and res["cpu_baseline"]["kind"] == "oracle"
+
+
+@pytest.mark.parametrize("workload,metric,unit", [("prefill", "PREFILL_METRIC", "tokens/s"),
+                                                  ("prefill_attn", "PREFILL_ATTN_METRIC", "query tokens/s")])
+def test_reference_arm_on_prefill_workloads(capsys, workload, metric, unit):
+    """The reference arm of the append and chunked-prefill workloads times the
+    oracle on that workload's own metric and unit."""
+    import json
+
+    import bench
+    bench.main(["--impl", "reference", "--workload", workload, "--steps", "2", "--warmup", "3",
+                "--cpu-budget", "0.5"])
+    res = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert res["impl"] == "reference" and res["metric"] == getattr(bench, metric) and res["unit"] == unit
+    assert res["value"] > 0 and res["cpu_baseline"]["kind"] == "oracle"
+    assert res["cpu_baseline"]["value"] == res["value"] and res["e2e"]["h2d_bytes_per_step"] == 0
