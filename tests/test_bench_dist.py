@@ -72,3 +72,32 @@ def test_reference_arm_on_prefill_workloads(capsys, workload, metric, unit):
     assert res["impl"] == "reference" and res["metric"] == getattr(bench, metric) and res["unit"] == unit
     assert res["value"] > 0 and res["cpu_baseline"]["kind"] == "oracle"
     assert res["cpu_baseline"]["value"] == res["value"] and res["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_profiled_traffic_only_for_the_captured_source(tmp_path):
+    """A bench line carries a committed capture's DRAM traffic only while the
+    kernel source still hashes to the one the capture was taken on."""
+    import hashlib
+
+    import bench
+    src = tmp_path / "kernel.cu"
+    src.write_text("// kernel v1\n")
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()
+    prof = tmp_path / "summary.md"
+    prof.write_text("# capture\n\ntraffic_bytes_per_launch: 1234\ntraffic_bytes_per_launch_nvfp4: 5678\n"
+                    f"source_sha256: {sha}\n")
+    assert bench.profiled_traffic(str(prof), str(src)) == 1234
+    assert bench.profiled_traffic(str(prof), str(src), "traffic_bytes_per_launch_nvfp4") == 5678
+    src.write_text("// kernel v2\n")
+    assert bench.profiled_traffic(str(prof), str(src)) is None
+    assert bench.profiled_traffic(str(tmp_path / "missing.md"), str(src)) is None
+
+
+def test_committed_captures_match_the_committed_sources():
+    """The committed decode, prefill and append summaries were taken on the
+    committed kernel sources, so the bench lines carry their traffic."""
+    import bench
+    assert bench.profiled_traffic(bench.PROFILE, bench.DECODE_SRC) is not None
+    assert bench.profiled_traffic(bench.PREFILL_PROFILE, bench.PREFILL_SRC) is not None
+    assert bench.profiled_traffic(bench.APPEND_PROFILE, bench.APPEND_SRC) is not None
+    assert bench.profiled_traffic(bench.APPEND_PROFILE, bench.APPEND_SRC, "traffic_bytes_per_launch_nvfp4") is not None
