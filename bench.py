@@ -503,7 +503,9 @@ def run_gpu(args, dist: Dist):
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_src,
                      "traffic": profiled_traffic() if w.name == "long_context" else None,
-                     "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_s * 1e3},
+                     "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_s * 1e3,
+                     "median_launch_ms": statistics.median(decode_ms) / L,
+                     "min_launch_ms": min(decode_ms) / L},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": Ke},
         "gpu_launches": L * (4 if w.window else 3) * K,
