@@ -170,9 +170,10 @@ def fp4_bytes_per_token(w) -> int:
 class Setup:
     """The resident FP4 cache of a workload plus the per-step inputs."""
 
-    def __init__(self, w, seed: int, device, layers: int = 1, nvfp4: bool = False):
+    def __init__(self, w, seed: int, device, layers: int = 1, nvfp4: bool = False, kernel: str = "mma"):
         from fp4_kv_cache_kvq_gb300 import kvq
         self.w = w
+        self.kernel = kernel
         self.layers = layers
         self.kvq = kvq
         self.lens0 = workloads.lengths(w, seed)
@@ -260,7 +261,8 @@ class Setup:
             ev[0].record()
         qq = self.q[i % NQ] if q is None else q
         for cache, swa, out in zip(self.caches, self.swas, self.outs if outs is None else outs):
-            kvq.decode_attn(cache, self.lens[s], qq, self.scale, swa=swa, out=out, workspace=self.ws, err=self.err)
+            kvq.decode_attn(cache, self.lens[s], qq, self.scale, swa=swa, out=out, workspace=self.ws, err=self.err,
+                            kernel=self.kernel)
         if ev is not None:
             ev[1].record()
         return self.kv_tokens[s] * self.layers
@@ -284,7 +286,7 @@ class Setup:
                 with torch.cuda.graph(gd, stream=side):
                     for cache, swa, out in zip(self.caches, self.swas, self.outs):
                         self.kvq.decode_attn(cache, self.lens[s], self.q[i % NQ], self.scale, swa=swa, out=out,
-                                             workspace=self.ws, err=self.err)
+                                             workspace=self.ws, err=self.err, kernel=self.kernel)
                 self.graphs.append((ga, gd))
         torch.cuda.current_stream().wait_stream(side)
         torch.cuda.synchronize()
@@ -323,7 +325,7 @@ def run_gpu(args, dist: Dist):
     build.build()
     w = workloads.WORKLOADS[args.workload]
     L = args.layers
-    st = Setup(w, args.seed, device, layers=L, nvfp4=args.format == "nvfp4")
+    st = Setup(w, args.seed, device, layers=L, nvfp4=args.format == "nvfp4", kernel=args.decode_kernel)
     K, Wm = args.steps, args.warmup
     for i in range(Wm):
         st.step(i)
@@ -493,7 +495,9 @@ def run_gpu(args, dist: Dist):
                    else f"inputs larger than L2 (FP4 cache {st.cache.nbytes} B vs {l2_bytes} B L2), no flush",
                    "launch": "CUDA graphs (one per step of the cycle: appends, then decode)" if args.graphs
                    else "eager launches",
-                   "parallelism": f"replicas x{dist.world}"},
+                   "parallelism": f"replicas x{dist.world}",
+                   "decode_kernel": "kvq_decode_attn_tc (tcgen05)" if args.decode_kernel == "tcgen05"
+                   else "kvq_decode_attn (mma.sync)"},
         "value_l2_warm": warm_value,
         "hbm_gbs_step": step_bytes * K / elapsed_s / 1e9,
         "hbm_gbs_decode": achieved,
@@ -502,7 +506,8 @@ def run_gpu(args, dist: Dist):
                      + (", FP8 window folded into the merge" if w.window else ""),
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_src,
-                     "traffic": profiled_traffic() if w.name == "long_context" else None,
+                     "traffic": profiled_traffic() if w.name == "long_context" and args.decode_kernel == "mma"
+                     else None,
                      "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": dec_s * 1e3,
                      "median_launch_ms": statistics.median(decode_ms) / L,
                      "min_launch_ms": min(decode_ms) / L},
@@ -1193,6 +1198,9 @@ def main(argv=None):
                     help="host seconds for the CPU-oracle baseline; the reference arm's whole run is sized "
                          "for three times this")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-kernel", choices=["mma", "tcgen05"], default="mma",
+                    help="decode kernel: mma (kvq_decode_attn, the default) or tcgen05 (kvq_decode_attn_tc, "
+                         "head_dim 128 only, a measured slower alternative)")
     ap.add_argument("--graphs", action=argparse.BooleanOptionalAction, default=False,
                     help="replay each step's appends and decode from CUDA graphs (decode workloads)")
     args = ap.parse_args(argv)

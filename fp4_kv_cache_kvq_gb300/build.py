@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvq.so")
-SOURCES = ["kvq_append.cu", "kvq_dequant.cu", "kvq_decode.cu", "kvq_sweep.cu", "kvq_prefill.cu", "kvq_replay.cu"]
+SOURCES = ["kvq_append.cu", "kvq_dequant.cu", "kvq_decode.cu", "kvq_decode_tc.cu", "kvq_sweep.cu", "kvq_prefill.cu", "kvq_replay.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-diag-suppress", "177"]

@@ -34,25 +34,27 @@
 //                                              fragment with movmatrix.trans
 // A stage's PV products go to fresh accumulators that are folded into O
 // (rescaled only when the running max moved).  Codes are expanded a 32-bit
-// word (8 codes) at a time.  Tokens sit on the MMA's M side so a GQA group of
+// word (8 codes) at a time.  Each slice's K bytes are read from the stage
+// right before its QK^T products and its V bytes right before its PV
+// products; the stage goes back to the producer after the last slice's V
+// loads.  (Reading the whole stage into registers first and releasing it
+// early costs 40 live registers, which at three CTAs per SM pushed the
+// kernel into spills.)  Tokens sit on the MMA's M side so a GQA group of
 // up to 8 query heads fills N = 8 without padding rows.  The query is
 // pre-scaled per head by a power of two so that its bf16 values are exact in
 // f16; the factor is undone in fp32.
 #include "kvq_common.cuh"
+#include "kvq_decode.cuh"
 #include "kvq_host.cuh"
 
 namespace kvq {
 namespace {
 
-constexpr int kChunk = 128;          // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;
 constexpr int kSlices = kChunk / (16 * kConsumerWarps);  // 16-token slices per warp per stage
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kStages = 3;
 constexpr int kMaxCopies = kChunk / 16;  // pool groups per stage at the smallest page size
-constexpr int kNG = 8;  // query rows per kv head held by one tile (G <= 8)
-constexpr float kLazySlack = 8.0f;
-constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMaxWindow = 1024;
 
 template <int D>
@@ -63,115 +65,6 @@ struct Geo {
   static constexpr int kFlushBytes = kConsumerWarps * kNG * (D + 2) * 4;
   static constexpr int kSmemBytes = kStages * kStageBytes + kFlushBytes + 2 * kStages * 8 + kStages * 4 + 16 + 1024;
 };
-
-// Compile-time view of one pool group of GT tokens (see Fp4Layout).
-template <int D, int GT>
-struct Grp {
-  static constexpr int kNB = D / 16;
-  static constexpr int kBytes = GT * 9 * D / 8;
-  static constexpr int kKS = GT * D / 2;          // K scales
-  static constexpr int kVC = GT * (D / 2 + kNB);  // V codes (token pairs)
-  static constexpr int kVS = GT * (D + kNB);      // V scales (token pairs)
-};
-
-struct DecodeParams {
-  const int32_t* lens;
-  const int32_t* page_table;
-  const uint8_t* pool;
-  const uint16_t* q;
-  float* part_o;
-  float* part_ml;
-  int2* unit_rec;
-  int32_t* flag;
-  const float* k_gscale;  // NVFP4 second-level scales [Hkv] (nullptr: plain FP4)
-  const float* v_gscale;
-  int64_t num_pages;
-  int32_t batch, hkv, g, hq, page, max_pages, window;
-  float qk_log2;  // softmax_scale * log2(e)
-};
-
-__device__ __forceinline__ int fp4_chunks(int32_t T, int window) {
-  if (T <= 0) return 0;
-  const int w = window > 0 ? min(window, T) : 0;
-  return (T - w + kChunk - 1) / kChunk;
-}
-
-__device__ __forceinline__ int fp4_tokens(int32_t T, int window) {
-  if (T <= 0) return 0;
-  const int w = window > 0 ? min(window, T) : 0;
-  return T - w;
-}
-
-// Position of a walker on the line of chunks: unit (b, h), chunk c of nch.
-struct Walker {
-  int b, h, c, nch;
-  int64_t v;  // index on the line
-};
-
-// Every warp computes the same thing: the line's length and where this CTA's
-// range starts.  Lanes scan 32 sequences at a time.
-__device__ __forceinline__ void plan(const DecodeParams& p, int64_t& total, int64_t& v0, int64_t& v1, Walker& wk) {
-  const int lane = threadIdx.x & 31;
-  int64_t acc = 0;
-  total = 0;
-  // pass 1: total
-  for (int base = 0; base < p.batch; base += 32) {
-    const int bb = base + lane;
-    int64_t x = bb < p.batch ? (int64_t)fp4_chunks(__ldg(p.lens + bb), p.window) * p.hkv : 0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
-    acc += x;
-  }
-  total = acc;
-  const int64_t per = (total + gridDim.x - 1) / gridDim.x;
-  v0 = min(total, (int64_t)blockIdx.x * per);
-  v1 = min(total, v0 + per);
-  wk.b = p.batch;
-  wk.h = 0;
-  wk.c = 0;
-  wk.nch = 0;
-  wk.v = v0;
-  if (v0 >= v1) return;
-  // pass 2: locate v0
-  acc = 0;
-  for (int base = 0; base < p.batch; base += 32) {
-    const int bb = base + lane;
-    const int n = bb < p.batch ? fp4_chunks(__ldg(p.lens + bb), p.window) : 0;
-    const int64_t x = (int64_t)n * p.hkv;
-    int64_t incl = x;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int64_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const int64_t group_total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    if (acc + group_total > v0) {
-      const unsigned hit = __ballot_sync(0xFFFFFFFFu, acc + incl > v0);
-      const int L = __ffs(hit) - 1;
-      const int64_t before = acc + __shfl_sync(0xFFFFFFFFu, incl - x, L);
-      const int nL = __shfl_sync(0xFFFFFFFFu, n, L);
-      const int64_t rem = v0 - before;
-      wk.b = base + L;
-      wk.nch = nL;
-      wk.h = (int)(rem / nL);
-      wk.c = (int)(rem % nL);
-      return;
-    }
-    acc += group_total;
-  }
-}
-
-__device__ __forceinline__ void advance(const DecodeParams& p, Walker& wk) {
-  ++wk.v;
-  if (++wk.c < wk.nch) return;
-  wk.c = 0;
-  if (++wk.h < p.hkv) return;
-  wk.h = 0;
-  do {
-    ++wk.b;
-    wk.nch = wk.b < p.batch ? fp4_chunks(__ldg(p.lens + wk.b), p.window) : 1;
-  } while (wk.nch == 0);
-}
 
 // Shared-memory carve-up.
 template <int D>
@@ -347,11 +240,9 @@ __device__ __forceinline__ void consume_stage(ConsumerState<D>& st, uint32_t sta
       R::kVC + tig * D + (D == 128 ? 16 * (g ^ (tig << 1)) : 8 * (g ^ (((tig >> 1) & 1) << 2)));
   const uint32_t vs_lane = R::kVS + tig * 2 * R::kNB + 2 * (D == 128 ? g : (g >> 1));
 
-  // ---- loads from the stage, then release it
-  uint32_t kw[kSlices][2][KW];  // rows g, g+8 of each slice
-  uint32_t ksb[kSlices][2];     // their scale bytes (blocks of this thread's channels)
-  uint32_t vw[kSlices][2][VW];  // token pairs (2t, 2t+1) and (2t+8, 2t+9): interleaved code bytes
-  uint32_t vsb[kSlices][2];     // their scale-byte pairs, block of this thread's channels
+  // ---- S^T = K^ Q^T per slice (rows: tokens g, g+8; columns: q rows 2t, 2t+1);
+  // each slice's K bytes are loaded right before its products
+  float S[kSlices][4];
 #pragma unroll
   for (int sl = 0; sl < kSlices; ++sl) {
     const int r0 = 16 * (kSlices * warp + sl);
@@ -359,66 +250,48 @@ __device__ __forceinline__ void consume_stage(ConsumerState<D>& st, uint32_t sta
     const uint32_t lr = r0 % GT;
     const uint32_t kp = grp + lr * (D / 2) + k_lane;
     const uint32_t ksp = grp + lr * R::kNB + ks_lane;
-    const uint32_t vp = grp + (lr / 2) * D + v_lane;
-    const uint32_t vsp = grp + (lr / 2) * 2 * R::kNB + vs_lane;
+    uint32_t kw[2][KW], ksb[2];
     if constexpr (D == 128) {
       const uint4 a = lds128(kp);
       const uint4 b = lds128(kp + 8 * (D / 2));
-      kw[sl][0][0] = a.x; kw[sl][0][1] = a.y; kw[sl][0][2] = a.z; kw[sl][0][3] = a.w;
-      kw[sl][1][0] = b.x; kw[sl][1][1] = b.y; kw[sl][1][2] = b.z; kw[sl][1][3] = b.w;
-      ksb[sl][0] = lds16(ksp);
-      ksb[sl][1] = lds16(ksp + 8 * R::kNB);
-      const uint4 x = lds128(vp);
-      const uint4 y = lds128(vp + 4 * D);  // pair row i + 4: same permutation
-      vw[sl][0][0] = x.x; vw[sl][0][1] = x.y; vw[sl][0][2] = x.z; vw[sl][0][3] = x.w;
-      vw[sl][1][0] = y.x; vw[sl][1][1] = y.y; vw[sl][1][2] = y.z; vw[sl][1][3] = y.w;
+      kw[0][0] = a.x; kw[0][1] = a.y; kw[0][2] = a.z; kw[0][3] = a.w;
+      kw[1][0] = b.x; kw[1][1] = b.y; kw[1][2] = b.z; kw[1][3] = b.w;
+      ksb[0] = lds16(ksp);
+      ksb[1] = lds16(ksp + 8 * R::kNB);
     } else {
       const uint2 a = lds64(kp);
       const uint2 b = lds64(kp + 8 * (D / 2));
-      kw[sl][0][0] = a.x; kw[sl][0][1] = a.y;
-      kw[sl][1][0] = b.x; kw[sl][1][1] = b.y;
-      ksb[sl][0] = lds8(ksp);
-      ksb[sl][1] = lds8(ksp + 8 * R::kNB);
-      const uint2 x = lds64(vp);
-      const uint2 y = lds64(vp + 4 * D);  // (i + 4) >> 1 keeps bit 0
-      vw[sl][0][0] = x.x; vw[sl][0][1] = x.y;
-      vw[sl][1][0] = y.x; vw[sl][1][1] = y.y;
+      kw[0][0] = a.x; kw[0][1] = a.y;
+      kw[1][0] = b.x; kw[1][1] = b.y;
+      ksb[0] = lds8(ksp);
+      ksb[1] = lds8(ksp + 8 * R::kNB);
     }
-    vsb[sl][0] = lds16(vsp);
-    vsb[sl][1] = lds16(vsp + 4 * 2 * R::kNB);
-  }
-  mbar_arrive(empty_bar);
-
-  // ---- S^T = K^ Q^T per slice (rows: tokens g, g+8; columns: q rows 2t, 2t+1)
-  float S[kSlices][4];
-#pragma unroll
-  for (int sl = 0; sl < kSlices; ++sl) {
     uint32_t sc[2][2];  // [row g / g+8][first / second block of the thread's channels]
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       if constexpr (D == 128) {
-        const uint32_t u = f16x2_from_e4m3x2(ksb[sl][r]);
+        const uint32_t u = f16x2_from_e4m3x2(ksb[r]);
         sc[r][0] = prmt(u, 0u, 0x1010u);
         sc[r][1] = prmt(u, 0u, 0x3232u);
       } else {
-        sc[r][0] = sc[r][1] = f16x2_from_e4m3x2(ksb[sl][r] * 0x0101u);
+        sc[r][0] = sc[r][1] = f16x2_from_e4m3x2(ksb[r] * 0x0101u);
       }
     }
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int q = 0; q < KW; ++q) {  // word q holds k-steps 2q (bytes 0,1) and 2q+1 (bytes 2,3)
       uint32_t ca[4], cb[4];
-      f16x2x4_from_e2m1x8(kw[sl][0][q], ca);
-      f16x2x4_from_e2m1x8(kw[sl][1][q], cb);
+      f16x2x4_from_e2m1x8(kw[0][q], ca);
+      f16x2x4_from_e2m1x8(kw[1][q], cb);
       const int half = (D == 128 && q >= KW / 2) ? 1 : 0;
       const uint32_t sA = sc[0][half], sB = sc[1][half];
-      mma_f16_16816(acc[0], hmul2_u32(ca[0], sA), hmul2_u32(cb[0], sB), hmul2_u32(ca[1], sA),
+      mma_f16_16816(acc, hmul2_u32(ca[0], sA), hmul2_u32(cb[0], sB), hmul2_u32(ca[1], sA),
                     hmul2_u32(cb[1], sB), st.qf[4 * q], st.qf[4 * q + 1]);
-      mma_f16_16816(acc[1], hmul2_u32(ca[2], sA), hmul2_u32(cb[2], sB), hmul2_u32(ca[3], sA),
+      mma_f16_16816(acc, hmul2_u32(ca[2], sA), hmul2_u32(cb[2], sB), hmul2_u32(ca[3], sA),
                     hmul2_u32(cb[3], sB), st.qf[4 * q + 2], st.qf[4 * q + 3]);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) S[sl][i] = acc[0][i] + acc[1][i];
+    for (int i = 0; i < 4; ++i) S[sl][i] = acc[i];
   }
   // PARTIAL: the stage holds fewer than kChunk tokens (only a unit's last
   // chunk); full stages get code without any of the masking below
@@ -476,8 +349,27 @@ __device__ __forceinline__ void consume_stage(ConsumerState<D>& st, uint32_t sta
     const uint32_t pbA = movmatrix_trans(pack_f16x2(p0, p1));
     const uint32_t pbB = movmatrix_trans(pack_f16x2(p2, p3));
 
-    // ---- O^T += V^T P^T
-    uint32_t vsA = vsb[sl][0], vsB = vsb[sl][1];
+    // ---- O^T += V^T P^T: this slice's V bytes, then (after the last slice)
+    // the stage goes back to the producer
+    const int r0v = 16 * (kSlices * warp + sl);
+    const uint32_t grpv = stage + (uint32_t)((r0v / GT) * R::kBytes);
+    const uint32_t lrv = r0v % GT;
+    const uint32_t vp = grpv + (lrv / 2) * D + v_lane;
+    const uint32_t vsp = grpv + (lrv / 2) * 2 * R::kNB + vs_lane;
+    uint32_t vwl[2][VW];
+    if constexpr (D == 128) {
+      const uint4 x = lds128(vp);
+      const uint4 y = lds128(vp + 4 * D);  // pair row i + 4: same permutation
+      vwl[0][0] = x.x; vwl[0][1] = x.y; vwl[0][2] = x.z; vwl[0][3] = x.w;
+      vwl[1][0] = y.x; vwl[1][1] = y.y; vwl[1][2] = y.z; vwl[1][3] = y.w;
+    } else {
+      const uint2 x = lds64(vp);
+      const uint2 y = lds64(vp + 4 * D);  // (i + 4) >> 1 keeps bit 0
+      vwl[0][0] = x.x; vwl[0][1] = x.y;
+      vwl[1][0] = y.x; vwl[1][1] = y.y;
+    }
+    uint32_t vsA = lds16(vsp), vsB = lds16(vsp + 4 * 2 * R::kNB);
+    if (sl == kSlices - 1) mbar_arrive(empty_bar);
     if (partial) {  // masked tokens get a zero V scale so stale bytes cannot inject NaN
       const int t0 = 16 * (kSlices * warp + sl) + 2 * tig;
       if (t0 >= ntok) vsA &= 0xFF00u;
@@ -492,8 +384,8 @@ __device__ __forceinline__ void consume_stage(ConsumerState<D>& st, uint32_t sta
 #pragma unroll
     for (int w = 0; w < VW; ++w) {
       uint32_t ta[4], tb[4];
-      f16x2x4_from_e2m1x8(vw[sl][0][w], ta);
-      f16x2x4_from_e2m1x8(vw[sl][1][w], tb);
+      f16x2x4_from_e2m1x8(vwl[0][w], ta);
+      f16x2x4_from_e2m1x8(vwl[1][w], tb);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         VA[4 * w + k] = ta[k];
@@ -593,7 +485,10 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   int64_t total, v0, v1;
   Walker wk;
-  plan(p, total, v0, v1, wk);
+  // the merge grid (launched as a programmatic dependent) may be scheduled
+  // now; it waits for this grid's results before reading them
+  grid_launch_dependents();
+  plan(p, blockIdx.x, gridDim.x, total, v0, v1, wk);
   if (v0 >= v1) return;
 
   if (warp == kConsumerWarps) {
@@ -673,6 +568,7 @@ struct MergeParams {
 // round trips whatever the split count.
 template <int D>
 __global__ void __launch_bounds__(kNG * D / 4) merge_splits_kernel(const MergeParams p) {
+  grid_dependency_wait();  // the decode grid has finished and its partials are visible
   const int u = blockIdx.x;
   const int b = u / p.hkv, h = u % p.hkv;
   const int r = threadIdx.x / (D / 4), c4 = threadIdx.x % (D / 4);
@@ -836,6 +732,7 @@ __global__ void __launch_bounds__(kWinThreads) merge_window_kernel(const MergePa
       }
     }
   }
+  grid_dependency_wait();  // the window's terms are done; now the decode grid's partials
   const int2 rec = nch > 0 ? __ldg(p.unit_rec + u) : make_int2(0, 0);
 #pragma unroll
   for (int r = 0; r < kRowsPV; ++r) {
@@ -865,6 +762,26 @@ __global__ void __launch_bounds__(kWinThreads) merge_window_kernel(const MergePa
 }
 
 // ------------------------------------------------------------------ host side
+// Launch a merge kernel as a programmatic dependent of the decode kernel just
+// enqueued on the stream: its grid may be scheduled as the decode's CTAs
+// retire (the decode releases dependents at its start), and it runs
+// griddepcontrol.wait before it reads the decode's partials.
+template <typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Args...), dim3 grid, dim3 block, int smem, cudaStream_t s,
+                             const MergeParams& mp) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, mp);
+}
+
 int window_smem_bytes(int d, int window) {
   const int rows = kNG / (d == 128 ? win_row_split<128>() : win_row_split<64>());
   return (rows * d + rows * window + 2 * rows) * (int)sizeof(float) + kWinTile * d;
@@ -881,8 +798,9 @@ kvq_status launch_window_merge(const MergeParams& mp, cudaStream_t s, int smem, 
       return KVQ_ERR_CUDA;
     attr_set.mark(dev);
   }
-  merge_window_kernel<D><<<dim3((unsigned)units, win_row_split<D>()), kWinThreads, smem, s>>>(mp);
-  return launch_status();
+  const cudaError_t e =
+      launch_dependent(merge_window_kernel<D>, dim3((unsigned)units, win_row_split<D>()), dim3(kWinThreads), smem, s, mp);
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
 struct WsLayout {
@@ -944,10 +862,13 @@ extern "C" size_t kvq_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
   return ws_layout(batch, num_kv_heads, num_q_heads / num_kv_heads, head_dim, ctas).total;
 }
 
-extern "C" kvq_status kvq_decode_attn(const kvq_cache* global, const kvq_cache* swa, int32_t batch,
-                                      int32_t num_q_heads, const int32_t* d_seq_lens, const void* q,
-                                      float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
-                                      int32_t* d_err_flag, kvq_stream stream) {
+namespace {
+
+// kvq_decode_attn and kvq_decode_attn_tc: the same checks, workspace, partials
+// and merge; `tcgen05` picks the tensor-memory decode kernel (head_dim 128).
+kvq_status decode_attn(const kvq_cache* global, const kvq_cache* swa, int32_t batch, int32_t num_q_heads,
+                       const int32_t* d_seq_lens, const void* q, float softmax_scale, float* out, void* workspace,
+                       size_t workspace_bytes, int32_t* d_err_flag, kvq_stream stream, bool tcgen05) {
   if (batch < 1) return KVQ_ERR_INVALID_ARGUMENT;
   kvq_status st = check_cache(global, batch);
   if (st != KVQ_OK) return st;
@@ -966,6 +887,7 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* global, const kvq_cache* 
       return KVQ_ERR_INVALID_ARGUMENT;
   }
   if (D != 64 && D != 128) return KVQ_ERR_UNSUPPORTED;
+  if (tcgen05 && D != 128) return KVQ_ERR_UNSUPPORTED;
   if (g > kNG) return KVQ_ERR_UNSUPPORTED;
   if (swa != nullptr && swa->page_size > kMaxWindow) return KVQ_ERR_UNSUPPORTED;
   const int ctas = decode_ctas();
@@ -996,7 +918,10 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* global, const kvq_cache* 
   dp.max_pages = global->max_pages_per_seq;
   dp.window = swa ? swa->page_size : 0;
   dp.qk_log2 = softmax_scale * kLog2e;
-  st = D == 128 ? launch_decode<128>(dp, s, ctas) : launch_decode<64>(dp, s, ctas);
+  if (tcgen05)
+    st = launch_decode_tc(dp, s);
+  else
+    st = D == 128 ? launch_decode<128>(dp, s, ctas) : launch_decode<64>(dp, s, ctas);
   if (st != KVQ_OK) return st;
 
   MergeParams mp;
@@ -1018,16 +943,33 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* global, const kvq_cache* 
   mp.head_dim = D;
   mp.qk_log2 = dp.qk_log2;
   if (swa == nullptr) {
-    if (D == 128)
-      merge_splits_kernel<128><<<(unsigned)(batch * hkv), kNG * 128 / 4, 0, s>>>(mp);
-    else
-      merge_splits_kernel<64><<<(unsigned)(batch * hkv), kNG * 64 / 4, 0, s>>>(mp);
-    return launch_status();
+    const cudaError_t e =
+        D == 128 ? launch_dependent(merge_splits_kernel<128>, dim3((unsigned)(batch * hkv)), dim3(kNG * 128 / 4), 0, s, mp)
+                 : launch_dependent(merge_splits_kernel<64>, dim3((unsigned)(batch * hkv)), dim3(kNG * 64 / 4), 0, s, mp);
+    return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
   }
   const int wsmem = window_smem_bytes(D, swa->page_size);
   st = D == 128 ? launch_window_merge<128>(mp, s, wsmem, batch * hkv)
                 : launch_window_merge<64>(mp, s, wsmem, batch * hkv);
   return st;
+}
+
+}  // namespace
+
+extern "C" kvq_status kvq_decode_attn(const kvq_cache* global, const kvq_cache* swa, int32_t batch,
+                                      int32_t num_q_heads, const int32_t* d_seq_lens, const void* q,
+                                      float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                                      int32_t* d_err_flag, kvq_stream stream) {
+  return decode_attn(global, swa, batch, num_q_heads, d_seq_lens, q, softmax_scale, out, workspace,
+                     workspace_bytes, d_err_flag, stream, false);
+}
+
+extern "C" kvq_status kvq_decode_attn_tc(const kvq_cache* global, const kvq_cache* swa, int32_t batch,
+                                         int32_t num_q_heads, const int32_t* d_seq_lens, const void* q,
+                                         float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                                         int32_t* d_err_flag, kvq_stream stream) {
+  return decode_attn(global, swa, batch, num_q_heads, d_seq_lens, q, softmax_scale, out, workspace,
+                     workspace_bytes, d_err_flag, stream, true);
 }
 
 // ------------------------------------------------------------------ decode without caller scratch

@@ -83,6 +83,8 @@ def load() -> ctypes.CDLL:
             L.kvq_decode_attn.restype = ctypes.c_int
             L.kvq_decode_attn.argtypes = [_CP, _CP, ctypes.c_int32, ctypes.c_int32, _P, _P, ctypes.c_float,
                                           _P, _P, ctypes.c_size_t, _P, _P]
+            L.kvq_decode_attn_tc.restype = ctypes.c_int
+            L.kvq_decode_attn_tc.argtypes = L.kvq_decode_attn.argtypes
             L.kvq_dequant.restype = ctypes.c_int
             L.kvq_dequant.argtypes = [_CP, ctypes.c_int32, _P, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]
             L.kvq_status_string.restype = ctypes.c_char_p
@@ -233,8 +235,12 @@ def decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head
 def decode_attn(cache: Fp4Cache, seq_lens: torch.Tensor, q: torch.Tensor, softmax_scale: Optional[float] = None,
                 swa: Optional[Fp8WindowCache] = None, out: Optional[torch.Tensor] = None,
                 workspace: Optional[torch.Tensor] = None, err: Optional[torch.Tensor] = None,
-                stream=None) -> torch.Tensor:
-    """kvq_decode_attn: q bf16 [batch][Hq][head_dim] -> out float32 [batch][Hq][head_dim]."""
+                stream=None, kernel: str = "mma") -> torch.Tensor:
+    """kvq_decode_attn: q bf16 [batch][Hq][head_dim] -> out float32 [batch][Hq][head_dim].
+    kernel="tcgen05" calls kvq_decode_attn_tc instead (head_dim 128: both
+    products on the tensor-memory MMA; a measured, slower alternative)."""
+    if kernel not in ("mma", "tcgen05"):
+        raise ValueError(f"unknown decode kernel {kernel!r}")
     _need(q, torch.bfloat16, "q")
     _need(seq_lens, torch.int32, "seq_lens")
     batch, hq, d = q.shape
@@ -248,10 +254,11 @@ def decode_attn(cache: Fp4Cache, seq_lens: torch.Tensor, q: torch.Tensor, softma
         softmax_scale = 1.0 / math.sqrt(d)
     g = cache.struct()
     w = swa.struct() if swa is not None else None
-    st = load().kvq_decode_attn(ctypes.byref(g), ctypes.byref(w) if w is not None else None, batch, hq,
-                                _ptr(seq_lens), _ptr(q), float(softmax_scale), _ptr(out), _ptr(workspace),
-                                workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream))
-    _check(st, "kvq_decode_attn")
+    fn = load().kvq_decode_attn_tc if kernel == "tcgen05" else load().kvq_decode_attn
+    st = fn(ctypes.byref(g), ctypes.byref(w) if w is not None else None, batch, hq, _ptr(seq_lens), _ptr(q),
+            float(softmax_scale), _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+            _ptr(err), _stream(stream))
+    _check(st, "kvq_decode_attn_tc" if kernel == "tcgen05" else "kvq_decode_attn")
     return out
 
 

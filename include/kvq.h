@@ -237,6 +237,26 @@ kvq_status kvq_decode_attn_noalloc(const kvq_cache *global, const kvq_cache *swa
                                    kvq_stream stream);
 
 /*
+ * kvq_decode_attn_tc -- kvq_decode_attn for head_dim 128 with both products
+ * on the 5th-generation tensor cores: per 128-token stage the E2M1 x E4M3
+ * expansion of K^ (tokens on TMEM lanes) and of V^T (channels on TMEM lanes)
+ * goes to tensor memory, S = K^ Q^T and O^T += V^T P^T run as tcgen05.mma
+ * M=128 N=16 (8 query rows padded), O stays in tensor memory, and three
+ * independent pipelines share an SM.  ("Quantising the KV cache", section
+ * "Code"; "KV Cache Quantisation", section "Common questions".)  Same
+ * arguments, workspace, results (within the decode tolerance) and device flags
+ * as kvq_decode_attn; head_dim 64 returns KVQ_ERR_UNSUPPORTED.  It is a
+ * measured alternative, not the default: on GB300 at 32k context it runs
+ * about 1.5x slower than kvq_decode_attn (the channel split of V^T that
+ * tensor-memory lanes impose costs more instructions than the tensor-core
+ * products save, and the per-stage warpgroup barriers stall).
+ */
+kvq_status kvq_decode_attn_tc(const kvq_cache *global, const kvq_cache *swa, int32_t batch,
+                              int32_t num_q_heads, const int32_t *d_seq_lens, const void *q,
+                              float softmax_scale, float *out, void *workspace,
+                              size_t workspace_bytes, int32_t *d_err_flag, kvq_stream stream);
+
+/*
  * kvq_prefill_attn -- attention of a chunk of new query tokens over the FP4 or
  * NVFP4 cache that already holds their keys and values (chunked prefill):
  * query token i of sequence b (0 <= i < chunk) sits at position

@@ -25,7 +25,7 @@ def _lib():
     ensure_built()
 
 
-def run_loop(w, lens, steps, check_steps, units_of_step, seed=0):
+def run_loop(w, lens, steps, check_steps, units_of_step, seed=0, kernel="mma"):
     W = w.window
     built = build_fp4(w, lens, seed=seed, reserve=steps + 1)
     B, Hkv, d, G = w.batch, w.num_kv_heads, w.head_dim, w.group
@@ -60,7 +60,7 @@ def run_loop(w, lens, steps, check_steps, units_of_step, seed=0):
         T += 1
         lens_dev = torch.full((B,), T, dtype=torch.int32, device="cuda")
         q = workloads.queries(w, seed=seed, step=step, device="cuda")
-        out = kvq.decode_attn(built.cache, lens_dev, q, scale, swa=swa, err=err)
+        out = kvq.decode_attn(built.cache, lens_dev, q, scale, swa=swa, err=err, kernel=kernel)
         for b in range(B):
             host_k[b] = torch.cat([host_k[b], kn[b, :1].float().cpu()])
             host_v[b] = torch.cat([host_v[b], vn[b, :1].float().cpu()])
