@@ -170,10 +170,14 @@ def fp4_bytes_per_token(w) -> int:
 class Setup:
     """The resident FP4 cache of a workload plus the per-step inputs."""
 
-    def __init__(self, w, seed: int, device, layers: int = 1, nvfp4: bool = False, kernel: str = "mma"):
+    def __init__(self, w, seed: int, device, layers: int = 1, nvfp4: bool = False, kernel: str = "mma",
+                 fused: bool = True):
         from fp4_kv_cache_kvq_gb300 import kvq
         self.w = w
         self.kernel = kernel
+        # the append fused into the decode launch (kvq_append_decode_attn):
+        # caches without an FP8 window, decoded by the default kernel
+        self.fused = fused and w.window == 0 and kernel == "mma"
         self.layers = layers
         self.kvq = kvq
         self.lens0 = workloads.lengths(w, seed)
@@ -232,6 +236,8 @@ class Setup:
         toks = [workloads.step_tokens(w, i, seed=seed, device=device) for i in range(CYCLE)]
         self.k_new = [t[0] for t in toks]
         self.v_new = [t[1] for t in toks]
+        self.k_row = [k[:, 0] for k in self.k_new]  # [B][Hkv][d] views for the fused call
+        self.v_row = [v[:, 0] for v in self.v_new]
         self.q = [workloads.queries(w, seed=seed, step=i, device=device) for i in range(NQ)]
         base = torch.tensor(self.lens0, dtype=torch.int32, device=device)
         self.pos = [base + i for i in range(CYCLE)]
@@ -253,13 +259,24 @@ class Setup:
         kvq = self.kvq
         kk = self.k_new[s] if k is None else k
         vv = self.v_new[s] if v is None else v
+        qq = self.q[i % NQ] if q is None else q
+        if self.fused:
+            if ev is not None:
+                ev[0].record()
+            kr = self.k_row[s] if k is None else kk[:, 0]
+            vr = self.v_row[s] if v is None else vv[:, 0]
+            for cache, out in zip(self.caches, self.outs if outs is None else outs):
+                kvq.append_decode_attn(cache, self.lens[s], kr, vr, qq, self.scale, out=out, workspace=self.ws,
+                                       err=self.err)
+            if ev is not None:
+                ev[1].record()
+            return self.kv_tokens[s] * self.layers
         for cache, swa in zip(self.caches, self.swas):
             kvq.append(cache, self.pos[s], kk, vv, err=self.err)
             if swa is not None:
                 kvq.append(swa, self.pos[s], kk, vv, err=self.err)
         if ev is not None:
             ev[0].record()
-        qq = self.q[i % NQ] if q is None else q
         for cache, swa, out in zip(self.caches, self.swas, self.outs if outs is None else outs):
             kvq.decode_attn(cache, self.lens[s], qq, self.scale, swa=swa, out=out, workspace=self.ws, err=self.err,
                             kernel=self.kernel)
@@ -325,7 +342,8 @@ def run_gpu(args, dist: Dist):
     build.build()
     w = workloads.WORKLOADS[args.workload]
     L = args.layers
-    st = Setup(w, args.seed, device, layers=L, nvfp4=args.format == "nvfp4", kernel=args.decode_kernel)
+    st = Setup(w, args.seed, device, layers=L, nvfp4=args.format == "nvfp4", kernel=args.decode_kernel,
+               fused=args.fused_append)
     K, Wm = args.steps, args.warmup
     for i in range(Wm):
         st.step(i)
@@ -497,12 +515,15 @@ def run_gpu(args, dist: Dist):
                    else "eager launches",
                    "parallelism": f"replicas x{dist.world}",
                    "decode_kernel": "kvq_decode_attn_tc (tcgen05)" if args.decode_kernel == "tcgen05"
+                   else "kvq_append_decode_attn (append fused into the mma.sync decode)" if st.fused
                    else "kvq_decode_attn (mma.sync)"},
         "value_l2_warm": warm_value,
         "hbm_gbs_step": step_bytes * K / elapsed_s / 1e9,
         "hbm_gbs_decode": achieved,
         "hbm_pct_of_8tbs_decode": 100.0 * achieved / 8000.0,
-        "roofline": {"bound": "hbm", "kernel": "kvq_decode_attn (split-K decode + merge launches)"
+        "roofline": {"bound": "hbm", "kernel": ("kvq_append_decode_attn (append fused into the split-K decode, "
+                                                "+ merge launch)" if st.fused
+                                                else "kvq_decode_attn (split-K decode + merge launches)")
                      + (", FP8 window folded into the merge" if w.window else ""),
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_src,
@@ -513,7 +534,7 @@ def run_gpu(args, dist: Dist):
                      "min_launch_ms": min(decode_ms) / L},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": Ke},
-        "gpu_launches": L * (4 if w.window else 3) * K,
+        "gpu_launches": L * (4 if w.window else 2 if st.fused else 3) * K,
     }
     if clk is not None:
         result["clocks"] = clk
@@ -1201,6 +1222,9 @@ def main(argv=None):
     ap.add_argument("--decode-kernel", choices=["mma", "tcgen05"], default="mma",
                     help="decode kernel: mma (kvq_decode_attn, the default) or tcgen05 (kvq_decode_attn_tc, "
                          "head_dim 128 only, a measured slower alternative)")
+    ap.add_argument("--fused-append", action=argparse.BooleanOptionalAction, default=True,
+                    help="each step as one kvq_append_decode_attn call (the append fused into the decode launch; "
+                         "workloads without an FP8 window) instead of kvq_append then kvq_decode_attn")
     ap.add_argument("--graphs", action=argparse.BooleanOptionalAction, default=False,
                     help="replay each step's appends and decode from CUDA graphs (decode workloads)")
     args = ap.parse_args(argv)

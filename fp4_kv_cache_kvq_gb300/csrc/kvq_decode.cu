@@ -43,6 +43,7 @@
 // up to 8 query heads fills N = 8 without padding rows.  The query is
 // pre-scaled per head by a power of two so that its bf16 values are exact in
 // f16; the factor is undone in fp32.
+#include "kvq_append.cuh"
 #include "kvq_common.cuh"
 #include "kvq_decode.cuh"
 #include "kvq_host.cuh"
@@ -103,12 +104,112 @@ __device__ __forceinline__ Smem<D> carve(uint8_t* raw) {
 }
 
 // ------------------------------------------------------------------ producer
+// Fused append (kvq_append_decode_attn): the newest token of unit (b, h),
+// position T_b - 1, quantised and stored into the pool by the producer warp
+// -- lanes 0 .. NQK-1 take the K items, the next NQV lanes the V item of its
+// token pair -- exactly as kvq_append with one new token would; then every
+// lane's stores are made visible to the bulk-copy (async) proxy before any
+// later copy of the warp reads them.
+template <int D>
+__device__ void append_newest(const DecodeParams& p, int b, int h) {
+  constexpr int NQK = D / 16 / kAppendBlocksK, NQV = D / 16 / kAppendBlocksV;
+  const int lane = threadIdx.x & 31;
+  if (lane < NQK + NQV) {
+    const int64_t pos = (int64_t)__ldg(p.lens + b) - 1;
+    const int64_t row = ((int64_t)b * p.hkv + h) * D;
+    int ls = 0;
+    if (lane < NQK) {
+      const int j0 = lane * kAppendBlocksK;
+      uint8_t* grp = fp4_group<D>(p.cache, b, pos, h, ls, p.flag);
+      if (grp != nullptr) {
+        if (p.nvfp4)
+          append_k_item<D, true>(p.cache, grp, ls, h, j0, p.k_new + row + 16 * j0, p.flag);
+        else
+          append_k_item<D, false>(p.cache, grp, ls, h, j0, p.k_new + row + 16 * j0, p.flag);
+      }
+    } else {
+      const int j0 = (lane - NQK) * kAppendBlocksV;
+      uint8_t* grp = fp4_group<D>(p.cache, b, pos & ~(int64_t)1, h, ls, p.flag);
+      if (grp != nullptr) {
+        const bool even = (pos & 1) == 0;  // the new token is the pair's first (else its second)
+        const uint16_t* src = p.v_new + row + 16 * j0;
+        if (p.nvfp4)
+          append_v_item<D, true>(p.cache, grp, ls, h, j0, even, !even, src, src, p.flag);
+        else
+          append_v_item<D, false>(p.cache, grp, ls, h, j0, even, !even, src, src, p.flag);
+      }
+    }
+  }
+  asm volatile("fence.proxy.async.global;\n" ::: "memory");
+  __syncwarp();
+}
+
+// Issue the bulk copies of one chunk into ring stage s (producer lane 0).
 template <int D, int GT>
-__device__ void producer(const DecodeParams& p, Smem<D>& sm, Walker wk, int64_t v1) {
+__device__ __forceinline__ void issue_chunk(const DecodeParams& p, Smem<D>& sm, const Walker& wk, uint32_t s) {
   using G = Geo<D>;
   using R = Grp<D, GT>;
   const int P = p.page;
+  const int n4 = fp4_tokens(__ldg(p.lens + wk.b), p.window);
+  const int tok0 = wk.c * kChunk;
+  const int ntok = min(kChunk, n4 - tok0);
+  // one copy per pool group: a 128-token group of a larger page, or whole small pages
+  const int ncopies = GT < kChunk ? (ntok + GT - 1) / GT : 1;
+  const int pg0 = tok0 / P;
+  const int groups_per_page = P / GT;
+  const int grp0 = GT < kChunk ? 0 : (tok0 % P) / GT;
+  int64_t src[kMaxCopies];
+  bool ok = true;
+  for (int i = 0; i < ncopies; ++i) {
+    const int pg = pg0 + i;
+    int64_t ph = -1;
+    if (pg < p.max_pages)
+      ph = p.page_table ? (int64_t)__ldg(p.page_table + (int64_t)wk.b * p.max_pages + pg)
+                        : (int64_t)wk.b * p.max_pages + pg;
+    if (ph < 0 || ph >= p.num_pages) ok = false;
+    src[i] = ((ph * p.hkv + wk.h) * groups_per_page + grp0) * (int64_t)R::kBytes;
+  }
+  const uint32_t full = smem_addr(&sm.full[s]);
+  uint8_t* st = sm.stages + s * G::kStageBytes;
+  if (!ok) {
+    set_flag(p.flag, KVQ_FLAG_PAGE_OOB);
+    sm.ntok[s] = 0;
+    mbar_arrive(full);
+    return;
+  }
+  sm.ntok[s] = ntok;
+  mbar_arrive_expect_tx(full, (uint32_t)(ncopies * R::kBytes));
+  for (int i = 0; i < ncopies; ++i) bulk_g2s(smem_addr(st + i * R::kBytes), p.pool + src[i], R::kBytes, full);
+}
+
+// The producer warp.  Lane 0 waits for free ring stages and issues the bulk
+// copies.  With a fused append (FUSED) the whole warp first stores the newest
+// token of every unit whose last chunk lies in this CTA's range: the units
+// ending in the first kStages chunks before those chunks are copied, the
+// rest while those first copies are in flight, so the stores never hold up
+// a refill of the ring.  The other lanes then leave and lane 0 goes on alone.
+template <int D, int GT, bool FUSED>
+__device__ void producer(const DecodeParams& p, Smem<D>& sm, Walker wk, int64_t v1) {
+  const int lane = threadIdx.x & 31;
+  if (!FUSED && lane != 0) return;
   uint32_t it = 0;
+  if (FUSED) {
+    Walker aw = wk;
+    for (int i = 0; i < kStages && aw.v < v1; ++i, advance(p, aw))
+      if (aw.c == aw.nch - 1) append_newest<D>(p, aw.b, aw.h);
+    for (; it < (uint32_t)kStages && wk.v < v1; advance(p, wk), ++it)
+      if (lane == 0) issue_chunk<D, GT>(p, sm, wk, it);
+    // the remaining unit ends of the range, one unit at a time
+    while (aw.v < v1) {
+      const int64_t last = aw.v + (aw.nch - 1 - aw.c);  // the unit's last chunk on the line
+      if (last >= v1) break;
+      append_newest<D>(p, aw.b, aw.h);
+      aw.v = last;
+      aw.c = aw.nch - 1;
+      advance(p, aw);
+    }
+    if (lane != 0) return;
+  }
   for (; wk.v < v1; advance(p, wk), ++it) {
     const uint32_t s = it % kStages;
     if (it >= (uint32_t)kStages) {
@@ -119,36 +220,7 @@ __device__ void producer(const DecodeParams& p, Smem<D>& sm, Walker wk, int64_t 
       }
     }
     if (*reinterpret_cast<volatile int*>(sm.abort)) break;
-    const int n4 = fp4_tokens(__ldg(p.lens + wk.b), p.window);
-    const int tok0 = wk.c * kChunk;
-    const int ntok = min(kChunk, n4 - tok0);
-    // one copy per pool group: a 128-token group of a larger page, or whole small pages
-    const int ncopies = GT < kChunk ? (ntok + GT - 1) / GT : 1;
-    const int pg0 = tok0 / P;
-    const int groups_per_page = P / GT;
-    const int grp0 = GT < kChunk ? 0 : (tok0 % P) / GT;
-    int64_t src[kMaxCopies];
-    bool ok = true;
-    for (int i = 0; i < ncopies; ++i) {
-      const int pg = pg0 + i;
-      int64_t ph = -1;
-      if (pg < p.max_pages)
-        ph = p.page_table ? (int64_t)__ldg(p.page_table + (int64_t)wk.b * p.max_pages + pg)
-                          : (int64_t)wk.b * p.max_pages + pg;
-      if (ph < 0 || ph >= p.num_pages) ok = false;
-      src[i] = ((ph * p.hkv + wk.h) * groups_per_page + grp0) * (int64_t)R::kBytes;
-    }
-    const uint32_t full = smem_addr(&sm.full[s]);
-    uint8_t* st = sm.stages + s * G::kStageBytes;
-    if (!ok) {
-      set_flag(p.flag, KVQ_FLAG_PAGE_OOB);
-      sm.ntok[s] = 0;
-      mbar_arrive(full);
-      continue;
-    }
-    sm.ntok[s] = ntok;
-    mbar_arrive_expect_tx(full, (uint32_t)(ncopies * R::kBytes));
-    for (int i = 0; i < ncopies; ++i) bulk_g2s(smem_addr(st + i * R::kBytes), p.pool + src[i], R::kBytes, full);
+    issue_chunk<D, GT>(p, sm, wk, s);
   }
   // Wait for every copy still in flight before the CTA can retire.
   const uint32_t issued = it;
@@ -466,7 +538,7 @@ __device__ void flush_unit(const DecodeParams& p, ConsumerState<D>& st, Smem<D>&
   }
 }
 
-template <int D, int GT>
+template <int D, int GT, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_fp4_kernel(const DecodeParams p) {
   using G = Geo<D>;
@@ -492,9 +564,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   if (v0 >= v1) return;
 
   if (warp == kConsumerWarps) {
-    if (lane == 0) {
-      producer<D, GT>(p, sm, wk, v1);
-    }
+    producer<D, GT, FUSED>(p, sm, wk, v1);
     return;
   }
 
@@ -821,20 +891,25 @@ WsLayout ws_layout(int64_t batch, int64_t hkv, int64_t g, int64_t d, int64_t cta
 
 int decode_ctas() { return 3 * device_sm_count(); }
 
-template <int D, int GT>
-kvq_status launch_decode_g(const DecodeParams& dp, cudaStream_t s, int ctas) {
+template <int D, int GT, bool FUSED>
+kvq_status launch_decode_f(const DecodeParams& dp, cudaStream_t s, int ctas) {
   const int smem = Geo<D>::kSmemBytes;
   static DeviceOnce attr_set;  // the shared-memory opt-in, once per device
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
   if (attr_set.pending(dev)) {
-    if (cudaFuncSetAttribute(decode_fp4_kernel<D, GT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    if (cudaFuncSetAttribute(decode_fp4_kernel<D, GT, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return KVQ_ERR_CUDA;
     attr_set.mark(dev);
   }
-  decode_fp4_kernel<D, GT><<<ctas, kThreads, smem, s>>>(dp);
+  decode_fp4_kernel<D, GT, FUSED><<<ctas, kThreads, smem, s>>>(dp);
   return launch_status();
+}
+
+template <int D, int GT>
+kvq_status launch_decode_g(const DecodeParams& dp, cudaStream_t s, int ctas) {
+  return dp.k_new != nullptr ? launch_decode_f<D, GT, true>(dp, s, ctas) : launch_decode_f<D, GT, false>(dp, s, ctas);
 }
 
 template <int D>
@@ -864,11 +939,14 @@ extern "C" size_t kvq_decode_workspace_bytes(int32_t batch, int32_t num_q_heads,
 
 namespace {
 
-// kvq_decode_attn and kvq_decode_attn_tc: the same checks, workspace, partials
-// and merge; `tcgen05` picks the tensor-memory decode kernel (head_dim 128).
+// kvq_decode_attn, kvq_decode_attn_tc and kvq_append_decode_attn: the same
+// checks, workspace, partials and merge; `tcgen05` picks the tensor-memory
+// decode kernel (head_dim 128); k_new / v_new (non-null) fuse the append of
+// every sequence's newest token into the decode kernel.
 kvq_status decode_attn(const kvq_cache* global, const kvq_cache* swa, int32_t batch, int32_t num_q_heads,
-                       const int32_t* d_seq_lens, const void* q, float softmax_scale, float* out, void* workspace,
-                       size_t workspace_bytes, int32_t* d_err_flag, kvq_stream stream, bool tcgen05) {
+                       const int32_t* d_seq_lens, const void* k_new, const void* v_new, const void* q,
+                       float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                       int32_t* d_err_flag, kvq_stream stream, bool tcgen05) {
   if (batch < 1) return KVQ_ERR_INVALID_ARGUMENT;
   kvq_status st = check_cache(global, batch);
   if (st != KVQ_OK) return st;
@@ -880,6 +958,10 @@ kvq_status decode_attn(const kvq_cache* global, const kvq_cache* swa, int32_t ba
   if (d_seq_lens == nullptr || q == nullptr || out == nullptr || workspace == nullptr)
     return KVQ_ERR_INVALID_ARGUMENT;
   if (!aligned_to(q, 16) || !aligned_to(out, 16) || !aligned_to(workspace, 16)) return KVQ_ERR_INVALID_ARGUMENT;
+  const bool fused = k_new != nullptr || v_new != nullptr;
+  if (fused && (k_new == nullptr || v_new == nullptr || !aligned_to(k_new, 16) || !aligned_to(v_new, 16)))
+    return KVQ_ERR_INVALID_ARGUMENT;
+  if (fused && (swa != nullptr || tcgen05)) return KVQ_ERR_UNSUPPORTED;
   if (swa != nullptr) {
     st = check_cache(swa, batch);
     if (st != KVQ_OK) return st;
@@ -897,7 +979,7 @@ kvq_status decode_attn(const kvq_cache* global, const kvq_cache* swa, int32_t ba
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  DecodeParams dp;
+  DecodeParams dp = {};
   dp.lens = d_seq_lens;
   dp.page_table = global->page_table;
   dp.pool = static_cast<const uint8_t*>(global->data);
@@ -918,6 +1000,10 @@ kvq_status decode_attn(const kvq_cache* global, const kvq_cache* swa, int32_t ba
   dp.max_pages = global->max_pages_per_seq;
   dp.window = swa ? swa->page_size : 0;
   dp.qk_log2 = softmax_scale * kLog2e;
+  dp.k_new = fused ? static_cast<const uint16_t*>(k_new) : nullptr;
+  dp.v_new = fused ? static_cast<const uint16_t*>(v_new) : nullptr;
+  dp.cache = *global;
+  dp.nvfp4 = nv ? 1 : 0;
   if (tcgen05)
     st = launch_decode_tc(dp, s);
   else
@@ -960,16 +1046,25 @@ extern "C" kvq_status kvq_decode_attn(const kvq_cache* global, const kvq_cache* 
                                       int32_t num_q_heads, const int32_t* d_seq_lens, const void* q,
                                       float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
                                       int32_t* d_err_flag, kvq_stream stream) {
-  return decode_attn(global, swa, batch, num_q_heads, d_seq_lens, q, softmax_scale, out, workspace,
-                     workspace_bytes, d_err_flag, stream, false);
+  return decode_attn(global, swa, batch, num_q_heads, d_seq_lens, nullptr, nullptr, q, softmax_scale, out,
+                     workspace, workspace_bytes, d_err_flag, stream, false);
+}
+
+extern "C" kvq_status kvq_append_decode_attn(const kvq_cache* global, int32_t batch, int32_t num_q_heads,
+                                             const int32_t* d_seq_lens, const void* k_new, const void* v_new,
+                                             const void* q, float softmax_scale, float* out, void* workspace,
+                                             size_t workspace_bytes, int32_t* d_err_flag, kvq_stream stream) {
+  if (k_new == nullptr || v_new == nullptr) return KVQ_ERR_INVALID_ARGUMENT;
+  return decode_attn(global, nullptr, batch, num_q_heads, d_seq_lens, k_new, v_new, q, softmax_scale, out,
+                     workspace, workspace_bytes, d_err_flag, stream, false);
 }
 
 extern "C" kvq_status kvq_decode_attn_tc(const kvq_cache* global, const kvq_cache* swa, int32_t batch,
                                          int32_t num_q_heads, const int32_t* d_seq_lens, const void* q,
                                          float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
                                          int32_t* d_err_flag, kvq_stream stream) {
-  return decode_attn(global, swa, batch, num_q_heads, d_seq_lens, q, softmax_scale, out, workspace,
-                     workspace_bytes, d_err_flag, stream, true);
+  return decode_attn(global, swa, batch, num_q_heads, d_seq_lens, nullptr, nullptr, q, softmax_scale, out,
+                     workspace, workspace_bytes, d_err_flag, stream, true);
 }
 
 // ------------------------------------------------------------------ decode without caller scratch

@@ -22,6 +22,12 @@ struct DecodeParams {
   int64_t num_pages;
   int32_t batch, hkv, g, hq, page, max_pages, window;
   float qk_log2;  // softmax_scale * log2(e)
+  // fused append of each sequence's newest token (position T_b - 1) before
+  // the decode reads it (kvq_append_decode_attn); k_new == nullptr: none
+  const uint16_t* k_new;  // bf16 [batch][Hkv][head_dim]
+  const uint16_t* v_new;
+  kvq_cache cache;        // the FP4 / NVFP4 cache written
+  int32_t nvfp4;
 };
 
 // The head_dim 128 decode on the tensor cores (kvq_decode_tc.cu): one CTA per

@@ -85,6 +85,9 @@ def load() -> ctypes.CDLL:
                                           _P, _P, ctypes.c_size_t, _P, _P]
             L.kvq_decode_attn_tc.restype = ctypes.c_int
             L.kvq_decode_attn_tc.argtypes = L.kvq_decode_attn.argtypes
+            L.kvq_append_decode_attn.restype = ctypes.c_int
+            L.kvq_append_decode_attn.argtypes = [_CP, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, ctypes.c_float,
+                                                 _P, _P, ctypes.c_size_t, _P, _P]
             L.kvq_dequant.restype = ctypes.c_int
             L.kvq_dequant.argtypes = [_CP, ctypes.c_int32, _P, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P]
             L.kvq_status_string.restype = ctypes.c_char_p
@@ -168,10 +171,20 @@ class Fp4Cache:
         self.v_gscale = torch.ones(num_kv_heads, dtype=torch.float32, device=device) if nvfp4 else None
 
     def struct(self, page_table: Optional[torch.Tensor] = None) -> KvqCacheStruct:
+        """The kvq_cache description (kept between calls while the tensors it
+        points at are the same objects; a page_table argument overrides the
+        cache's own for one call)."""
         pt = self.page_table if page_table is None else page_table
-        return KvqCacheStruct(FORMAT_NVFP4 if self.nvfp4 else FORMAT_FP4, self.num_kv_heads, self.head_dim,
-                              self.page_size, self.num_pages, self.max_pages_per_seq, 0, _ptr(pt), _ptr(self.pool),
-                              None, _ptr(self.k_gscale), _ptr(self.v_gscale))
+        key = (id(self.pool), id(pt), id(self.k_gscale), id(self.v_gscale))
+        cached = self.__dict__.get("_struct")
+        if cached is not None and cached[0] == key:
+            return cached[1]
+        s = KvqCacheStruct(FORMAT_NVFP4 if self.nvfp4 else FORMAT_FP4, self.num_kv_heads, self.head_dim,
+                           self.page_size, self.num_pages, self.max_pages_per_seq, 0, _ptr(pt), _ptr(self.pool),
+                           None, _ptr(self.k_gscale), _ptr(self.v_gscale))
+        if page_table is None:
+            self._struct = (key, s)
+        return s
 
     @property
     def nbytes(self) -> int:
@@ -195,9 +208,15 @@ class Fp8WindowCache:
         self.v_scales = torch.ones_like(self.k_scales)
 
     def struct(self) -> KvqCacheStruct:
-        return KvqCacheStruct(FORMAT_FP8, self.num_kv_heads, self.head_dim, self.window, self.num_seqs, 0, 0,
-                              None, _ptr(self.k_codes), _ptr(self.v_codes), _ptr(self.k_scales),
-                              _ptr(self.v_scales))
+        """The kvq_cache description (kept while the tensors are the same objects)."""
+        key = (id(self.k_codes), id(self.v_codes), id(self.k_scales), id(self.v_scales))
+        cached = self.__dict__.get("_struct")
+        if cached is not None and cached[0] == key:
+            return cached[1]
+        s = KvqCacheStruct(FORMAT_FP8, self.num_kv_heads, self.head_dim, self.window, self.num_seqs, 0, 0,
+                           None, _ptr(self.k_codes), _ptr(self.v_codes), _ptr(self.k_scales), _ptr(self.v_scales))
+        self._struct = (key, s)
+        return s
 
 
 
@@ -259,6 +278,33 @@ def decode_attn(cache: Fp4Cache, seq_lens: torch.Tensor, q: torch.Tensor, softma
             float(softmax_scale), _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
             _ptr(err), _stream(stream))
     _check(st, "kvq_decode_attn_tc" if kernel == "tcgen05" else "kvq_decode_attn")
+    return out
+
+
+def append_decode_attn(cache: Fp4Cache, seq_lens: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                       q: torch.Tensor, softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None, err: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
+    """kvq_append_decode_attn: append k_new/v_new bf16 [batch][Hkv][head_dim] at
+    position seq_lens[b] - 1, then decode attention over seq_lens[b] positions."""
+    _need(q, torch.bfloat16, "q")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(k_new, torch.bfloat16, "k_new")
+    _need(v_new, torch.bfloat16, "v_new")
+    batch, hq, d = q.shape
+    if out is None:
+        out = torch.empty((batch, hq, d), dtype=torch.float32, device=q.device)
+    _need(out, torch.float32, "out")
+    if workspace is None:
+        need = decode_workspace_bytes(batch, hq, cache.num_kv_heads, d)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    g = cache.struct()
+    st = load().kvq_append_decode_attn(ctypes.byref(g), batch, hq, _ptr(seq_lens), _ptr(k_new), _ptr(v_new), _ptr(q),
+                                       float(softmax_scale), _ptr(out), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _ptr(err), _stream(stream))
+    _check(st, "kvq_append_decode_attn")
     return out
 
 

@@ -237,6 +237,32 @@ kvq_status kvq_decode_attn_noalloc(const kvq_cache *global, const kvq_cache *swa
                                    kvq_stream stream);
 
 /*
+ * kvq_append_decode_attn -- one decode step with its append fused in:
+ * kvq_append of one new token per sequence at position T_b - 1 followed by
+ * kvq_decode_attn over positions 0..T_b-1, in one decode launch (plus the
+ * merge).  ("Quantising the KV cache", section "Code": each new K/V row is
+ * quantised as it enters the cache, and attention reads it back.)  The codes
+ * and scale bytes written equal those of kvq_append (same quantiser, same
+ * placement), and the output equals that of kvq_append followed by
+ * kvq_decode_attn.  The producer warp of the CTA that reads a sequence's
+ * last chunk stores that sequence's new token a few chunks before copying
+ * it, so no separate append launch is needed.
+ *   global       FP4 or NVFP4 cache (head_dim 64 or 128), as kvq_decode_attn.
+ *   d_seq_lens   device int32 [batch]: T_b including the new token; T_b == 0
+ *                appends nothing and gives a zero output row.
+ *   k_new, v_new device bf16 [batch][num_kv_heads][head_dim], 16-byte aligned:
+ *                the new token of every sequence (row b is ignored when
+ *                T_b == 0).
+ *   other arguments, workspace and device flags as kvq_decode_attn, plus the
+ *   append's NONFINITE flag.  There is no FP8 window form: with a sliding
+ *   window, call kvq_append on both caches and then kvq_decode_attn.
+ */
+kvq_status kvq_append_decode_attn(const kvq_cache *global, int32_t batch, int32_t num_q_heads,
+                                  const int32_t *d_seq_lens, const void *k_new, const void *v_new,
+                                  const void *q, float softmax_scale, float *out, void *workspace,
+                                  size_t workspace_bytes, int32_t *d_err_flag, kvq_stream stream);
+
+/*
  * kvq_decode_attn_tc -- kvq_decode_attn for head_dim 128 with both products
  * on the 5th-generation tensor cores: per 128-token stage the E2M1 x E4M3
  * expansion of K^ (tokens on TMEM lanes) and of V^T (channels on TMEM lanes)
