@@ -41,12 +41,16 @@ from fp4_kv_cache_kvq_gb300 import workloads  # noqa: E402
 
 METRIC = "decode-attn KV-tokens/s and achieved HBM GB/s (% of ~8 TB/s) on FP4 cache, 1xGB300"
 UNIT = "KV-tokens/s"
+PREROLL_US = 100    # GPU-side wait queued ahead of a timed region
 CYCLE = 64          # appended positions cycle through this many slots after the context
 NQ = 8              # distinct query sets cycled through the steps
 FALLBACK_HBM_GBS = 6800.0
-DECODE_SRC = os.path.join(ROOT, "fp4_kv_cache_kvq_gb300", "csrc", "kvq_decode.cu")
+_CSRC = os.path.join(ROOT, "fp4_kv_cache_kvq_gb300", "csrc")
+# the sources a committed capture's kernel is compiled from (hashed together)
+DECODE_SRC = tuple(os.path.join(_CSRC, f) for f in ("kvq_decode_kernel.cuh", "kvq_decode.cu", "kvq_append.cuh",
+                                                    "kvq_common.cuh"))
 PROFILE = os.path.join(ROOT, "profiles", "decode_fp4_long_context.md")
-APPEND_SRC = os.path.join(ROOT, "fp4_kv_cache_kvq_gb300", "csrc", "kvq_append.cu")
+APPEND_SRC = tuple(os.path.join(_CSRC, f) for f in ("kvq_append.cu", "kvq_append.cuh", "kvq_common.cuh"))
 APPEND_PROFILE = os.path.join(ROOT, "profiles", "append_fp4_prefill.md")
 PREFILL_SRC = os.path.join(ROOT, "fp4_kv_cache_kvq_gb300", "csrc", "kvq_prefill.cu")
 PREFILL_PROFILE = os.path.join(ROOT, "profiles", "prefill_fp4_prefill_attn.md")
@@ -148,18 +152,36 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def source_sha256(src) -> str:
+    """sha256 of a kernel's source: one file, or several files' bytes in order."""
+    h = hashlib.sha256()
+    for f in ((src,) if isinstance(src, str) else src):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def profiled_traffic(profile=PROFILE, src=DECODE_SRC, key="traffic_bytes_per_launch"):
     """DRAM bytes per launch (the summary's line `key`) from a committed ncu
     summary, if it was taken on the current kernel source (else None)."""
     try:
         text = open(profile).read()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        sha = source_sha256(src)
         fields = dict(line.split(":", 1) for line in text.splitlines() if line.startswith(("traffic_", "source_")))
         if fields.get("source_sha256", "").strip() != sha:
             return None
         return int(float(fields[key].strip()))
     except Exception:
         return None
+
+
+def flush_l2(buf, i: int):
+    """Evict L2 before a timed step: write `buf` (2 x L2) and then read it
+    back, so that L2 holds clean lines of an unrelated buffer (as after a
+    flush and invalidate) rather than dirty ones whose write-back would land
+    inside the next timed launch."""
+    buf.fill_(i & 0xFF)
+    buf.view(torch.int32).max()
 
 
 def fp4_bytes_per_token(w) -> int:
@@ -367,6 +389,18 @@ def run_gpu(args, dist: Dist):
     def run_step(i, ev=None):
         return st.step_graph(i, ev=ev) if args.graphs else st.step(i, ev=ev)
 
+    def preroll():
+        """Queue a GPU-side wait of about PREROLL_US before the first timed
+        event, so that the stream is busy while the host enqueues the first
+        step: the start event then marks the GPU reaching the steps, not the
+        host's latency from an idle stream.  After the first step the host
+        stays ahead by itself (a step's enqueue takes a fraction of its GPU
+        time), so this only removes the start-up gap."""
+        torch.cuda._sleep(int(PREROLL_US * 1e-6 * sm_hz))
+
+    sm_hz = torch.cuda.get_device_properties(device).clock_rate * 1e3 if hasattr(
+        torch.cuda.get_device_properties(device), "clock_rate") else 2.0e9
+
     def timed(flushed: bool):
         """K steps.  Back to back (events only at the two ends: a timing event
         between two kernels keeps the second from starting while the first
@@ -376,11 +410,12 @@ def run_gpu(args, dist: Dist):
         clocks = ClockSampler(device.index)
         dist.barrier()
         torch.cuda.synchronize()
+        preroll()
         t0.record()
         tokens = 0
         for i in range(K):
             if flushed:
-                flush.fill_(i & 0xFF)
+                flush_l2(flush, i)
                 steps[i][0].record()
             tokens += run_step(Wm + i)
             if flushed:
@@ -400,9 +435,10 @@ def run_gpu(args, dist: Dist):
         each step), for the roofline: the same steps, timed again."""
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
         torch.cuda.synchronize()
+        preroll()
         for i in range(K):
             if flushed:
-                flush.fill_(i & 0xFF)
+                flush_l2(flush, i)
             run_step(Wm + i, ev=evs[i])
         torch.cuda.synchronize()
         return [a.elapsed_time(b) for a, b in evs]
@@ -508,11 +544,15 @@ def run_gpu(args, dist: Dist):
                    "batch": w.batch, "kv_heads": w.num_kv_heads, "q_heads": w.num_q_heads,
                    "head_dim": w.head_dim, "context": w.context, "page_size": w.page_size,
                    "cache_bytes": st.cache.nbytes * L,
-                   "l2": (f"cache smaller than 2 x L2: {2 * l2_bytes} B written before every step, steps timed "
+                   "l2": (f"cache smaller than 2 x L2: {2 * l2_bytes} B written and read back before every step, "
+                          f"steps timed "
                           f"one by one (warm-L2 rate without the flush: {warm_value:.4g} {UNIT})") if small
                    else f"inputs larger than L2 (FP4 cache {st.cache.nbytes} B vs {l2_bytes} B L2), no flush",
                    "launch": "CUDA graphs (one per step of the cycle: appends, then decode)" if args.graphs
                    else "eager launches",
+                   "timing": f"a {PREROLL_US} us GPU-side wait is queued before the start event (and before "
+                             "the per-call events), so the host's enqueue of the first step from an idle "
+                             "stream is not timed",
                    "parallelism": f"replicas x{dist.world}",
                    "decode_kernel": "kvq_decode_attn_tc (tcgen05)" if args.decode_kernel == "tcgen05"
                    else "kvq_append_decode_attn (append fused into the mma.sync decode)" if st.fused
@@ -612,14 +652,17 @@ def append_oracle_sample(w, seed: int, budget_s: float, nvfp4: bool = False):
 
 
 def run_prefill(args, dist: Dist):
-    """A step appends a whole prefill (B16 x 16384 tokens, Hkv8, d128, bf16 K
-    and V) into the FP4 cache; value = appended tokens/s (one token = one
-    position of one sequence across all kv heads, K and V)."""
+    """A step appends a whole prefill (B16 x 16384 tokens, or B1 x 16384 for
+    prefill_b1; Hkv8, d128, bf16 K and V) into the FP4 cache; value = appended
+    tokens/s (one token = one position of one sequence across all kv heads, K
+    and V).  The B16 step reads 1.07 GB (past L2); the B1 step's 67 MB would
+    sit in L2, so that run writes a 2 x L2 buffer before every step and times
+    each append alone with events on its own stream position."""
     from fp4_kv_cache_kvq_gb300 import build, kvq
     device = torch.device("cuda", dist.local)
     torch.cuda.set_device(device)
     build.build()
-    w = workloads.WORKLOADS["prefill"]
+    w = workloads.WORKLOADS[args.workload]
     B, T = w.batch, w.context
     max_pages = -(-T // w.page_size)
     nv = args.format == "nvfp4"
@@ -633,22 +676,36 @@ def run_prefill(args, dist: Dist):
     if nv:  # second-level scales from the whole prefill (calibration, outside the timed region)
         kvq.fp8_set_scales(cache, k, v, err=err)
     K, Wm = args.steps, args.warmup
-    for _ in range(Wm):
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=device) if 2 * k.nbytes < 2 * l2 else None
+    for i in range(Wm):
+        if flush is not None:
+            flush_l2(flush, i)
         kvq.append(cache, start, k, v, err=err)
     torch.cuda.synchronize()
     clocks = ClockSampler(device.index)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     dist.barrier()
-    t0.record()
-    for _ in range(K):
-        kvq.append(cache, start, k, v, err=err)
-    t1.record()
-    torch.cuda.synchronize()
+    if flush is None:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(K):
+            kvq.append(cache, start, k, v, err=err)
+        t1.record()
+        torch.cuda.synchronize()
+        secs = t0.elapsed_time(t1) / 1e3
+    else:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            flush_l2(flush, i)
+            evs[i][0].record()
+            kvq.append(cache, start, k, v, err=err)
+            evs[i][1].record()
+        torch.cuda.synchronize()
+        secs = sum(a.elapsed_time(b) for a, b in evs) / 1e3
     dist.barrier()
     clk = clocks.stop()
     if err.item() != 0:
         raise RuntimeError(f"device error flag {err.item()}")
-    secs = t0.elapsed_time(t1) / 1e3
     tokens = B * T
     value, max_s = combine_ranks(dist, tokens * K, secs)
     nbytes = 2 * k.numel() * 2 + tokens * fp4_bytes_per_token(w)
@@ -673,15 +730,19 @@ def run_prefill(args, dist: Dist):
         "metric": PREFILL_METRIC, "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": K,
         "warmup": Wm, "ms_per_step": max_s * 1e3 / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"prefill: {w.description}" + (", NVFP4 cache" if nv else ""), "format": args.format,
+        "config": {"workload": f"{w.name}: {w.description}" + (", NVFP4 cache" if nv else ""), "format": args.format,
                    "batch": B, "tokens": T, "kv_heads": w.num_kv_heads,
                    "head_dim": w.head_dim, "page_size": w.page_size,
-                   "l2": "inputs larger than L2 (1.07 GB of bf16 per step), no flush",
+                   "l2": (f"inputs larger than L2 ({2 * k.nbytes / 1e9:.2f} GB of bf16 per step), no flush"
+                          if flush is None else
+                          f"L2 flushed before every step (a {2 * l2 >> 20} MiB buffer written and read back); "
+                          f"each append timed alone"),
                    "parallelism": f"replicas x{dist.world}"},
         "roofline": {"bound": "hbm", "kernel": "append_fp4_kernel", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
                      "traffic": profiled_traffic(APPEND_PROFILE, APPEND_SRC,
-                                                 "traffic_bytes_per_launch_nvfp4" if nv else "traffic_bytes_per_launch"),
+                                                 "traffic_bytes_per_launch" + ("_b1" if B == 1 else "")
+                                                 + ("_nvfp4" if nv else "")),
                      "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": secs * 1e3 / K},
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": 2 * k.numel() * 2, "d2h_bytes_per_step": 4,
                 "steps": Ke},
@@ -1087,7 +1148,7 @@ def run_reference_prefill(args):
     """The oracle's quantise-on-append of the prefill workload: each step one
     pass of an AppendOracleSample sized so that the whole run takes about
     reference_budget_s of host time."""
-    w = workloads.WORKLOADS["prefill"]
+    w = workloads.WORKLOADS[args.workload]
     nv = args.format == "nvfp4"
     cores = os.cpu_count() or 1
     with cf.ThreadPoolExecutor(max_workers=cores) as pool:
@@ -1103,7 +1164,7 @@ def run_reference_prefill(args):
             n, dt = sample.run(pool)
             toks += n
             secs += dt
-    config = {"workload": f"prefill: {w.description}" + (", NVFP4 cache" if nv else ""), "format": args.format,
+    config = {"workload": f"{w.name}: {w.description}" + (", NVFP4 cache" if nv else ""), "format": args.format,
               "batch": w.batch, "tokens": w.context, "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
               "page_size": w.page_size, "parallelism": "host threads"}
     return _reference_line(args, PREFILL_METRIC, "tokens/s", toks / secs, secs, "f32", config, cores,
@@ -1161,7 +1222,7 @@ def run_reference(args, dist: Dist):
         return None
     if args.workload == "swa_replay":
         return run_reference_replay(args)
-    if args.workload == "prefill":
+    if args.workload in ("prefill", "prefill_b1"):
         return run_reference_prefill(args)
     if args.workload == "prefill_attn":
         return run_reference_prefill_attn(args)
@@ -1209,7 +1270,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
     ap.add_argument("--workload", default="long_context",
                     choices=["long_context", "gqa_outliers", "paged_ragged", "swa_append", "tiny", "prefill",
-                             "prefill_attn", "swa_replay"])
+                             "prefill_b1", "prefill_attn", "swa_replay"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--format", choices=["fp4", "nvfp4"], default="fp4",
                     help="cache format: FP4 (E4M3 scale per 16) or NVFP4 (plus an fp32 scale per kv head)")
@@ -1234,7 +1295,7 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             res = run_reference(args, dist)
-        elif args.workload == "prefill":
+        elif args.workload in ("prefill", "prefill_b1"):
             res = run_prefill(args, dist)
         elif args.workload == "prefill_attn":
             res = run_prefill_attn(args, dist)

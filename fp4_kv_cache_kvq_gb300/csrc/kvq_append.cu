@@ -58,7 +58,7 @@ template <int D, bool NV>
 __global__ void __launch_bounds__(256, kAppendMinCtas) append_fp4_kernel(const kvq_cache c, int32_t b_begin, uint32_t k_items,
                                                          uint32_t v_items, uint32_t k_ctas, DivU32 div_hkv,
                                                          DivU32 div_k_per, DivU32 div_v_per, int32_t n_new,
-                                                         const int32_t* __restrict__ start_pos,
+                                                         const int32_t* __restrict__ start_pos, int32_t sp_offset,
                                                          const uint16_t* __restrict__ k,
                                                          const uint16_t* __restrict__ v, int32_t* flag) {
   constexpr int NB = D / 16;
@@ -76,9 +76,11 @@ __global__ void __launch_bounds__(256, kAppendMinCtas) append_fp4_kernel(const k
   const uint32_t bq = (is_k ? div_k_per : div_v_per).div(r2);
   const uint32_t t = r2 - bq * per;
   const int b = b_begin + (int)bq;
-  const int32_t sp = __ldg(start_pos + b);
+  // sp_offset -1: start_pos holds lengths that include the one new token
+  // (the decode step's append); a zero length appends nothing
+  const int32_t sp = __ldg(start_pos + b) + sp_offset;
   if (sp < 0) {
-    if (is_k) set_flag(flag, KVQ_FLAG_BAD_LENGTH);
+    if (is_k && sp < sp_offset) set_flag(flag, KVQ_FLAG_BAD_LENGTH);
     return;
   }
   // first position handled by this item (K: the token, V: the pair's even token)
@@ -89,6 +91,9 @@ __global__ void __launch_bounds__(256, kAppendMinCtas) append_fp4_kernel(const k
   uint8_t* grp = fp4_group<D>(c, b, pos, h, ls, flag);
   if (grp == nullptr) return;
   const int64_t row = (int64_t)b * n_new;  // first input row of sequence b
+  // (bounds-checked build: the item's input rows lie inside this launch's
+  // batch x n_new rows)
+  if (!KVQ_IN(t < (uint32_t)n_new && (is_k || (pos - sp >= -1 && pos + 1 - sp <= n_new)), flag)) return;
   if (is_k) {
     append_k_item<D, NV>(c, grp, ls, h, j0, k + ((row + t) * hkv + h) * D + 16 * j0, flag);
     return;
@@ -189,6 +194,56 @@ __global__ void __launch_bounds__(256) fp8_scales_kernel(const kvq_cache c, int6
 
 using namespace kvq;
 
+namespace kvq {
+
+// The FP4 / NVFP4 append launches of kvq_append (n_new tokens per sequence
+// from start_pos[b] + sp_offset), shared with kvq_append_decode_attn's
+// separate-append path (n_new 1, start_pos the lengths, sp_offset -1).
+kvq_status launch_fp4_append(const kvq_cache* cache, int32_t batch, int32_t n_new, const int32_t* d_start_pos,
+                             int32_t sp_offset, const uint16_t* k16, const uint16_t* v16, int32_t* d_err_flag,
+                             cudaStream_t s) {
+  const bool nv = cache->format == KVQ_FORMAT_NVFP4;
+  // 32-bit item indices: one sequence's items must fit, the batch is split.
+  const int64_t nqk = cache->head_dim / 16 / kAppendBlocksK;  // items per (token, head)
+  const int64_t nqv = cache->head_dim / 16 / kAppendBlocksV;
+  const int64_t per_seq = (int64_t)n_new * cache->num_kv_heads * nqk;
+  const int64_t limit = (int64_t)1 << 30;
+  if ((int64_t)n_new * cache->num_kv_heads * (cache->head_dim / 16) > limit) return KVQ_ERR_UNSUPPORTED;
+  const int64_t chunk = limit / per_seq;
+  for (int64_t b0 = 0; b0 < batch; b0 += chunk) {
+    const int64_t bc = (batch - b0 < chunk) ? batch - b0 : chunk;
+    const uint32_t k_items = (uint32_t)(bc * per_seq);
+    const uint32_t v_items = (uint32_t)(bc * (n_new / 2 + 1) * cache->num_kv_heads * nqv);
+    const uint32_t k_ctas = (k_items + 255u) / 256u;
+    const uint32_t grid = k_ctas + (v_items + 255u) / 256u;
+    const DivU32 dh = DivU32::make((uint32_t)cache->num_kv_heads);
+    const DivU32 dk = DivU32::make((uint32_t)n_new);
+    const DivU32 dv = DivU32::make((uint32_t)(n_new / 2 + 1));
+    switch (cache->head_dim) {
+      case 64:
+        (nv ? append_fp4_kernel<64, true> : append_fp4_kernel<64, false>)<<<grid, 256, 0, s>>>(
+            *cache, (int32_t)b0, k_items, v_items, k_ctas, dh, dk, dv, n_new, d_start_pos, sp_offset, k16, v16,
+            d_err_flag);
+        break;
+      case 128:
+        (nv ? append_fp4_kernel<128, true> : append_fp4_kernel<128, false>)<<<grid, 256, 0, s>>>(
+            *cache, (int32_t)b0, k_items, v_items, k_ctas, dh, dk, dv, n_new, d_start_pos, sp_offset, k16, v16,
+            d_err_flag);
+        break;
+      default:
+        (nv ? append_fp4_kernel<256, true> : append_fp4_kernel<256, false>)<<<grid, 256, 0, s>>>(
+            *cache, (int32_t)b0, k_items, v_items, k_ctas, dh, dk, dv, n_new, d_start_pos, sp_offset, k16, v16,
+            d_err_flag);
+        break;
+    }
+    const kvq_status ls = launch_status();
+    if (ls != KVQ_OK) return ls;
+  }
+  return KVQ_OK;
+}
+
+}  // namespace kvq
+
 extern "C" kvq_status kvq_append(const kvq_cache* cache, int32_t batch, int32_t n_new, const int32_t* d_start_pos,
                                  const void* k, const void* v, int32_t* d_err_flag, kvq_stream stream) {
   if (batch < 0 || n_new < 0) return KVQ_ERR_INVALID_ARGUMENT;
@@ -200,46 +255,7 @@ extern "C" kvq_status kvq_append(const kvq_cache* cache, int32_t batch, int32_t 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const uint16_t* k16 = static_cast<const uint16_t*>(k);
   const uint16_t* v16 = static_cast<const uint16_t*>(v);
-  if (is_fp4_layout(cache)) {
-    const bool nv = cache->format == KVQ_FORMAT_NVFP4;
-    // 32-bit item indices: one sequence's items must fit, the batch is split.
-    const int64_t nqk = cache->head_dim / 16 / kAppendBlocksK;  // items per (token, head)
-    const int64_t nqv = cache->head_dim / 16 / kAppendBlocksV;
-    const int64_t per_seq = (int64_t)n_new * cache->num_kv_heads * nqk;
-    const int64_t limit = (int64_t)1 << 30;
-    if ((int64_t)n_new * cache->num_kv_heads * (cache->head_dim / 16) > limit) return KVQ_ERR_UNSUPPORTED;
-    const int64_t chunk = limit / per_seq;
-    for (int64_t b0 = 0; b0 < batch; b0 += chunk) {
-      const int64_t bc = (batch - b0 < chunk) ? batch - b0 : chunk;
-      const uint32_t k_items = (uint32_t)(bc * per_seq);
-      const uint32_t v_items = (uint32_t)(bc * (n_new / 2 + 1) * cache->num_kv_heads * nqv);
-      const uint32_t k_ctas = (k_items + 255u) / 256u;
-      const uint32_t grid = k_ctas + (v_items + 255u) / 256u;
-      const DivU32 dh = DivU32::make((uint32_t)cache->num_kv_heads);
-      const DivU32 dk = DivU32::make((uint32_t)n_new);
-      const DivU32 dv = DivU32::make((uint32_t)(n_new / 2 + 1));
-      switch (cache->head_dim) {
-        case 64:
-          (nv ? append_fp4_kernel<64, true> : append_fp4_kernel<64, false>)<<<grid, 256, 0, s>>>(
-              *cache, (int32_t)b0, k_items, v_items, k_ctas, dh, dk, dv, n_new,
-                                                     d_start_pos, k16, v16, d_err_flag);
-          break;
-        case 128:
-          (nv ? append_fp4_kernel<128, true> : append_fp4_kernel<128, false>)<<<grid, 256, 0, s>>>(
-              *cache, (int32_t)b0, k_items, v_items, k_ctas, dh, dk, dv, n_new,
-                                                      d_start_pos, k16, v16, d_err_flag);
-          break;
-        default:
-          (nv ? append_fp4_kernel<256, true> : append_fp4_kernel<256, false>)<<<grid, 256, 0, s>>>(
-              *cache, (int32_t)b0, k_items, v_items, k_ctas, dh, dk, dv, n_new,
-                                                      d_start_pos, k16, v16, d_err_flag);
-          break;
-      }
-      const kvq_status ls = launch_status();
-      if (ls != KVQ_OK) return ls;
-    }
-    return KVQ_OK;
-  }
+  if (is_fp4_layout(cache)) return launch_fp4_append(cache, batch, n_new, d_start_pos, 0, k16, v16, d_err_flag, s);
   const int64_t work = (int64_t)batch * n_new * cache->num_kv_heads * (cache->head_dim / 16);
   append_fp8_kernel<<<grid_for(work, 256), 256, 0, s>>>(*cache, batch, n_new, d_start_pos, k16, v16, d_err_flag);
   return launch_status();

@@ -240,8 +240,12 @@ __device__ __forceinline__ uint8_t* fp4_group(const kvq_cache& c, int b, int64_t
   }
   const int64_t group_bytes = (int64_t)G * (9 * D / 8);
   ls = slot & (G - 1);
-  return static_cast<uint8_t*>(c.data) +
-         (((int64_t)phys * c.num_kv_heads + h) * (c.page_size >> lg_g) + (slot >> lg_g)) * group_bytes;
+  const int64_t off = (((int64_t)phys * c.num_kv_heads + h) * (c.page_size >> lg_g) + (slot >> lg_g)) * group_bytes;
+  if (!KVQ_IN(h >= 0 && h < c.num_kv_heads && off >= 0 &&
+                  off + group_bytes <= c.num_pages * (int64_t)c.num_kv_heads * c.page_size * (9 * D / 8),
+              flag))
+    return nullptr;
+  return static_cast<uint8_t*>(c.data) + off;
 }
 
 // K item: blocks [j0, j0 + kAppendBlocksK) of one token (src = its bf16 row of

@@ -24,6 +24,21 @@ __device__ __forceinline__ void set_flag(int32_t* flag, int32_t bits) {
   if (flag != nullptr) atomicOr(flag, bits);
 }
 
+// Bounds-checked build (-DKVQ_DEBUG_BOUNDS): KVQ_IN(cond, flag) checks that an
+// index or address range lies inside its buffer before the access; when it
+// does not, it raises KVQ_FLAG_BOUNDS and yields false, and the caller skips
+// the access (no trap).  In a normal build it is the constant true and cond is
+// not evaluated.
+#ifdef KVQ_DEBUG_BOUNDS
+__device__ __forceinline__ bool bounds_ok(bool ok, int32_t* flag) {
+  if (!ok) set_flag(flag, KVQ_FLAG_BOUNDS);
+  return ok;
+}
+#define KVQ_IN(cond, flag) (::kvq::bounds_ok((cond), (flag)))
+#else
+#define KVQ_IN(cond, flag) (true)
+#endif
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -207,6 +222,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   while (true) {
     if (mbar_try_wait_hint(bar, parity, 1000000u)) return true;
     if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// The same wait with an explicit limit in ns (used by the decode kernel's
+// test instantiation, whose limit a test shortens): each poll suspends for at
+// most min(limit, 1 ms), so a limit of a few ns gives up after one poll that
+// finds the phase incomplete.
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint32_t hint = limit_ns < 1000000ull ? (uint32_t)limit_ns : 1000000u;
+  if (mbar_try_wait_hint(bar, parity, hint)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (global_ns() - t0 > limit_ns) return false;
+    if (mbar_try_wait_hint(bar, parity, hint)) return true;
   }
 }
 

@@ -20,7 +20,7 @@ struct DecodeParams {
   const float* k_gscale;  // NVFP4 second-level scales [Hkv] (nullptr: plain FP4)
   const float* v_gscale;
   int64_t num_pages;
-  int32_t batch, hkv, g, hq, page, max_pages, window;
+  int32_t batch, hkv, g, hq, page, max_pages, window, head_dim;
   float qk_log2;  // softmax_scale * log2(e)
   // fused append of each sequence's newest token (position T_b - 1) before
   // the decode reads it (kvq_append_decode_attn); k_new == nullptr: none
@@ -28,12 +28,45 @@ struct DecodeParams {
   const uint16_t* v_new;
   kvq_cache cache;        // the FP4 / NVFP4 cache written
   int32_t nvfp4;
+  uint64_t wait_ns;       // 0, or a test's shortened limit of the mma.sync kernel's work waits (ns)
+  int64_t pool_bytes;     // bytes of the FP4 pool, and partial slots of the workspace (bounds checks)
+  int64_t n_slots;
 };
 
-// The head_dim 128 decode on the tensor cores (kvq_decode_tc.cu): one CTA per
-// SM with three pipelines, i.e. the ranges and partial slots of 3 x (number
-// of SMs) CTAs.
+// The merge of the per-range partials (and of the FP8 window's terms).
+struct MergeParams {
+  const int32_t* lens;
+  const uint16_t* q;
+  const float* part_o;
+  const float* part_ml;
+  const int2* unit_rec;
+  float* out;
+  int32_t* flag;
+  // FP8 window (k8 == nullptr: none)
+  const uint8_t* k8;
+  const uint8_t* v8;
+  const float* k8_scale;
+  const float* v8_scale;
+  int32_t window;
+  int32_t hkv, g, hq, head_dim;
+  float qk_log2;
+  int64_t n_slots;        // partial slots of the workspace, sequences (bounds checks)
+  int32_t batch;
+};
+
+// The decode kernels: mma.sync (kvq_decode_kernel.cuh; head_dim 64 or 128,
+// `ctas` persistent CTAs, three per SM), instantiated with the fixed wait
+// limit (kvq_decode.cu) and with the limit dp.wait_ns (kvq_decode_test_wait.cu,
+// launched only while a test has set one); and the head_dim 128 tcgen05
+// variant (kvq_decode_tc.cu; one CTA per SM with three pipelines, i.e. the
+// ranges and partial slots of 3 x (number of SMs) CTAs; fixed limit only).
+kvq_status launch_decode_mma(const DecodeParams& dp, cudaStream_t s, int ctas);
+kvq_status launch_decode_mma_test_wait(const DecodeParams& dp, cudaStream_t s, int ctas);
 kvq_status launch_decode_tc(const DecodeParams& dp, cudaStream_t s);
+// The merge launch (kvq_merge.cu), a programmatic dependent of the decode
+// launch just enqueued: merge_splits_kernel, or merge_window_kernel when
+// mp.k8 is set.
+kvq_status launch_merge(const MergeParams& mp, int64_t units, cudaStream_t s);
 
 namespace {
 
@@ -41,6 +74,7 @@ constexpr int kChunk = 128;          // tokens per pipeline stage
 constexpr int kNG = 8;  // query rows per kv head held by one tile (G <= 8)
 constexpr float kLazySlack = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxWindow = 1024;  // largest FP8 window the window merge takes
 
 // Compile-time view of one pool group of GT tokens (see Fp4Layout).
 template <int D, int GT>

@@ -71,8 +71,13 @@ __global__ void __launch_bounds__(256) dequant_fp4_kernel(const kvq_cache c, int
         set_flag(flag, KVQ_FLAG_PAGE_OOB);
         ok = false;
       } else {
-        grp = static_cast<const uint8_t*>(c.data) + L.group(phys, Hkv, h, pos % P);
-        ls = (pos % P) % L.G;
+        const int64_t off = L.group(phys, Hkv, h, pos % P);
+        if (KVQ_IN(off >= 0 && off + L.group_bytes <= c.num_pages * (int64_t)Hkv * P * (9 * c.head_dim / 8), flag)) {
+          grp = static_cast<const uint8_t*>(c.data) + off;
+          ls = (pos % P) % L.G;
+        } else {
+          ok = false;
+        }
       }
     }
     if (ok) {

@@ -89,4 +89,11 @@ inline kvq_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
+// kvq_append's FP4 / NVFP4 launches (kvq_append.cu): n_new tokens per
+// sequence from position start_pos[b] + sp_offset; sp_offset -1 reads the
+// lengths of a decode step (a zero length appends nothing).
+kvq_status launch_fp4_append(const kvq_cache* cache, int32_t batch, int32_t n_new, const int32_t* d_start_pos,
+                             int32_t sp_offset, const uint16_t* k16, const uint16_t* v16, int32_t* d_err_flag,
+                             cudaStream_t s);
+
 }  // namespace kvq

@@ -85,6 +85,8 @@ def load() -> ctypes.CDLL:
                                           _P, _P, ctypes.c_size_t, _P, _P]
             L.kvq_decode_attn_tc.restype = ctypes.c_int
             L.kvq_decode_attn_tc.argtypes = L.kvq_decode_attn.argtypes
+            L.kvq_test_set_wait_limit_ns.restype = None
+            L.kvq_test_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
             L.kvq_append_decode_attn.restype = ctypes.c_int
             L.kvq_append_decode_attn.argtypes = [_CP, ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, ctypes.c_float,
                                                  _P, _P, ctypes.c_size_t, _P, _P]

@@ -79,6 +79,8 @@ WORKLOADS = {
                            description="B16 Hkv8 Hq64 d128 FP4 T65536 + FP8 window 128, append 1/step"),
     "prefill": Workload("prefill", 16, 8, 8, 128, context=16384,
                         description="B16 x 16384-token bf16 prefill, Hkv8 d128"),
+    "prefill_b1": Workload("prefill_b1", 1, 8, 8, 128, context=16384,
+                           description="B1 x 16384-token bf16 prefill, Hkv8 d128"),
     "prefill_attn": Workload("prefill_attn", 4, 8, 64, 128, context=16384, chunk=1024,
                              description="B4 Hkv8 Hq64 d128: a 1024-token chunk attending causally over a "
                                          "16384-position FP4 cache (the chunk's own tokens included)"),

@@ -19,8 +19,13 @@
  *
  * Conventions shared by every entry point
  *   - All pointers named d_* or documented as "device" are CUDA device memory
- *     owned by the caller.  The library allocates nothing and keeps no global
- *     state; calls on different streams with disjoint buffers are independent.
+ *     owned by the caller.  The library allocates nothing at call time.  Two
+ *     things are held by the library itself: a fixed 8 MiB device array on
+ *     every device that loads it (the scratch of kvq_decode_attn_noalloc, used
+ *     by that entry point only, whose calls must be serialised -- see its
+ *     comment), and the process-wide wait limit a test can set with
+ *     kvq_test_set_wait_limit_ns.  Apart from kvq_decode_attn_noalloc, calls
+ *     on different streams with disjoint buffers are independent.
  *   - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream).  The return value reports only host-side
  *     argument checks and launch errors:
@@ -105,6 +110,10 @@ typedef enum kvq_status {
                                   outside [0, max_pages_per_seq) */
 #define KVQ_FLAG_TIMEOUT 0x4   /* a bounded wait inside a kernel gave up (~2 s) */
 #define KVQ_FLAG_BAD_LENGTH 0x8 /* a negative sequence length or start position */
+#define KVQ_FLAG_BOUNDS 0x10    /* an index outside its buffer; raised only by a
+                                   bounds-checked build of the library
+                                   (-DKVQ_DEBUG_BOUNDS), which then skips the
+                                   access */
 
 typedef enum kvq_format {
     KVQ_FORMAT_FP4_E2M1_E4M3_G16 = 1,
@@ -225,7 +234,11 @@ kvq_status kvq_decode_attn(const kvq_cache *global, const kvq_cache *swa, int32_
  * exits.  Sizes whose kvq_decode_workspace_bytes exceed 8 MiB are refused with
  * KVQ_ERR_WORKSPACE (nothing is enqueued).  The first call on each device looks
  * up the array's device address (cudaGetSymbolAddress), so make that first call
- * before any stream capture.  The array needs no clearing (each call writes the
+ * before any stream capture.  With CUDA's lazy module loading (the default),
+ * the first libkvq call on a device -- or that address lookup -- is also what
+ * loads the library's device module and reserves its memory, the 8 MiB array
+ * included; a caller that must not allocate on its call path makes one call
+ * (of this entry point, or any libkvq call on that device) during its setup.  The array needs no clearing (each call writes the
  * scratch it reads), but all calls share it: calls whose kernels can overlap on
  * the GPU (different streams, or a second call before the first finished on
  * another stream) race and give wrong results; serialise them on one stream.
@@ -281,6 +294,22 @@ kvq_status kvq_decode_attn_tc(const kvq_cache *global, const kvq_cache *swa, int
                               int32_t num_q_heads, const int32_t *d_seq_lens, const void *q,
                               float softmax_scale, float *out, void *workspace,
                               size_t workspace_bytes, int32_t *d_err_flag, kvq_stream stream);
+
+/*
+ * kvq_test_set_wait_limit_ns -- for tests of the timeout path only: every
+ * bounded wait of the mma.sync decode kernel on its own pipeline (a consumer
+ * waiting for a stage to land, the producer waiting for a free stage) gives
+ * up after `ns` nanoseconds instead of about 2 s, for kvq_decode_attn,
+ * kvq_decode_attn_noalloc and kvq_append_decode_attn calls enqueued after
+ * this one; 0 restores the default.  A wait that gives up sets
+ * KVQ_FLAG_TIMEOUT, the CTA stops consuming, its producer waits (always up to
+ * about 2 s) for the copies it already issued, and the call's output is
+ * undefined.  A non-zero limit selects a separate instantiation of the
+ * kernel that reads the limit at run time; 0 selects the production one,
+ * whose limit is a compile-time constant.  Process-wide; not for production
+ * use.
+ */
+void kvq_test_set_wait_limit_ns(uint64_t ns);
 
 /*
  * kvq_prefill_attn -- attention of a chunk of new query tokens over the FP4 or

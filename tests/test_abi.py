@@ -33,7 +33,8 @@ def test_header_declares_the_boundary():
         "kvq_append", "kvq_append_decode_attn", "kvq_attn_dense", "kvq_decode_attn", "kvq_decode_attn_noalloc", "kvq_decode_attn_tc",
         "kvq_decode_workspace_bytes",
         "kvq_dequant", "kvq_fake_quant", "kvq_fp4_pool_bytes", "kvq_fp8_set_scales", "kvq_prefill_attn",
-        "kvq_status_string", "kvq_swa_replay", "kvq_swa_replay_workspace_bytes", "kvq_version"])
+        "kvq_status_string", "kvq_swa_replay", "kvq_swa_replay_workspace_bytes", "kvq_test_set_wait_limit_ns",
+        "kvq_version"])
 
 
 def test_library_exports_every_declared_function(lib):

@@ -59,6 +59,7 @@ def test_reference_arm_on_tiny_workload(capsys):
 
 
 @pytest.mark.parametrize("workload,metric,unit", [("prefill", "PREFILL_METRIC", "tokens/s"),
+                                                  ("prefill_b1", "PREFILL_METRIC", "tokens/s"),
                                                   ("prefill_attn", "PREFILL_ATTN_METRIC", "query tokens/s")])
 def test_reference_arm_on_prefill_workloads(capsys, workload, metric, unit):
     """The reference arm of the append and chunked-prefill workloads times the

@@ -23,6 +23,7 @@ def _fp4_bytes_per_token(w):
     ("long_context", (32, 8, 64, 128, 32768)),
     ("swa_append", (16, 8, 64, 128, 65536)),
     ("prefill", (16, 8, 8, 128, 16384)),
+    ("prefill_b1", (1, 8, 8, 128, 16384)),
     ("prefill_attn", (4, 8, 64, 128, 16384)),
 ])
 def test_shapes(name, shape):
