@@ -238,8 +238,9 @@ kvq_status kvq_decode_attn(const kvq_cache *global, const kvq_cache *swa, int32_
  * the first libkvq call on a device -- or that address lookup -- is also what
  * loads the library's device module and reserves its memory, the 8 MiB array
  * included; a caller that must not allocate on its call path makes one call
- * (of this entry point, or any libkvq call on that device) during its setup.  The array needs no clearing (each call writes the
- * scratch it reads), but all calls share it: calls whose kernels can overlap on
+ * (of this entry point, or any libkvq call on that device) during its setup.
+ * The array needs no clearing (each call writes the scratch it reads), but
+ * all calls share it: calls whose kernels can overlap on
  * the GPU (different streams, or a second call before the first finished on
  * another stream) race and give wrong results; serialise them on one stream.
  * Allocates nothing and calls no allocating routine.
@@ -256,10 +257,16 @@ kvq_status kvq_decode_attn_noalloc(const kvq_cache *global, const kvq_cache *swa
  * merge).  ("Quantising the KV cache", section "Code": each new K/V row is
  * quantised as it enters the cache, and attention reads it back.)  The codes
  * and scale bytes written equal those of kvq_append (same quantiser, same
- * placement), and the output equals that of kvq_append followed by
- * kvq_decode_attn.  The producer warp of the CTA that reads a sequence's
- * last chunk stores that sequence's new token a few chunks before copying
- * it, so no separate append launch is needed.
+ * placement).  The output is that of kvq_append followed by kvq_decode_attn
+ * with the same products summed in another order: the fused kernel adds each
+ * stage's PV products straight into its fp32 accumulator, so the two differ
+ * by fp32 reassociation only (at most about 3 n 2^-24 max|V^| after n
+ * 128-token stages of one CTA range).  The producer warp of the CTA that
+ * reads a sequence's last chunk stores that sequence's new token a few
+ * chunks before copying it, so no separate append launch is needed.  When
+ * the cache's capacity (max_pages_per_seq * page_size) gives the CTA ranges
+ * fewer than 16 chunks each, the append runs as its own launch before the
+ * decode instead, and the output then equals the two calls' bit for bit.
  *   global       FP4 or NVFP4 cache (head_dim 64 or 128), as kvq_decode_attn.
  *   d_seq_lens   device int32 [batch]: T_b including the new token; T_b == 0
  *                appends nothing and gives a zero output row.
@@ -286,7 +293,7 @@ kvq_status kvq_append_decode_attn(const kvq_cache *global, int32_t batch, int32_
  * arguments, workspace, results (within the decode tolerance) and device flags
  * as kvq_decode_attn; head_dim 64 returns KVQ_ERR_UNSUPPORTED.  It is a
  * measured alternative, not the default: on GB300 at 32k context it runs
- * about 1.5x slower than kvq_decode_attn (the channel split of V^T that
+ * about 1.6x slower than kvq_decode_attn (the channel split of V^T that
  * tensor-memory lanes impose costs more instructions than the tensor-core
  * products save, and the per-stage warpgroup barriers stall).
  */
