@@ -41,7 +41,7 @@ from fp4_kv_cache_kvq_gb300 import workloads  # noqa: E402
 
 METRIC = "decode-attn KV-tokens/s and achieved HBM GB/s (% of ~8 TB/s) on FP4 cache, 1xGB300"
 UNIT = "KV-tokens/s"
-PREROLL_US = 100    # GPU-side wait queued ahead of a timed region
+PREROLL_US = 2000   # GPU-side wait queued ahead of a timed region
 CYCLE = 64          # appended positions cycle through this many slots after the context
 NQ = 8              # distinct query sets cycled through the steps
 FALLBACK_HBM_GBS = 6800.0

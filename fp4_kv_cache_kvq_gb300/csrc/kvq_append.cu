@@ -64,6 +64,9 @@ __global__ void __launch_bounds__(256, kAppendMinCtas) append_fp4_kernel(const k
   constexpr int NB = D / 16;
   constexpr int BK = kAppendBlocksK, BV = kAppendBlocksV;
   constexpr int NQK = NB / BK, NQV = NB / BV;  // items per (token, head) row
+  // a decode launched as a programmatic dependent of this append may be
+  // scheduled now; it waits for this grid before copying any pool bytes
+  grid_launch_dependents();
   const bool is_k = blockIdx.x < k_ctas;
   const uint32_t i = (is_k ? blockIdx.x : blockIdx.x - k_ctas) * 256u + threadIdx.x;
   if (i >= (is_k ? k_items : v_items)) return;

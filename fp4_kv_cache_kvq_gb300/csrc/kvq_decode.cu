@@ -4,8 +4,9 @@
 
 namespace kvq {
 
-kvq_status launch_decode_mma(const DecodeParams& dp, cudaStream_t s, int ctas) {
-  return dp.head_dim == 128 ? launch_decode<128, false>(dp, s, ctas) : launch_decode<64, false>(dp, s, ctas);
+kvq_status launch_decode_mma(const DecodeParams& dp, cudaStream_t s, int ctas, bool after_append) {
+  return dp.head_dim == 128 ? launch_decode<128, false>(dp, s, ctas, after_append)
+                            : launch_decode<64, false>(dp, s, ctas, after_append);
 }
 
 }  // namespace kvq

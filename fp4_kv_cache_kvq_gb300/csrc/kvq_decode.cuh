@@ -60,8 +60,10 @@ struct MergeParams {
 // launched only while a test has set one); and the head_dim 128 tcgen05
 // variant (kvq_decode_tc.cu; one CTA per SM with three pipelines, i.e. the
 // ranges and partial slots of 3 x (number of SMs) CTAs; fixed limit only).
-kvq_status launch_decode_mma(const DecodeParams& dp, cudaStream_t s, int ctas);
-kvq_status launch_decode_mma_test_wait(const DecodeParams& dp, cudaStream_t s, int ctas);
+// `after_append`: launch as a programmatic dependent of the append kernel
+// enqueued just before (the producer waits for it before its first copy).
+kvq_status launch_decode_mma(const DecodeParams& dp, cudaStream_t s, int ctas, bool after_append);
+kvq_status launch_decode_mma_test_wait(const DecodeParams& dp, cudaStream_t s, int ctas, bool after_append);
 kvq_status launch_decode_tc(const DecodeParams& dp, cudaStream_t s);
 // The merge launch (kvq_merge.cu), a programmatic dependent of the decode
 // launch just enqueued: merge_splits_kernel, or merge_window_kernel when

@@ -142,25 +142,30 @@ kvq_status decode_attn(const kvq_cache* global, const kvq_cache* swa, int32_t ba
   dp.v_new = fused ? static_cast<const uint16_t*>(v_new) : nullptr;
   dp.cache = *global;
   dp.nvfp4 = nv ? 1 : 0;
+  bool after_append = false;  // the decode follows its own append launch (small caches)
   if (fused) {
     // The producer warp's appends hide behind a CTA's first copies only when
     // its range is long; with short ranges (judged from the cache's capacity,
     // which the host knows) the append runs as its own launch first -- the
-    // same quantiser, so the same bytes.
+    // same quantiser, so the same bytes -- and the decode is launched as its
+    // programmatic dependent: its CTAs start (barriers, range walk, query
+    // rows) while the append runs, and its producer waits for the append
+    // before the first copy.
     const int64_t cap = (int64_t)global->max_pages_per_seq * global->page_size;
     const int64_t cap_chunks = (int64_t)batch * hkv * ((cap + kChunk - 1) / kChunk);
     if (cap_chunks < (int64_t)kFuseMinChunksPerRange * ctas) {
       st = launch_fp4_append(global, batch, 1, d_seq_lens, -1, dp.k_new, dp.v_new, d_err_flag, s);
       if (st != KVQ_OK) return st;
       dp.k_new = dp.v_new = nullptr;
+      after_append = true;
     }
   }
   if (tcgen05)
     st = launch_decode_tc(dp, s);
   else if (dp.wait_ns != 0)
-    st = launch_decode_mma_test_wait(dp, s, ctas);
+    st = launch_decode_mma_test_wait(dp, s, ctas, after_append);
   else
-    st = launch_decode_mma(dp, s, ctas);
+    st = launch_decode_mma(dp, s, ctas, after_append);
   if (st != KVQ_OK) return st;
 
   MergeParams mp;

@@ -214,6 +214,10 @@ template <int D, int GT, bool FUSED, bool TEST_WAIT>
 __device__ void producer(const DecodeParams& p, Smem<D>& sm, Walker wk, int64_t v1) {
   const int lane = threadIdx.x & 31;
   if (!FUSED && lane != 0) return;
+  // launched as a programmatic dependent of the append kernel (the small-cache
+  // path of kvq_append_decode_attn): the pool bytes are read only after that
+  // grid has finished; otherwise this returns at once
+  grid_dependency_wait();
   uint32_t it = 0;
   if (FUSED) {
     Walker aw = wk;
@@ -677,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 }
 
 template <int D, int GT, bool FUSED, bool TEST_WAIT>
-kvq_status launch_decode_f(const DecodeParams& dp, cudaStream_t s, int ctas) {
+kvq_status launch_decode_f(const DecodeParams& dp, cudaStream_t s, int ctas, bool after_append) {
   const int smem = Geo<D>::kSmemBytes;
   static DeviceOnce attr_set;  // the shared-memory opt-in, once per device
   int dev = 0;
@@ -688,23 +692,38 @@ kvq_status launch_decode_f(const DecodeParams& dp, cudaStream_t s, int ctas) {
       return KVQ_ERR_CUDA;
     attr_set.mark(dev);
   }
-  decode_fp4_kernel<D, GT, FUSED, TEST_WAIT><<<ctas, kThreads, smem, s>>>(dp);
-  return launch_status();
+  if (!after_append) {
+    decode_fp4_kernel<D, GT, FUSED, TEST_WAIT><<<ctas, kThreads, smem, s>>>(dp);
+    return launch_status();
+  }
+  // a programmatic dependent of the append kernel just enqueued
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_fp4_kernel<D, GT, FUSED, TEST_WAIT>, dp) == cudaSuccess ? KVQ_OK
+                                                                                           : KVQ_ERR_CUDA;
 }
 
 template <int D, int GT, bool TEST_WAIT>
-kvq_status launch_decode_g(const DecodeParams& dp, cudaStream_t s, int ctas) {
-  return dp.k_new != nullptr ? launch_decode_f<D, GT, true, TEST_WAIT>(dp, s, ctas)
-                             : launch_decode_f<D, GT, false, TEST_WAIT>(dp, s, ctas);
+kvq_status launch_decode_g(const DecodeParams& dp, cudaStream_t s, int ctas, bool after_append) {
+  return dp.k_new != nullptr ? launch_decode_f<D, GT, true, TEST_WAIT>(dp, s, ctas, after_append)
+                             : launch_decode_f<D, GT, false, TEST_WAIT>(dp, s, ctas, after_append);
 }
 
 template <int D, bool TEST_WAIT>
-kvq_status launch_decode(const DecodeParams& dp, cudaStream_t s, int ctas) {
+kvq_status launch_decode(const DecodeParams& dp, cudaStream_t s, int ctas, bool after_append) {
   switch (dp.page < kChunk ? dp.page : kChunk) {
-    case 16: return launch_decode_g<D, 16, TEST_WAIT>(dp, s, ctas);
-    case 32: return launch_decode_g<D, 32, TEST_WAIT>(dp, s, ctas);
-    case 64: return launch_decode_g<D, 64, TEST_WAIT>(dp, s, ctas);
-    default: return launch_decode_g<D, kChunk, TEST_WAIT>(dp, s, ctas);
+    case 16: return launch_decode_g<D, 16, TEST_WAIT>(dp, s, ctas, after_append);
+    case 32: return launch_decode_g<D, 32, TEST_WAIT>(dp, s, ctas, after_append);
+    case 64: return launch_decode_g<D, 64, TEST_WAIT>(dp, s, ctas, after_append);
+    default: return launch_decode_g<D, kChunk, TEST_WAIT>(dp, s, ctas, after_append);
   }
 }
 
