@@ -52,7 +52,7 @@ DECODE_SRC = tuple(os.path.join(_CSRC, f) for f in ("kvq_decode_kernel.cuh", "kv
 PROFILE = os.path.join(ROOT, "profiles", "decode_fp4_long_context.md")
 APPEND_SRC = tuple(os.path.join(_CSRC, f) for f in ("kvq_append.cu", "kvq_append.cuh", "kvq_common.cuh"))
 APPEND_PROFILE = os.path.join(ROOT, "profiles", "append_fp4_prefill.md")
-PREFILL_SRC = os.path.join(ROOT, "fp4_kv_cache_kvq_gb300", "csrc", "kvq_prefill.cu")
+PREFILL_SRC = tuple(os.path.join(_CSRC, f) for f in ("kvq_prefill.cu", "kvq_tc.cuh", "kvq_common.cuh"))
 PREFILL_PROFILE = os.path.join(ROOT, "profiles", "prefill_fp4_prefill_attn.md")
 
 

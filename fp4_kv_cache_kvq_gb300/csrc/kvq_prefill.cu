@@ -8,32 +8,37 @@
 // positions 0..T - C + i (causal), all read from the FP4 cache.  With many
 // query rows per cache tile the products are dense (unlike decode), so they
 // run on the tensor cores; the cache is dequantised once per tile into shared
-// memory and shared by the CTA's 128 query rows.
+// memory and shared by the CTA's 256 query rows.
 //
-// CTA = the G query heads of one kv head times 128/G consecutive query tokens
-// of one sequence (128 query rows), ten warps in four roles that run as a
+// CTA = the G query heads of one kv head times 256/G consecutive query tokens
+// of one sequence: 256 query rows as two 128-row query tiles (A and B) that
+// share each dequantised cache tile.  Fourteen warps in four roles run as a
 // pipeline over the sequence's 128-position cache tiles:
+//   softmax (2 x 4 warps)  warpgroup X serves query tile X, thread r owns row
+//                       r: per 64-score half of the tile, read from TMEM once,
+//                       the half's max against the lazy reference (raised only
+//                       past +8 in the log2 domain; O rescaled in TMEM then),
+//                       then P = 2^(S - m) as f16 pairs written back over the
+//                       first half of S_X's columns; the causal mask only on
+//                       the diagonal tiles
+//   dequant (4 warps)   K^ [128 pos][d] (one slot) and V^ [d][128 pos] (two
+//                       slots) into shared memory in the tensor core's
+//                       K-major core-matrix layout (f16, E2M1 code times E4M3
+//                       scale; positions past the end 0)
 //   loader (1 thread)   bulk copies of the FP4 tiles, 3 in flight
-//   dequant (4 warps)   K^ [128 pos][d] and V^ [d][128 pos] into shared memory
-//                       in the tensor core's K-major core-matrix layout (f16,
-//                       E2M1 code times E4M3 scale; positions past the end 0),
-//                       2 slots each
-//   MMA (1 thread)      S(j) = Q K^(j)^T     tcgen05.mma M=128 N=128 K=d into
-//                                           one of 3 TMEM S buffers
-//                       O += P(j-1) V^(j-1) tcgen05.mma M=128 N=d K=128, P read
-//                                           from TMEM, O accumulated in TMEM
-//   softmax (4 warps)   thread r owns row r: the tile's row max from TMEM, the
-//                       lazy reference (raised only past +8 in the log2 domain;
-//                       O rescaled in TMEM then), causal mask on the diagonal
-//                       tiles only, P = 2^(S - m) as f16 pairs written back over
-//                       the first half of its S buffer
-// so the tensor cores compute S(j+1) and O += P(j-1) V while the softmax warps
-// work on tile j and the dequantisers on tile j+1.  mbarriers hand each buffer
-// from producer to consumer and back (MMA completions arrive via
-// tcgen05.commit).  Finally O / l (times the NVFP4 value scale) goes to global
-// memory.  Every wait is bounded; a timeout raises the CTA's abort word, every
-// role leaves its loop, copies and MMAs still in flight are waited for
-// (bounded), the TMEM is freed and the timeout flag set.
+//   MMA (1 thread)      S_X(j) = Q_X K^(j)^T   tcgen05.mma M=128 N=128 K=d
+//                       O_X += P_X(j) V^(j)   tcgen05.mma M=128 N=d K=128, P_X
+//                                           read from TMEM, O_X in TMEM
+//                       in the order O_A(j), S_A(j+1), O_B(j), S_B(j+1)
+// mbarriers hand each buffer from producer to consumer and back (MMA
+// completions arrive via tcgen05.commit).  V^ has two slots so that the
+// dequantisation of tile j+1's V^ never waits for tile j's last PV product:
+// with one slot that dequantisation sat between O_B(j) and O_A(j+1) on every
+// tile (2.10 -> 1.78 ms on prefill_attn); K^'s single slot is refilled while
+// the softmax of tile j runs.  Finally O / l (times the NVFP4 value scale)
+// goes to global memory.  Every wait is bounded; a timeout raises the CTA's
+// abort word, every role leaves its loop, copies and MMAs still in flight are
+// waited for (bounded), the TMEM is freed and the timeout flag set.
 #include "kvq_common.cuh"
 #include "kvq_host.cuh"
 #include "kvq_tc.cuh"
@@ -53,7 +58,8 @@ constexpr int kPThreads = 32 * (kMmaWarp + 1);
 constexpr int kOCol = kQTiles * kPTile;  // TMEM: S_X (then P_X) at [128 X, +128), O_X at [256 + 128 X, +d)
 constexpr int kTmemCols = 512;
 constexpr int kFp4Stages = 3;   // FP4 tiles in flight
-constexpr int kKSlots = 2;      // K^ slots (V^ has one)
+constexpr int kKSlots = 1;      // K^ slots (refilled while the softmax runs)
+constexpr int kVSlots = 2;      // V^ slots (see above)
 constexpr float kPSlack = 8.0f;
 constexpr uint32_t kPollNs = 20000;  // suspend hint of a barrier poll
 
@@ -63,9 +69,9 @@ enum : int {
   kBFp4Empty = kBFp4Full + kFp4Stages,  // [kFp4Stages] dequantisers done with the tile (128 arrivals)
   kBKFull = kBFp4Empty + kFp4Stages,    // [kKSlots] K^ slot written (128 arrivals)
   kBKEmpty = kBKFull + kKSlots,         // [kKSlots] both S = Q K^T done reading it (MMA commit)
-  kBVFull = kBKEmpty + kKSlots,         // V^ written
-  kBVEmpty = kBVFull + 1,               // both O += P V done reading it
-  kBSFull = kBVEmpty + 1,               // [kQTiles] S_X in TMEM
+  kBVFull = kBKEmpty + kKSlots,         // [kVSlots] V^ slot written (128 arrivals)
+  kBVEmpty = kBVFull + kVSlots,         // [kVSlots] both O += P V done reading it (MMA commit)
+  kBSFull = kBVEmpty + kVSlots,         // [kQTiles] S_X in TMEM
   kBPFull = kBSFull + kQTiles,          // [kQTiles] P_X in TMEM, O_X rescaled (128 arrivals)
   kBPvDone = kBPFull + kQTiles,         // [kQTiles] O_X += P_X V done (S_X's TMEM free again)
   kNumBars = kBPvDone + kQTiles
@@ -91,8 +97,8 @@ struct PGeo {
   static constexpr int kOpBytes = kPTile * D * 2;         // one query tile, K^ slot or V^ (f16, core layout)
   static constexpr int kQ = 0;                            // Q  [kQTiles][128 rows][D]
   static constexpr int kK = kQ + kQTiles * kOpBytes;      // K^ [kKSlots][128 positions][D]
-  static constexpr int kV = kK + kKSlots * kOpBytes;      // V^ [D channels][128 positions]
-  static constexpr int kStage = kV + kOpBytes;            // FP4 tiles [kFp4Stages]
+  static constexpr int kV = kK + kKSlots * kOpBytes;      // V^ [kVSlots][D channels][128 positions]
+  static constexpr int kStage = kV + kVSlots * kOpBytes;  // FP4 tiles [kFp4Stages]
   static constexpr int kBars = kStage + kFp4Stages * kTileBytes;
   static constexpr int kUsed = kBars + 8 * kNumBars + 8 + 128;  // + TMEM slot, abort word, alignment slack
   // at least half an SM's shared memory, so that one CTA (holding all 512
@@ -347,8 +353,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
       mbar_init(bars + 8 * (kBKFull + i), 32 * kDeqWarps);
       mbar_init(bars + 8 * (kBKEmpty + i), 1);
     }
-    mbar_init(bars + 8 * kBVFull, 32 * kDeqWarps);
-    mbar_init(bars + 8 * kBVEmpty, 1);
+    for (int i = 0; i < kVSlots; ++i) {
+      mbar_init(bars + 8 * (kBVFull + i), 32 * kDeqWarps);
+      mbar_init(bars + 8 * (kBVEmpty + i), 1);
+    }
     for (int i = 0; i < kQTiles; ++i) {
       mbar_init(bars + 8 * (kBSFull + i), 1);
       mbar_init(bars + 8 * (kBPFull + i), 32 * 4);
@@ -539,11 +547,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
       dequant_k<D, GT>(stage, sb + G::kK + slot * G::kOpBytes, valid, dt);
       fence_async_smem();
       mbar_arrive(bars + 8 * (kBKFull + slot));
-      if (j >= 1 && !wwait(bars + 8 * kBVEmpty, (uint32_t)(j - 1) & 1u, abort)) break;
-      dequant_v<D, GT>(stage, sb + G::kV, valid, dt);
+      const int vslot = j % kVSlots;
+      if (j >= kVSlots && !wwait(bars + 8 * (kBVEmpty + vslot), (uint32_t)(j / kVSlots - 1) & 1u, abort)) break;
+      dequant_v<D, GT>(stage, sb + G::kV + vslot * G::kOpBytes, valid, dt);
       mbar_arrive(bars + 8 * (kBFp4Empty + s));
       fence_async_smem();
-      mbar_arrive(bars + 8 * kBVFull);
+      mbar_arrive(bars + 8 * (kBVFull + vslot));
     }
   } else if (warp == kLoadWarp) {
     // ---------------------------------------------------------- bulk copies
@@ -594,12 +603,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
       tc_commit(bars + 8 * kBKEmpty);
     }
     for (int j = 0; j < ntiles && ok; ++j) {
-      if (!(ok = pwait(bars + 8 * kBVFull, (uint32_t)j & 1u, abort))) break;
+      if (!(ok = pwait(bars + 8 * (kBVFull + j % kVSlots), (uint32_t)(j / kVSlots) & 1u, abort))) break;
 #pragma unroll
       for (int x = 0; x < kQTiles; ++x) {
         if (!(ok = pwait(bars + 8 * (kBPFull + x), (uint32_t)j & 1u, abort))) break;
         tc_fence_after();
-        const uint64_t dv = smem_desc(sb + G::kV, (D / 8) * 128, 128);
+        const uint64_t dv = smem_desc(sb + G::kV + (j % kVSlots) * G::kOpBytes, (D / 8) * 128, 128);
 #pragma unroll
         for (int ks = 0; ks < kPTile / 16; ++ks)
           tc_mma_f16_ta(tmem + (uint32_t)(kOCol + x * kPTile), tmem + (uint32_t)(x * kPTile + ks * 8),
@@ -607,7 +616,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_fp4_kernel(const Prefill
         tc_commit(bars + 8 * (kBPvDone + x));
         last_bar = bars + 8 * (kBPvDone + x);
         last_par = (uint32_t)j & 1u;
-        if (x == kQTiles - 1) tc_commit(bars + 8 * kBVEmpty);
+        if (x == kQTiles - 1) tc_commit(bars + 8 * (kBVEmpty + j % kVSlots));
         if (j + 1 < ntiles) {
           const int jn = j + 1;
           if (x == 0 && !(ok = pwait(bars + 8 * (kBKFull + jn % kKSlots), (uint32_t)(jn / kKSlots) & 1u, abort)))
