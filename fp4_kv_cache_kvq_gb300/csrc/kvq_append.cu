@@ -41,8 +41,13 @@ struct DivU32 {
   __device__ __forceinline__ uint32_t div(uint32_t n) const { return (__umulhi(n, mul) + n) >> shift; }
 };
 
-// CTAs per SM the register budget is set for (blocks per item: kvq_append.cuh).
-constexpr int kAppendMinCtas = 4;
+// CTAs per SM the register budget is set for (blocks per item:
+// kvq_append.cuh).  Six CTAs of 256 threads cap the kernel at 40 registers,
+// with a few spilled bytes, but keep 50% more loads in flight than four
+// (63 registers, no spills): measured on the 16 x 16384-token prefill,
+// 258 -> 240 us (FP4) and 312 -> 291 us (NVFP4); eight CTAs (32 registers,
+// 150-250 spilled bytes) ran at 266 us.
+constexpr int kAppendMinCtas = 6;
 
 // Work items, one thread each: one per (sequence, new token, kv head, group
 // of kAppendBlocksK blocks) for K, in the first k_ctas CTAs; then one per
