@@ -482,6 +482,7 @@ def run_gpu(args, dist: Dist):
     torch.cuda.synchronize()
     dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    preroll()  # as for the device-resident timing: the host's first enqueue is not timed as GPU idle
     e0.record()
     copier.wait_stream(compute)
 
@@ -550,9 +551,9 @@ def run_gpu(args, dist: Dist):
                    else f"inputs larger than L2 (FP4 cache {st.cache.nbytes} B vs {l2_bytes} B L2), no flush",
                    "launch": "CUDA graphs (one per step of the cycle: appends, then decode)" if args.graphs
                    else "eager launches",
-                   "timing": f"a {PREROLL_US} us GPU-side wait is queued before the start event (and before "
-                             "the per-call events), so the host's enqueue of the first step from an idle "
-                             "stream is not timed",
+                   "timing": f"a {PREROLL_US} us GPU-side wait is queued before the start events (the "
+                             "device-resident steps, the per-call events and the end-to-end steps), so the "
+                             "host's enqueue of the first step from an idle stream is not timed",
                    "parallelism": f"replicas x{dist.world}",
                    "decode_kernel": "kvq_decode_attn_tc (tcgen05)" if args.decode_kernel == "tcgen05"
                    else "kvq_append_decode_attn (append fused into the mma.sync decode)" if st.fused
