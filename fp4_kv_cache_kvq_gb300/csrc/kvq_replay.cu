@@ -129,6 +129,11 @@ __global__ void __launch_bounds__(D) swa_proj_kernel(const float* __restrict__ x
   const int o = threadIdx.x, lane = o & 31, wp = o >> 5;
   const int m = blockIdx.y;
   stage_matrix<D>(wsm, wt + (size_t)m * D * D, D);  // in flight during the normalisation
+  // the layer's kernels run as a chain of programmatic dependents: this one
+  // reads x (and overwrites q, k, v) only once the previous kernel has
+  // finished; the weights, transposed before the chain started, are staged
+  // before that
+  grid_dependency_wait();
   const int64_t i0 = (int64_t)blockIdx.x * kProjPos;
   float xv[kProjPos];
 #pragma unroll
@@ -216,6 +221,7 @@ __global__ void __launch_bounds__(kAttnThreads) swa_attn_kernel(float* __restric
   float* sums = as + D * P;                     // [P]
   float* wos = sums + P;                        // [D][D]: wos[c * D + o] = Wo[o][c]
   stage_matrix<D>(wos, wot, kAttnThreads);      // in flight until the Wo phase
+  grid_dependency_wait();                       // see swa_proj_kernel
   const int tid = threadIdx.x, lane = tid & 31, p = tid >> 5;
   const int64_t i0 = (int64_t)blockIdx.x * P;
   const int64_t i = i0 + p;  // this warp's position
@@ -342,13 +348,31 @@ kvq_status run_replay(const float* w, int layers, const float* emb, int64_t n, i
   const dim3 proj_grid((unsigned)((n + kProjPos - 1) / kProjPos), 3);
   const unsigned attn_grid = (unsigned)((n + kAttnPos - 1) / kAttnPos);
   const int attn_smem = attn_smem_floats(D, n_win) * (int)sizeof(float);
+  // every kernel after the first is a programmatic dependent of the one
+  // before it (the first follows the copy of the embeddings)
+  auto launch = [&](auto kernel, dim3 grid, dim3 block, size_t smem, bool dependent, auto... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+  };
   for (int l = 0; l < layers; ++l) {
     const float* wl = wt + (size_t)4 * l * D * D;
     float* st_k = states + (size_t)(2 * l) * n_win * D;
     float* st_v = states + (size_t)(2 * l + 1) * n_win * D;
-    swa_proj_kernel<D><<<proj_grid, D, D * D * sizeof(float), st>>>(xb, wl, qb, kb, vb, st_k, st_v, n, n_win);
-    swa_attn_kernel<D><<<attn_grid, kAttnThreads, attn_smem, st>>>(xb, qb, kb, vb, wl + (size_t)3 * D * D, n,
-                                                                   n_win, scale);
+    if (launch(swa_proj_kernel<D>, proj_grid, dim3(D), D * D * sizeof(float), l > 0, (const float*)xb, wl, qb, kb,
+               vb, st_k, st_v, n, n_win) != cudaSuccess ||
+        launch(swa_attn_kernel<D>, dim3(attn_grid), dim3(kAttnThreads), (size_t)attn_smem, true, xb,
+               (const float*)qb, (const float*)kb, (const float*)vb, wl + (size_t)3 * D * D, n, n_win, scale) !=
+            cudaSuccess)
+      return KVQ_ERR_CUDA;
   }
   if (hidden != nullptr &&
       cudaMemcpyAsync(hidden, xb, (size_t)n * D * sizeof(float), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
