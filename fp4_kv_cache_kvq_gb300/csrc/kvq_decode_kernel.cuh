@@ -620,9 +620,14 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   int64_t total, v0, v1;
   Walker wk;
-  // the merge grid (launched as a programmatic dependent) may be scheduled
-  // now; it waits for this grid's results before reading them
-  grid_launch_dependents();
+  // The merge grid is launched as a programmatic dependent and waits for
+  // this grid's results before reading them.  With an FP8 window it has
+  // work of its own (the window's scores and PV products) that overlaps
+  // this grid's tail only if it is released now: swa_append 222.9 -> 215.3
+  // us.  Without a window it has nothing to do before the wait, and
+  // releasing it at each CTA's exit instead is faster: long_context's fused
+  // step 211.3 -> 209.6 us.
+  if (p.window > 0) grid_launch_dependents();
   plan(p, blockIdx.x, gridDim.x, total, v0, v1, wk);
   if (v0 >= v1) return;
 
