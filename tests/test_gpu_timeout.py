@@ -23,12 +23,16 @@ def lib():
     return ensure_built()
 
 
-@pytest.mark.parametrize("fused", [False, True])
-def test_short_wait_limit_times_out_and_returns(lib, fused):
-    # about 36 chunks per CTA range: every producer reaches its fourth stage and
-    # waits for the consumers to free one
-    w = workloads.scaled(workloads.WORKLOADS["long_context"], batch=8, context=65536, k_outlier_channels=())
-    lens = [65536] * 8
+@pytest.mark.parametrize("fused,context", [(False, 65536), (True, 65536), (True, 8192)])
+def test_short_wait_limit_times_out_and_returns(lib, fused, context):
+    # 65536 positions: about 36 chunks per CTA range, so every producer reaches
+    # its fourth stage and waits for the consumers to free one, and
+    # kvq_append_decode_attn fuses the append into the decode kernel.  8192
+    # positions: about 9 chunks per range, under the capacity at which it
+    # fuses, so it launches the append kernel and the decode as its
+    # programmatic dependent
+    w = workloads.scaled(workloads.WORKLOADS["long_context"], batch=8, context=context, k_outlier_channels=())
+    lens = [context] * 8
     built = build_fp4(w, lens, seed=11, reserve=1, keep_kv=False)
     q = workloads.queries(w, seed=11, device="cuda")
     scale = 1.0 / math.sqrt(w.head_dim)
