@@ -9,8 +9,9 @@
 // the sign of every value kept in its nibble.  Finite blocks take a
 // division-free path whose codes equal those of the IEEE divisions
 // (reciprocal quotient plus one exact residual correction, argued at
-// block_quotient); blocks holding Inf or NaN take the plain IEEE-division
-// quantiser.
+// block_quotient; for the codes the reciprocal of the block scale may be the
+// hardware's approximate one, argued at scale_recip); blocks holding Inf or
+// NaN take the plain IEEE-division quantiser.
 #pragma once
 
 #include "kvq_common.cuh"
@@ -33,6 +34,19 @@ namespace {
 __device__ __forceinline__ float block_quotient(float x, float s, float r) {
   const float q = __fmul_rn(x, r);
   return __fmaf_rn(-__fmaf_rn(q, s, -x), r, q);
+}
+
+// The reciprocal of a block scale for block_quotient on bf16 values: the
+// hardware's approximate reciprocal.  The E2M1 code of the corrected quotient
+// is that of x / s for any r within two ulps of RN(1/s) (checked on the host
+// for every E4M3 scale, every such r and every bf16 value the block can
+// hold); on a midpoint x = tau * s the residual stays exact and the
+// correction lands on tau, off one the quotient stays on its side.  s is a
+// normal fp32 value in [2^-9, 448], so the flush-to-zero form is exact.
+__device__ __forceinline__ float scale_recip(float s) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(s));
+  return r;
 }
 
 // Four pairs of fp32 values to four E2M1 byte pairs (saturating RNE, sign
@@ -293,7 +307,7 @@ __device__ __forceinline__ void append_k_item(const kvq_cache& c, uint8_t* grp, 
       if (kb[jb].finite) {
         sb = block_scale_byte(kb[jb].amax);
         const float s = e4m3_to_f32(sb);
-        q = k_codes_finite(kb[jb].w, s, __frcp_rn(s));
+        q = k_codes_finite(kb[jb].w, s, scale_recip(s));
       } else {
         set_flag(flag, KVQ_FLAG_NONFINITE);
         const uint4 r4 = quantize_plain(src + 16 * jb, 1.0f);
@@ -366,7 +380,7 @@ __device__ __forceinline__ void append_v_item(const kvq_cache& c, uint8_t* grp, 
       sb0 = block_scale_byte(vb[0][jb].amax);
       sb1 = block_scale_byte(vb[1][jb].amax);
       const float s0 = e4m3_to_f32(sb0), s1 = e4m3_to_f32(sb1);
-      codes = v_pair_codes_finite(vb[0][jb].w, s0, __frcp_rn(s0), vb[1][jb].w, s1, __frcp_rn(s1));
+      codes = v_pair_codes_finite(vb[0][jb].w, s0, scale_recip(s0), vb[1][jb].w, s1, scale_recip(s1));
     } else if (NV && nv_fast_scale(S) && nv_quotients(vb[0][jb], S, __frcp_rn(S), y0, sb0) &&
                nv_quotients(vb[1][jb], S, __frcp_rn(S), y1, sb1)) {
       const float s0 = e4m3_to_f32(sb0), s1 = e4m3_to_f32(sb1);

@@ -193,6 +193,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// Non-blocking test of a phase (no suspension at all).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
@@ -226,16 +237,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 }
 
 // The same wait with an explicit limit in ns (used by the decode kernel's
-// test instantiation, whose limit a test shortens): each poll suspends for at
-// most min(limit, 1 ms), so a limit of a few ns gives up after one poll that
-// finds the phase incomplete.
+// test instantiation, whose limit a test shortens).  A limit under 1 ms polls
+// with the non-blocking test, so a phase that is not complete at the first
+// test gives up after the limit (a suspending try_wait may itself wait for a
+// hardware-chosen time and hide a short limit); longer limits poll like
+// mbar_wait.
 __device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  const uint32_t hint = limit_ns < 1000000ull ? (uint32_t)limit_ns : 1000000u;
-  if (mbar_try_wait_hint(bar, parity, hint)) return true;
+  const bool short_limit = limit_ns < 1000000ull;
+  if (short_limit ? mbar_test_wait(bar, parity) : mbar_try_wait_hint(bar, parity, 1000000u)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
     if (global_ns() - t0 > limit_ns) return false;
-    if (mbar_try_wait_hint(bar, parity, hint)) return true;
+    if (short_limit ? mbar_test_wait(bar, parity) : mbar_try_wait_hint(bar, parity, 1000000u)) return true;
   }
 }
 

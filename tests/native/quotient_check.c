@@ -15,6 +15,14 @@
 //      the quotient keeps the sign and stays under 2^-11 (its E2M1 code under
 //      any block scale is the signed zero); where the IEEE quotient
 //      overflows the quotient is not finite either.
+//   4. the FP4 codes with an approximate reciprocal: for every positive
+//      finite E4M3 block scale s (normal and subnormal), every r within two
+//      ulps of RN(1/s) and every finite bf16 x the block could hold (|x| at
+//      most 8 s, any x when s is the saturated 448), the saturating round-to-
+//      nearest-even E2M1 code (sign kept) of the corrected quotient
+//      fma(-fma(q, s, -x), r, q), q = x * r, equals the code of x / s.  (The
+//      value itself may differ from x / s by an ulp; on an E2M1 midpoint it
+//      does not, and off one it stays on the same side.)
 // Exit status 0 when every case matches.
 #include <math.h>
 #include <stdint.h>
@@ -33,6 +41,28 @@ static long check(float y, float s, float r, long* bad, const char* what) {
     ++*bad;
   }
   return 1;
+}
+
+// E2M1 code of v: sign bit 8, magnitude code by the grid's midpoints, ties to
+// the even code, saturating above 6.
+static int e2m1_code(float v) {
+  static const float mid[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
+  const float a = fabsf(v);
+  int c = 0;
+  for (int i = 0; i < 7; ++i) {
+    if (a > mid[i]) {
+      c = i + 1;
+    } else {
+      if (a == mid[i]) c = (i % 2 == 0) ? i : i + 1;
+      break;
+    }
+  }
+  return (signbit(v) ? 8 : 0) | c;
+}
+
+static float e4m3_value(int b) {  // b in 1..0x7E (positive finite)
+  const int e = b >> 3, m = b & 7;
+  return e ? ldexpf(1.0f + m / 8.0f, e - 7) : ldexpf((float)m, -9);
 }
 
 int main(void) {
@@ -82,5 +112,29 @@ int main(void) {
       }
     }
   printf("second-level scale range ends: checked %ld, mismatches %ld\n", total, bad3);
-  return bad != 0 || bad3 != 0;
+  long bad4 = 0;
+  total = 0;
+  for (int b = 1; b <= 0x7E; ++b) {
+    const float s = e4m3_value(b);
+    const uint32_t r0 = u_of(1.0f / s);
+    for (int k = -2; k <= 2; ++k) {
+      const float r = f_of(r0 + (uint32_t)k);
+      for (uint32_t xb = 0; xb < 0x10000u; ++xb) {
+        if ((xb & 0x7F80u) == 0x7F80u) continue;  // Inf and NaN take the IEEE path
+        const float x = f_of(xb << 16);
+        // reachable pairs only: a block's scale s = RNE_e4m3(amax / 6) is at
+        // least amax / 6.4 unless it saturated at 448, so |x| <= 6.4 s
+        if (b != 0x7E && !(fabsf(x) <= 8.0f * s)) continue;
+        const float q = x * r;
+        const float q2 = fmaf(-fmaf(q, s, -x), r, q);
+        ++total;
+        if (e2m1_code(q2) != e2m1_code(x / s)) {
+          if (bad4 < 5) printf("code mismatch s=%a r=%a x=%a q2=%a ref=%a\n", s, r, x, q2, x / s);
+          ++bad4;
+        }
+      }
+    }
+  }
+  printf("approximate reciprocals, e2m1 codes: checked %ld, mismatches %ld\n", total, bad4);
+  return bad != 0 || bad3 != 0 || bad4 != 0;
 }
