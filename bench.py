@@ -956,6 +956,10 @@ def run_swa_replay(args, dist: Dist):
             kvq.swa_replay(w, e, nw, want_hidden=False, workspace=ws, states=states)
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # the same GPU-side wait as the decode workloads: the host enqueues
+        # the first replays while the stream is busy
+        sm_hz = getattr(torch.cuda.get_device_properties(device), "clock_rate", 2.0e6) * 1e3
+        torch.cuda._sleep(int(PREROLL_US * 1e-6 * sm_hz))
         a.record()
         for _ in range(n_steps):
             kvq.swa_replay(w, e, nw, want_hidden=False, workspace=ws, states=states)
