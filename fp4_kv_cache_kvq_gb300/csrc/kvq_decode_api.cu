@@ -2,9 +2,10 @@
 // sizing, kvq_decode_attn, kvq_append_decode_attn (the append fused into
 // the decode launch), kvq_decode_attn_tc and kvq_decode_attn_noalloc.
 // Argument checks run on the host before anything is enqueued; a call
-// enqueues the decode kernel (kvq_decode.cu or kvq_decode_tc.cu), an append
-// launch first when the fused append falls back to one, and the merge
-// (kvq_merge.cu).
+// enqueues the decode kernel (kvq_decode_kernel.cuh, instantiated in
+// kvq_decode.cu, or kvq_decode_tc.cu), preceded by an append launch when the
+// fused append falls back to one (the decode then runs as that launch's
+// programmatic dependent), and the merge (kvq_merge.cu).
 #include "kvq_common.cuh"
 #include "kvq_decode.cuh"
 #include "kvq_host.cuh"
@@ -45,9 +46,10 @@ constexpr int kSmallRangeChunks = 8;
 // capacity (max_pages_per_seq * page_size, which the host knows) would give
 // each of three per SM fewer than kSmallRangeChunks chunks -- then fewer,
 // longer ranges mean fewer per-CTA prologues and fewer partials to merge
-// (gqa_outliers, about 4.6 chunks per range at three per SM: 23.3 -> 21.2 us
-// per call with L2 flushed; one per SM was slower, 25.2 us).  The tcgen05
-// kernel always covers the ranges of three per SM.
+// (gqa_outliers, about 4.6 chunks per range at three per SM: 22.5 -> 20.5 us
+// per call with L2 flushed; one per SM was slower, 23.6 us; at 9 chunks per
+// range the two grids tie, at 18 three per SM wins).  The tcgen05 kernel
+// always covers the ranges of three per SM.
 int grid_ctas(const kvq_cache* c, int64_t batch, int64_t hkv, bool tcgen05) {
   const int full = decode_ctas();
   if (tcgen05 || full <= 0) return full;
