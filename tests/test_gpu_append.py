@@ -4,7 +4,9 @@ Covers the exhaustive sets of the oracle's pins run through the GPU
 quantiser: every finite bf16 amax (scale byte), every reachable (bf16 value,
 E4M3 scale) pair (codes), special blocks (zeros, -0.0, saturation, ties),
 paged layouts with random page tables and ragged start positions, the FP8
-window codes over every finite bf16 value, and the device error flags.
+window codes over every finite bf16 value, the device error flags, and the
+prefill appends at their full sizes in the benchmark's launch (sampled pages
+bit for bit, every scale byte in range).
 """
 import numpy as np
 import pytest
@@ -12,7 +14,7 @@ import torch
 
 import oracle
 from fp4_kv_cache_kvq_gb300 import kvq, workloads
-from tests.helpers import ensure_built, gather_unit_bytes
+from tests.helpers import ensure_built, gather_unit_bytes, unpack_pool_rows
 from tests.test_oracle_formats import all_bf16_as_f32
 
 pytestmark = pytest.mark.gpu
@@ -214,3 +216,54 @@ def test_fp8_set_scales_and_ring_slots():
                 slot = (int(start[b]) + t) % W
                 want, _ = oracle.fp8_quantize(k[b, t, h].float().numpy(), sk)
                 assert np.array_equal(cache.k_codes[b, h, slot].cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("name,nv", [("prefill", False), ("prefill", True), ("prefill_b1", False)])
+def test_prefill_append_full_size_sampled(name, nv):
+    """The benchmark's prefill append (B16 or B1 x 16384 tokens, Hkv 8, d 128,
+    the whole batch in one call) at full size: 26 sampled (sequence, kv head,
+    page) blocks -- the first and last pages among them -- bit for bit
+    against the oracle's quantiser (NVFP4: with the second-level scales,
+    themselves checked against the oracle from each head's amax), and every
+    scale byte of the pool a positive finite E4M3 value (0x01..0x7E)."""
+    w = workloads.WORKLOADS[name]
+    B, T, H, D, P = w.batch, w.context, w.num_kv_heads, w.head_dim, w.page_size
+    max_pages = -(-T // P)
+    cache = kvq.Fp4Cache(H, D, P, B * max_pages, max_pages, device="cuda", nvfp4=nv)
+    k = torch.empty((B, T, H, D), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    for b in range(B):
+        k[b], v[b] = workloads.sequence_kv(w, b, T, seed=0, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if nv:
+        kvq.fp8_set_scales(cache, k, v, err=err)
+    kvq.append(cache, torch.zeros(B, dtype=torch.int32, device="cuda"), k, v, err=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    if nv:
+        Sk, Sv = cache.k_gscale.cpu().numpy(), cache.v_gscale.cpu().numpy()
+        for h in range(H):
+            ak = k[:, :, h].float().abs().amax().item()
+            av = v[:, :, h].float().abs().amax().item()
+            assert Sk[h] == np.float32(oracle.nvfp4_global_scale(np.array([ak], np.float32)))
+            assert Sv[h] == np.float32(oracle.nvfp4_global_scale(np.array([av], np.float32)))
+    G, nb = cache.group, D // 16
+    blocks = cache.pool.reshape(-1, cache.pool.shape[-1])
+    for lo, hi in ((G * D // 2, G * (D // 2 + nb)), (G * (D + nb), blocks.shape[1])):
+        sc = blocks[:, lo:hi]
+        assert int(sc.min().item()) >= 0x01 and int(sc.max().item()) <= 0x7E
+    rng = np.random.default_rng(23)
+    picks = [(0, 0, 0), (B - 1, H - 1, max_pages - 1)]
+    picks += [(int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(max_pages))) for _ in range(24)]
+    for b, h, pg in picks:
+        kc, ks, vc, vs = unpack_pool_rows(cache, [b * max_pages + pg], h, P)
+        xk = k[b, pg * P:(pg + 1) * P, h].float().cpu().numpy()
+        xv = v[b, pg * P:(pg + 1) * P, h].float().cpu().numpy()
+        if nv:
+            okc, oks, _ = oracle.nvfp4_quantize_rows(xk, float(Sk[h]))
+            ovc, ovs, _ = oracle.nvfp4_quantize_rows(xv, float(Sv[h]))
+        else:
+            okc, oks, _ = oracle.quantize_rows(xk)
+            ovc, ovs, _ = oracle.quantize_rows(xv)
+        assert np.array_equal(ks, oks) and np.array_equal(kc, okc), (b, h, pg)
+        assert np.array_equal(vs, ovs) and np.array_equal(vc, ovc), (b, h, pg)
